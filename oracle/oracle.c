@@ -1,0 +1,488 @@
+/*
+ * oracle.c -- plain, slow, single-threaded CPU oracle for the MoE routing +
+ * FP8 quantisation path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file: only the tests, the package smoke check and the bench's CPU
+ * baseline leg use it.  It shares no code, header, table or constant with the
+ * CUDA library, and includes nothing from it.
+ *
+ * Compile: cc -O2 -ffp-contract=off -fPIC -shared oracle.c -o liboracle.so -lm
+ * (no fast-math; -ffp-contract=off so every float operation written below is
+ * rounded on its own, exactly as written).
+ *
+ * Sources it follows (page title and section):
+ *  - "DeepSeek open-sources TileKernels" (itsolotime.com), section 2.1
+ *    "Top-K Gating": pick the k highest expert scores per token, ties going to
+ *    the lower expert index.
+ *  - same page, the routing chain at the top of section 2 ("Top-K Gating ->
+ *    Group Counting -> Token-Expert Mapping -> Fused Expand/Reduce -> Weight
+ *    Normalization"), whose weight formula the page leaves open: read here as
+ *    the softmax over the k selected scores.
+ *  - "CuTeDSL at Perplexity", MoE dispatch/combine (TP=1 local kernel): count
+ *    tokens per expert and give each routed copy a unique index in its
+ *    expert's list; combine accumulates the weighted copies back per token.
+ *  - TileKernels page, section 3.1 (CastOutputConfig: clamp_min_value 1e-4 for
+ *    E4M3), section 3.2 (per_token_cast: group absmax -> scale -> multiply by
+ *    the inverse scale), section 2.2 (expand_to_fused: copy each token and
+ *    its scales to the rows given by pos, pos < 0 meaning "no copy"),
+ *    section 3.3 (SwiGLU: val_l / (1 + exp(-val_l)) * val_r in fp32, then the
+ *    same per-group cast).
+ *  - E4M3FN itself (sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ *    infinities, S.1111.111 = NaN, largest finite 448) comes from the OCP 8-bit
+ *    floating point specification, which the pages name but do not print.
+ *
+ * Return codes of every entry: 0 = ok, 1 = invalid argument, 2 = non-finite or
+ * out-of-range input that the method leaves undefined.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* bf16 and E4M3FN as plain number formats                                   */
+/* ------------------------------------------------------------------------ */
+
+/* A bf16 value is the upper 16 bits of an IEEE binary32; widening is exact. */
+static float bf16_bits_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* The non-negative finite E4M3FN value of a 7-bit magnitude code (0..126).
+ * Exponent field 0: subnormal m * 2^-9.  Otherwise (1 + m/8) * 2^(e-7). */
+double oracle_e4m3_value(int code)
+{
+    int e = (code >> 3) & 0xF;
+    int m = code & 7;
+    if (e == 0)
+        return ldexp((double)m, -9);
+    return ldexp(1.0 + m / 8.0, e - 7);
+}
+
+/* Decode any byte; NaN codes (0x7F, 0xFF) give NaN. */
+double oracle_e4m3_decode(uint8_t c)
+{
+    int mag = c & 0x7F;
+    double v;
+    if (mag == 0x7F)
+        return NAN;
+    v = oracle_e4m3_value(mag);
+    return (c & 0x80) ? -v : v;
+}
+
+static double g_e4m3_table[127];
+static int g_e4m3_table_ready = 0;
+
+static void e4m3_table_init(void)
+{
+    int c;
+    if (g_e4m3_table_ready)
+        return;
+    for (c = 0; c < 127; ++c)
+        g_e4m3_table[c] = oracle_e4m3_value(c);
+    g_e4m3_table_ready = 1;
+}
+
+/* Round v to the nearest E4M3FN value, ties to the even code, and saturate
+ * magnitudes at or beyond 448 (including infinity) to 448 ("satfinite").
+ * The sign bit of v is kept, so -0.0 and negative values that round to zero
+ * give 0x80.  NaN gives the NaN code with v's sign. */
+uint8_t oracle_e4m3_encode(float v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a;
+    int lo, hi, c;
+    double mid;
+
+    e4m3_table_init();
+    if (isnan(v))
+        return (uint8_t)(sign | 0x7F);
+    a = fabs((double)v);
+    if (a >= g_e4m3_table[126])
+        return (uint8_t)(sign | 126);
+    /* largest c with table[c] <= a (table is increasing; table[0] = 0) */
+    lo = 0;
+    hi = 126;
+    while (hi - lo > 1) {
+        int m = (lo + hi) / 2;
+        if (g_e4m3_table[m] <= a)
+            lo = m;
+        else
+            hi = m;
+    }
+    c = lo;
+    /* a lies in [table[c], table[c+1]) */
+    mid = 0.5 * (g_e4m3_table[c] + g_e4m3_table[c + 1]); /* exact: dyadic */
+    if (a < mid)
+        return (uint8_t)(sign | c);
+    if (a > mid)
+        return (uint8_t)(sign | (c + 1));
+    return (uint8_t)(sign | ((c % 2 == 0) ? c : c + 1));
+}
+
+void oracle_e4m3_encode_array(const float *v, int64_t n, uint8_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_encode(v[i]);
+}
+
+/* Round a double to the nearest bf16 (8 significant bits), ties to even,
+ * directly from the double (no intermediate float, so no double rounding).
+ * Returns the 16 bf16 bits. */
+uint16_t oracle_bf16_from_double(double x)
+{
+    double a, q, r, val;
+    int ex;
+    float f;
+    uint32_t u;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+
+    if (isnan(x))
+        return (uint16_t)(sign | 0x7FC0);
+    a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    frexp(a, &ex); /* a in [2^(ex-1), 2^ex) */
+    if (ex - 1 < -126)
+        q = ldexp(1.0, -133); /* subnormal spacing of bf16 */
+    else
+        q = ldexp(1.0, ex - 1 - 7);
+    r = nearbyint(a / q); /* default rounding mode: to nearest, ties even */
+    val = r * q;
+    if (val >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80); /* overflow to infinity */
+    f = (float)val; /* exact: val has at most 8 significant bits */
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (uint16_t)(u >> 16));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 1: top-k gate and top-k weights                                      */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    float score;
+    int32_t expert;
+} scored_expert_t;
+
+/* Descending score; among equal scores the lower expert index first. */
+static int by_score_then_index(const void *pa, const void *pb)
+{
+    const scored_expert_t *a = (const scored_expert_t *)pa;
+    const scored_expert_t *b = (const scored_expert_t *)pb;
+    if (a->score > b->score)
+        return -1;
+    if (a->score < b->score)
+        return 1;
+    return (a->expert < b->expert) ? -1 : (a->expert > b->expert);
+}
+
+/* TileKernels page, section 2.1: for each token the k experts with the
+ * largest scores, in descending score order, ties to the lower index.  Written
+ * as its plain definition: sort all E (score, index) pairs and keep k.
+ *
+ * weights (nullable): softmax over the k selected scores,
+ *   w_j = exp(s_j - s_0) / sum_i exp(s_i - s_0),
+ * evaluated in double and rounded once to fp32.
+ * Scores must not be NaN (rc 2); weights also need finite selected scores. */
+int oracle_topk_gate(const float *scores, int64_t T, int32_t E, int32_t k,
+                     int32_t *topk_idx, float *topk_weights)
+{
+    scored_expert_t *row;
+    int64_t t;
+    int32_t e, j;
+
+    if (T < 0 || E < 1 || k < 1 || k > E)
+        return 1;
+    if (T == 0)
+        return 0;
+    row = (scored_expert_t *)malloc(sizeof(scored_expert_t) * (size_t)E);
+    if (!row)
+        return 1;
+    for (t = 0; t < T; ++t) {
+        for (e = 0; e < E; ++e) {
+            float s = scores[t * E + e];
+            if (isnan(s)) {
+                free(row);
+                return 2;
+            }
+            row[e].score = s;
+            row[e].expert = e;
+        }
+        qsort(row, (size_t)E, sizeof(scored_expert_t), by_score_then_index);
+        for (j = 0; j < k; ++j)
+            topk_idx[t * k + j] = row[j].expert;
+        if (topk_weights) {
+            double s0 = (double)row[0].score;
+            double sum = 0.0;
+            for (j = 0; j < k; ++j) {
+                if (!isfinite(row[j].score)) {
+                    free(row);
+                    return 2;
+                }
+                sum += exp((double)row[j].score - s0);
+            }
+            for (j = 0; j < k; ++j)
+                topk_weights[t * k + j] =
+                    (float)(exp((double)row[j].score - s0) / sum);
+        }
+    }
+    free(row);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 2: token -> expert mapping                                           */
+/* ------------------------------------------------------------------------ */
+
+/* "CuTeDSL at Perplexity", local dispatch: count the routed copies of each
+ * expert, then give every copy a unique slot in its expert's list.  Here the
+ * list order is made stable: copies are visited in (token, slot) row-major
+ * order and each takes the next free slot of its expert, so
+ *   counts[e]      = #{(t,j) : idx[t,j] = e}
+ *   offsets[0] = 0, offsets[e+1] = offsets[e] + counts[e]
+ *   pos[t,j]       = offsets[e] + #{(t',j') before (t,j) : idx[t',j'] = e}
+ *   sorted_src[pos[t,j]] = t*k + j.
+ * An index outside [0, E) is rc 2. */
+int oracle_route_map(const int32_t *topk_idx, int64_t T, int32_t E, int32_t k,
+                     int32_t *counts, int32_t *offsets, int32_t *pos,
+                     int32_t *sorted_src)
+{
+    int64_t R, p;
+    int32_t e;
+    int64_t *cursor;
+
+    if (T < 0 || E < 1 || k < 1)
+        return 1;
+    R = T * (int64_t)k;
+    for (e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (p = 0; p < R; ++p) {
+        int32_t x = topk_idx[p];
+        if (x < 0 || x >= E)
+            return 2;
+        counts[x] += 1;
+    }
+    offsets[0] = 0;
+    for (e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + counts[e];
+    cursor = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+    if (!cursor)
+        return 1;
+    for (p = 0; p < R; ++p) {
+        int32_t x = topk_idx[p];
+        int64_t slot = offsets[x] + cursor[x];
+        cursor[x] += 1;
+        pos[p] = (int32_t)slot;
+        sorted_src[slot] = (int32_t)p;
+    }
+    free(cursor);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The per-group FP8 cast (TileKernels page, sections 3.1 and 3.2)            */
+/* ------------------------------------------------------------------------ */
+
+/* Cast one group of n fp32 values: amax = max |v|; sf = max(amax, 1e-4)/448
+ * in fp32; sf_inv = 1/sf in fp32; q_i = E4M3(v_i * sf_inv).  Returns sf. */
+static float cast_group(const float *v, int n, uint8_t *q)
+{
+    float amax = 0.0f;
+    float clamped, sf, sf_inv;
+    int i;
+
+    for (i = 0; i < n; ++i) {
+        float a = fabsf(v[i]);
+        if (a > amax)
+            amax = a;
+    }
+    clamped = (amax < 1e-4f) ? 1e-4f : amax;
+    sf = clamped / 448.0f;
+    sf_inv = 1.0f / sf;
+    for (i = 0; i < n; ++i) {
+        float scaled = v[i] * sf_inv;
+        q[i] = oracle_e4m3_encode(scaled);
+    }
+    return sf;
+}
+
+/* per_token_cast: x [T, H] bf16 bits -> q [T, H] E4M3 bytes and
+ * sf [T, H/group] fp32, row-major. */
+int oracle_per_token_cast(const uint16_t *x, int64_t T, int32_t H,
+                          int32_t group, uint8_t *q, float *sf)
+{
+    int64_t t;
+    int32_t g, i, G;
+    float *buf;
+
+    if (T < 0 || group < 1 || H < group || H % group != 0)
+        return 1;
+    G = H / group;
+    buf = (float *)malloc(sizeof(float) * (size_t)group);
+    if (!buf)
+        return 1;
+    for (t = 0; t < T; ++t) {
+        for (g = 0; g < G; ++g) {
+            const uint16_t *src = x + t * H + (int64_t)g * group;
+            for (i = 0; i < group; ++i)
+                buf[i] = bf16_bits_to_float(src[i]);
+            sf[t * G + g] = cast_group(buf, group, q + t * H + (int64_t)g * group);
+        }
+    }
+    free(buf);
+    return 0;
+}
+
+/* Step 3 as the page sequences it: per_token_cast of each token row, then
+ * expand_to_fused copies the row's bytes and scales to every row pos[t,j]
+ * (pos < 0: that copy is dropped).  Rows of out that no pos names are left
+ * untouched.  pos >= num_rows is rc 2. */
+int oracle_expand_cast_fp8(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                           const int32_t *pos, int64_t num_rows, int32_t group,
+                           uint8_t *out, float *out_sf)
+{
+    int64_t t;
+    int32_t j, G;
+    uint8_t *qrow;
+    float *sfrow;
+    int rc;
+
+    if (T < 0 || k < 1 || group < 1 || H < group || H % group != 0 || num_rows < 0)
+        return 1;
+    G = H / group;
+    qrow = (uint8_t *)malloc((size_t)H);
+    sfrow = (float *)malloc(sizeof(float) * (size_t)G);
+    if (!qrow || !sfrow) {
+        free(qrow);
+        free(sfrow);
+        return 1;
+    }
+    for (t = 0; t < T; ++t) {
+        rc = oracle_per_token_cast(x + t * H, 1, H, group, qrow, sfrow);
+        if (rc) {
+            free(qrow);
+            free(sfrow);
+            return rc;
+        }
+        for (j = 0; j < k; ++j) {
+            int32_t r = pos[t * k + j];
+            if (r < 0)
+                continue;
+            if (r >= num_rows) {
+                free(qrow);
+                free(sfrow);
+                return 2;
+            }
+            memcpy(out + (int64_t)r * H, qrow, (size_t)H);
+            memcpy(out_sf + (int64_t)r * G, sfrow, sizeof(float) * (size_t)G);
+        }
+    }
+    free(qrow);
+    free(sfrow);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 4: SwiGLU + cast (TileKernels page, section 3.3, plain form)          */
+/* ------------------------------------------------------------------------ */
+
+/* v[r, c] = g / (1 + exp(-g)) * u with g = x[r, c] (left half, "val_l") and
+ * u = x[r, N + c] (right half, "val_r"), each step rounded to fp32 in the
+ * order written; exp is the host C library's expf. */
+int oracle_swiglu_values(const uint16_t *x, int64_t M, int32_t N, float *v)
+{
+    int64_t r;
+    int32_t c;
+    if (M < 0 || N < 1)
+        return 1;
+    for (r = 0; r < M; ++r) {
+        const uint16_t *row = x + r * 2 * (int64_t)N;
+        for (c = 0; c < N; ++c) {
+            float g = bf16_bits_to_float(row[c]);
+            float u = bf16_bits_to_float(row[N + c]);
+            float e = expf(-g);
+            float den = 1.0f + e;
+            float silu = g / den;
+            v[r * N + c] = silu * u;
+        }
+    }
+    return 0;
+}
+
+/* x [M, 2N] bf16 -> q [M, N] E4M3 + sf [M, N/group] fp32. */
+int oracle_swiglu_cast_fp8(const uint16_t *x, int64_t M, int32_t N,
+                           int32_t group, uint8_t *q, float *sf)
+{
+    int64_t r;
+    int32_t g, G;
+    float *v;
+
+    if (M < 0 || group < 1 || N < group || N % group != 0)
+        return 1;
+    G = N / group;
+    v = (float *)malloc(sizeof(float) * (size_t)N);
+    if (!v)
+        return 1;
+    for (r = 0; r < M; ++r) {
+        oracle_swiglu_values(x + r * 2 * (int64_t)N, 1, N, v);
+        for (g = 0; g < G; ++g)
+            sf[r * G + g] = cast_group(v + (int64_t)g * group, group,
+                                       q + r * N + (int64_t)g * group);
+    }
+    free(v);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 5: weighted combine ("CuTeDSL at Perplexity", combine kernel)         */
+/* ------------------------------------------------------------------------ */
+
+/* out[t, c] = sum_j w[t,j] * y[pos[t,j], c], summed in double (each product
+ * of an fp32 and a bf16 is exact in double), then rounded once: to fp32 into
+ * out_f32 and, directly from the double, to bf16 into out_bf16 (either may be
+ * NULL).  pos < 0 drops that copy; pos >= num_rows is rc 2.
+ * abs_sum (nullable) receives sum_j |w y| per element, the scale of the
+ * rounding error any fp32 accumulation can make. */
+int oracle_combine(const uint16_t *y, const float *w, const int32_t *pos,
+                   int64_t T, int32_t H, int32_t k, int64_t num_rows,
+                   float *out_f32, uint16_t *out_bf16, float *abs_sum)
+{
+    int64_t t;
+    int32_t c, j;
+    if (T < 0 || H < 1 || k < 1 || num_rows < 0)
+        return 1;
+    for (t = 0; t < T; ++t) {
+        for (j = 0; j < k; ++j) {
+            int32_t r = pos[t * k + j];
+            if (r >= num_rows)
+                return 2;
+        }
+        for (c = 0; c < H; ++c) {
+            double acc = 0.0, mag = 0.0;
+            for (j = 0; j < k; ++j) {
+                int32_t r = pos[t * k + j];
+                double term;
+                if (r < 0)
+                    continue;
+                term = (double)w[t * k + j] *
+                       (double)bf16_bits_to_float(y[(int64_t)r * H + c]);
+                acc += term;
+                mag += fabs(term);
+            }
+            if (out_f32)
+                out_f32[t * H + c] = (float)acc;
+            if (out_bf16)
+                out_bf16[t * H + c] = oracle_bf16_from_double(acc);
+            if (abs_sum)
+                abs_sum[t * H + c] = (float)mag;
+        }
+    }
+    return 0;
+}
