@@ -1,0 +1,578 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE routing + FP8 hot path on one GB300 (or N, as replicas).
+
+One step is one pass of the whole path over the large-prefill workload
+(T=65536 tokens, E=256 experts, top-8, hidden 7168):
+    topk_gate -> route_map -> expand_cast_fp8 -> swiglu_cast_fp8 -> combine
+The SwiGLU input is [T*k, 2*2048] bf16 (the SwiGLU workload's row shape, one
+row per routed copy) and the combine input y is [T*k, 7168] bf16; both stand
+in for the expert GEMM outputs, which this path does not compute.
+
+`value` is the headline metric: routed tokens (T*k) per second through
+route + expand + cast (topk_gate + route_map + expand_cast_fp8), timed with
+CUDA events inside each step; `ms_per_step` is the whole step.  Inputs are
+resident in HBM before timing; every input tensor but the 67 MB score matrix
+is larger than L2, and the step moves ~19 GB, so nothing is L2-resident when a
+step starts.
+
+--impl reference times the CPU oracle (test infrastructure) on the same
+metric, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "routed tokens/s and achieved HBM GB/s (% of GB300 peak) for route+expand+cast"
+UNIT = "routed tokens/s"
+WORKLOAD = "prefill_64k"
+SWIGLU_N = 2048
+FALLBACK_HBM_GBS = 6800.0
+L2_NOTE = ("inputs larger than L2: x 0.94 GB, SwiGLU input 4.3 GB, y 7.5 GB; the 67 MB score "
+           "matrix is evicted by the ~19 GB each step moves")
+
+
+# ---------------------------------------------------------------- helpers
+
+def algorithmic_bytes(T, E, k, H, N=SWIGLU_N, M=None):
+    """Bytes each op must move (reads + writes), per launch."""
+    R = T * k
+    G = H // 128
+    M = R if M is None else M
+    b = {
+        "topk_gate": T * E * 4 + R * 8,
+        "route_map": R * 4 + R * 8 + (2 * E + 1) * 4,
+        "expand_cast_fp8": T * H * 2 + R * 4 + R * H + R * G * 4,
+        "swiglu_cast_fp8": M * 2 * N * 2 + M * N + M * (N // 128) * 4,
+        "combine": R * H * 2 + R * 4 + R * 4 + T * H * 2,
+    }
+    b["route_expand_cast"] = b["topk_gate"] + b["route_map"] + b["expand_cast_fp8"]
+    return b
+
+
+KERNEL_OF_OP = {  # op -> (kernel name in ncu, source file)
+    "topk_gate": ("topk_gate_kernel", "topk_gate.cu"),
+    "expand_cast_fp8": ("expand_cast_kernel", "expand_cast.cu"),
+    "swiglu_cast_fp8": ("swiglu_cast_kernel", "swiglu_cast.cu"),
+    "combine": ("combine_kernel", "combine.cu"),
+}
+
+
+def source_sha(fname):
+    p = os.path.join(ROOT, "moe_routing_precision_gb300", "csrc", fname)
+    h = hashlib.sha256()
+    for q in (p, os.path.join(ROOT, "moe_routing_precision_gb300", "csrc", "common.cuh")):
+        with open(q, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(op, units_scale=1.0):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if op not in KERNEL_OF_OP or not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(KERNEL_OF_OP[op][0])
+    if not rec or rec.get("source_sha") != source_sha(KERNEL_OF_OP[op][1]):
+        return None
+    return rec["dram_bytes_per_launch"] * units_scale
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        if p.get("hbm_gbs"):
+            return float(p["hbm_gbs"]), "of measured"
+    return FALLBACK_HBM_GBS, "of fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+
+    from moe_routing_precision_gb300 import ops, workloads
+    from moe_routing_precision_gb300._build import build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build()
+    L = ops.lib()
+
+    w = workloads.WORKLOADS[WORKLOAD]
+    T, E, k, H, R, G = w.T, w.E, w.k, w.H, w.R, w.G
+    N = SWIGLU_N
+    # weak scaling: every rank routes its own batch (seed = rank), no collective
+    inp = workloads.make_inputs(w, seed=rank, device=dev, with_y=True, with_swiglu=True,
+                                swiglu_rows=R, swiglu_n=N)
+    scores, x, y, hx = inp["scores"], inp["x"], inp["y"], inp["swiglu_x"]
+    i32 = dict(dtype=torch.int32, device=dev)
+    idx = torch.empty(T, k, **i32)
+    wt = torch.empty(T, k, dtype=torch.float32, device=dev)
+    counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    pos, src = torch.empty(T, k, **i32), torch.empty(R, **i32)
+    ws = torch.empty(max(1, ops.route_map_workspace_bytes(T, E, k)), dtype=torch.uint8, device=dev)
+    q = torch.empty(R, H, dtype=torch.uint8, device=dev)
+    sf = torch.empty(R, G, dtype=torch.float32, device=dev)
+    q2 = torch.empty(R, N, dtype=torch.uint8, device=dev)
+    sf2 = torch.empty(R, N // 128, dtype=torch.float32, device=dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream or None
+
+    def chk(rc, what):
+        if rc != 0:
+            raise ops.MoeError(rc, what)
+
+    def route_expand_cast():
+        chk(L.moe_topk_gate(scores.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
+        chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
+                            pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
+        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
+                                  sf.data_ptr(), 128, sp), "expand")
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        chk(L.moe_topk_gate(scores.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
+        if ev:
+            ev[1].record(stream)
+        chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
+                            pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
+        if ev:
+            ev[2].record(stream)
+        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
+                                  sf.data_ptr(), 128, sp), "expand")
+        if ev:
+            ev[3].record(stream)
+        chk(L.swiglu_cast_fp8(hx.data_ptr(), R, N, q2.data_ptr(), sf2.data_ptr(), 128, sp), "swiglu")
+        if ev:
+            ev[4].record(stream)
+        chk(L.moe_combine(y.data_ptr(), wt.data_ptr(), pos.data_ptr(), T, H, k, R, out.data_ptr(),
+                          0, sp), "combine")
+        if ev:
+            ev[5].record(stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    if L.moe_get_device_status(sp, None) != 0:
+        raise RuntimeError("device error flagged during warm-up")
+
+    # ---- timed region: exactly K steps
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    launches0 = L.moe_kernel_launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t_end.record(stream)
+    barrier()
+    launches = L.moe_kernel_launch_count() - launches0
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    ops_names = ["topk_gate", "route_map", "expand_cast_fp8", "swiglu_cast_fp8", "combine"]
+    per_op = {n: [] for n in ops_names}
+    rec_ms = []
+    for e in evs:
+        for j, n in enumerate(ops_names):
+            per_op[n].append(e[j].elapsed_time(e[j + 1]))
+        rec_ms.append(e[0].elapsed_time(e[3]))
+    if L.moe_get_device_status(sp, None) != 0:
+        raise RuntimeError("device error flagged during the timed region")
+
+    def maxr(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    step_ms = maxr(total_ms / K)
+    rec_ms_mean = maxr(sum(rec_ms) / K)
+    op_ms = {n: maxr(sum(v) / K) for n, v in per_op.items()}
+
+    # ---- e2e: the same metric through the C ABI from pinned host buffers
+    e2e = None
+    if rank == 0 or world > 1:
+        e2e = e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, src,
+                      ws, q, sf, T, E, k, H, R, chk, barrier, maxr)
+
+    # ---- other workloads (their own lines' worth of numbers, L2 flushed)
+    extra = None
+    if rank == 0 and not args.no_extra:
+        extra = extra_workloads(L, dev, stream, sp, chk, args)
+
+    peak_copy = measure_peak_copy(L, dev, stream, sp) if rank == 0 else None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_leg(scores, x, k, E)
+
+    if world > 1:
+        dist.barrier()
+    if rank != 0:
+        dist.destroy_process_group()
+        return None
+
+    peak, peak_src = load_peaks()
+    B = algorithmic_bytes(T, E, k, H, N, R)
+    breakdown = {}
+    for n in ops_names:
+        ms = op_ms[n]
+        gbs = B[n] / (ms * 1e-3) / 1e9
+        breakdown[n] = {"ms": round(ms, 4), "algorithmic_bytes": B[n], "GB_s": round(gbs, 1),
+                        "frac_of_peak": round(gbs / peak, 4)}
+    rec_gbs = B["route_expand_cast"] / (rec_ms_mean * 1e-3) / 1e9
+    breakdown["route_expand_cast"] = {
+        "ms": round(rec_ms_mean, 4), "algorithmic_bytes": B["route_expand_cast"],
+        "GB_s": round(rec_gbs, 1), "frac_of_peak": round(rec_gbs / peak, 4),
+        "tokens_per_s": round(T * world / (rec_ms_mean * 1e-3), 1)}
+    dom = max((n for n in ops_names if n in KERNEL_OF_OP), key=lambda n: op_ms[n])
+    dom_gbs = B[dom] / (op_ms[dom] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": KERNEL_OF_OP[dom][0], "achieved": round(dom_gbs, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
+                "peak_source": peak_src, "traffic": ncu_traffic(dom),
+                "algorithmic_bytes_per_launch": B[dom]}
+    value = R * world / (rec_ms_mean * 1e-3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3",
+        "data": "synthetic (seeded torch.Generator, no dataset)",
+        "config": {"workload": "large prefill T=65536 E=256 k=8 H=7168 (+SwiGLU 2x2048 per routed "
+                               "row, combine y [T*k,H]); value = route+expand+cast",
+                   "T": T, "E": E, "k": k, "H": H, "swiglu_N": N, "seed": "rank",
+                   "parallelism": f"replicas x{world} (token-sharded, no collective)",
+                   "l2": L2_NOTE},
+        "value_scope": "T*k routed tokens / (topk_gate + route_map + expand_cast_fp8 time)",
+        "route_expand_cast_GB_s": round(rec_gbs, 1),
+        "route_expand_cast_frac_of_peak": round(rec_gbs / peak, 4),
+        "step_routed_tokens_per_s": round(R * world / (step_ms * 1e-3), 1),
+        "breakdown": breakdown,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "peak_copy_GB_s": peak_copy,
+        "other_workloads": extra,
+    }
+    return line
+
+
+def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, src, ws, q, sf,
+            T, E, k, H, R, chk, barrier, maxr):
+    """route+expand+cast with the inputs copied from pinned host memory and
+    every output copied back to pinned host memory, all inside the timing."""
+    import torch
+    h_scores = torch.empty_like(scores, device="cpu").pin_memory()
+    h_x = torch.empty_like(x, device="cpu").pin_memory()
+    h_scores.copy_(scores)
+    h_x.copy_(x)
+    outs = [idx, wt, counts, offsets, pos, src, q, sf]
+    h_outs = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    h2d = h_scores.numel() * 4 + h_x.numel() * 2
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    steps = max(3, min(args.steps, args.e2e_steps))
+
+    def one():
+        scores.copy_(h_scores, non_blocking=True)
+        x.copy_(h_x, non_blocking=True)
+        chk(L.moe_topk_gate(scores.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
+        chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
+                            pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
+        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
+                                  sf.data_ptr(), 128, sp), "expand")
+        for h, d in zip(h_outs, outs):
+            h.copy_(d, non_blocking=True)
+
+    one()
+    barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    barrier()
+    ms = maxr(a.elapsed_time(b) / steps)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return {"value": round(R * world / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
+            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "path": "pinned host -> device, C ABI topk_gate/route_map/expand_cast_fp8, "
+                    "all outputs -> pinned host"}
+
+
+def measure_peak_copy(L, dev, stream, sp):
+    import torch
+    n = 1 << 30  # 1 GiB each way
+    a = torch.empty(n, dtype=torch.uint8, device=dev)
+    b = torch.empty(n, dtype=torch.uint8, device=dev)
+    a.fill_(1)
+    best = 0.0
+    for _ in range(3):
+        L.moe_peak_copy(a.data_ptr(), b.data_ptr(), n, sp)
+    for _ in range(10):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        L.moe_peak_copy(a.data_ptr(), b.data_ptr(), n, sp)
+        e1.record(stream)
+        e1.synchronize()
+        best = max(best, 2 * n / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del a, b
+    return round(best, 1)
+
+
+def extra_workloads(L, dev, stream, sp, chk, args):
+    """The skewed-routing and SwiGLU workloads, each iteration after an L2
+    flush (a 512 MB device write outside the timed events)."""
+    import torch
+
+    from moe_routing_precision_gb300 import ops, workloads
+    peak, _ = load_peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    iters = args.extra_iters
+    res = {}
+
+    def timed(fn):
+        ts = []
+        for i in range(iters + 3):
+            flush.fill_(i & 0xFF)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    w = workloads.WORKLOADS["skewed_8k"]
+    inp = workloads.make_inputs(w, seed=0, device=dev)
+    s, x = inp["scores"], inp["x"]
+    T, E, k, H, R, G = w.T, w.E, w.k, w.H, w.R, w.G
+    i32 = dict(dtype=torch.int32, device=dev)
+    idx, wt = torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device=dev)
+    counts, offsets, pos, src = (torch.empty(E, **i32), torch.empty(E + 1, **i32),
+                                 torch.empty(T, k, **i32), torch.empty(R, **i32))
+    ws = torch.empty(max(1, ops.route_map_workspace_bytes(T, E, k)), dtype=torch.uint8, device=dev)
+    q = torch.empty(R, H, dtype=torch.uint8, device=dev)
+    sf = torch.empty(R, G, dtype=torch.float32, device=dev)
+
+    def rec():
+        chk(L.moe_topk_gate(s.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
+        chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
+                            pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
+        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
+                                  sf.data_ptr(), 128, sp), "expand")
+
+    def exp_only():
+        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
+                                  sf.data_ptr(), 128, sp), "expand")
+
+    ms = timed(rec)
+    ms_e = timed(exp_only)
+    B = algorithmic_bytes(T, E, k, H)
+    gbs = B["route_expand_cast"] / (ms * 1e-3) / 1e9
+    gbs_e = B["expand_cast_fp8"] / (ms_e * 1e-3) / 1e9
+    res["skewed_8k"] = {"op": "route+expand+cast", "ms": round(ms, 4),
+                        "routed_tokens_per_s": round(R / (ms * 1e-3), 1),
+                        "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                        "expand_only_ms": round(ms_e, 4), "expand_only_GB_s": round(gbs_e, 1),
+                        "skew": workloads.skew_stats(counts.cpu())}
+    del inp, s, x, q, sf
+    w = workloads.WORKLOADS["swiglu_64k"]
+    hx = workloads.make_inputs(w, seed=0, device=dev)["swiglu_x"]
+    M, N = w.M, w.N
+    q2 = torch.empty(M, N, dtype=torch.uint8, device=dev)
+    sf2 = torch.empty(M, N // 128, dtype=torch.float32, device=dev)
+    ms = timed(lambda: chk(L.swiglu_cast_fp8(hx.data_ptr(), M, N, q2.data_ptr(), sf2.data_ptr(),
+                                             128, sp), "swiglu"))
+    bsw = M * 2 * N * 2 + M * N + M * (N // 128) * 4
+    gbs = bsw / (ms * 1e-3) / 1e9
+    res["swiglu_64k"] = {"op": "swiglu_cast_fp8", "ms": round(ms, 4),
+                         "rows_per_s": round(M / (ms * 1e-3), 1), "GB_s": round(gbs, 1),
+                         "frac_of_peak": round(gbs / peak, 4)}
+    del hx, q2, sf2, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline_leg(scores, x, k, E, tokens=16384):
+    """The oracle as it stands, single-threaded, on the first `tokens` tokens."""
+    import oracle
+    s = scores[:tokens].cpu().numpy()
+    xb = oracle.bf16_bits(x[:tokens].cpu())
+    t0 = time.perf_counter()
+    idx, _ = oracle.topk_gate(s, k)
+    _, _, pos, _ = oracle.route_map(idx, E)
+    oracle.expand_cast_fp8(xb, pos)
+    dt = time.perf_counter() - t0
+    return {"value": round(tokens * k / dt, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {tokens} of 65536 tokens of the large-prefill workload "
+                      f"(topk_gate + route_map + expand_cast_fp8), {dt:.1f} s single-threaded"}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def reference_arm(args):
+    """The oracle timed on the host cores, same metric and workload, each step
+    a bounded sample (2048 tokens) of the large-prefill workload."""
+    import torch
+
+    import oracle
+    from moe_routing_precision_gb300 import workloads
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    oracle.build()
+    w = workloads.WORKLOADS[WORKLOAD]
+    tokens = args.ref_tokens
+    sub = workloads.Workload(w.name, T=tokens, E=w.E, k=w.k, H=w.H, bias=w.bias, x_std=w.x_std)
+    inp = workloads.make_inputs(sub, seed=0, device="cpu")
+    s = inp["scores"].numpy()
+    xb = oracle.bf16_bits(inp["x"])
+
+    def step():
+        idx, _ = oracle.topk_gate(s, w.k)
+        _, _, pos, _ = oracle.route_map(idx, w.E)
+        oracle.expand_cast_fp8(xb, pos)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = tokens * w.k / dt
+    del torch
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 (CPU oracle)", "data": "synthetic",
+        "config": {"workload": f"large prefill T=65536 E=256 k=8 H=7168, bounded sample of "
+                               f"{tokens} tokens per step", "T": tokens, "E": w.E, "k": w.k,
+                   "H": w.H},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{tokens} tokens per step (topk_gate + route_map + "
+                                   f"expand_cast_fp8), single-threaded C"},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--extra-iters", type=int, default=30)
+    ap.add_argument("--ref-tokens", type=int, default=2048)
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = reference_arm(args) if args.impl == "reference" else gpu_arm(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

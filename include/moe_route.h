@@ -1,0 +1,228 @@
+/*
+ * moe_route.h -- C ABI of the GB300 (sm_103a) MoE routing + FP8 quantisation
+ * hot path.
+ *
+ * Five operations, in the order a MoE layer runs them:
+ *
+ *   moe_topk_gate        scores [T,E] f32  -> topk_idx [T,k] i32, topk_weights [T,k] f32
+ *   moe_route_map        topk_idx          -> counts [E], offsets [E+1], pos [T,k], sorted_src [T*k]
+ *   moe_expand_cast_fp8  x [T,H] bf16, pos -> out [R,H] E4M3 bytes, out_sf [R,H/128] f32
+ *   swiglu_cast_fp8      x [M,2N] bf16     -> out [M,N] E4M3 bytes, out_sf [M,N/128] f32
+ *   moe_combine          y [R,H] bf16, topk_weights, pos -> out [T,H] bf16 or f32
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers are DEVICE pointers into memory the caller owns (allocated by the
+ *   caller, e.g. through PyTorch).  The library allocates no device memory and
+ *   keeps no per-call state; a caller-provided workspace is the only scratch.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Every call only enqueues work on it and returns at once; no call
+ *   synchronises except moe_get_device_status.
+ * - Tensors are dense row-major with the shapes given; bf16 is passed as raw
+ *   16-bit patterns, E4M3 (OCP E4M3FN: bias 7, max 448, no infinities) as raw
+ *   bytes.
+ * - Arguments are checked on the host BEFORE anything is launched.  A bad
+ *   argument returns MOE_ERR_INVALID_ARG (or MOE_ERR_UNSUPPORTED for a valid
+ *   but unimplemented option) and launches nothing.  A zero-sized problem
+ *   returns MOE_OK and launches no kernel (moe_route_map with T == 0 still
+ *   zero-fills counts and offsets with cudaMemsetAsync).
+ * - Conditions only the data can reveal (an expert index outside [0,E), a
+ *   pos row outside [0,num_rows)) are not memory errors: the kernel skips the
+ *   offending access, and sets a bit in a device-side error word that
+ *   moe_get_device_status reports and clears.
+ * - A launch failure returns MOE_ERR_CUDA; moe_last_cuda_error_string gives
+ *   the CUDA text.  No C++ exception crosses this boundary.
+ * - Calls on distinct streams may run concurrently; the device error word is
+ *   shared by all of them.
+ * - Inputs must not contain NaN.  Results for NaN inputs are unspecified.
+ *
+ * Sources (page title, section):
+ *   [TK]  "DeepSeek open-sources TileKernels: GPU operators written in Python
+ *         approach hardware limits" (itsolotime.com): 2.1 Top-K Gating,
+ *         2.2 Fused Expand, 3.1 quantisation config, 3.2 per-token cast,
+ *         3.3 SwiGLU + quantisation, and the routing chain opening section 2.
+ *   [PX]  "CuTeDSL at Perplexity" (perplexity.ai blog): MoE dispatch and
+ *         combine, the TP=1 local kernel.
+ */
+#ifndef MOE_ROUTE_H
+#define MOE_ROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ROUTE_ABI_VERSION 1
+
+/* Largest supported expert count and top-k. */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK 32
+/* The only scaling-group size implemented: one fp32 scale per 128 channels. */
+#define MOE_CAST_GROUP 128
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or range       */
+    MOE_ERR_UNSUPPORTED = 2, /* valid request this library does not implement */
+    MOE_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed          */
+    MOE_ERR_DEVICE = 4       /* a kernel flagged bad data (see error bits)    */
+} moe_status_t;
+
+typedef enum moe_weight_mode {
+    MOE_WEIGHTS_NONE = 0,        /* write topk_idx only                         */
+    MOE_WEIGHTS_SOFTMAX_TOPK = 1 /* softmax over the k selected scores          */
+} moe_weight_mode_t;
+
+typedef enum moe_out_dtype {
+    MOE_OUT_BF16 = 0,
+    MOE_OUT_F32 = 1
+} moe_out_dtype_t;
+
+/* Bits of the device error word (moe_get_device_status). */
+#define MOE_DEVERR_EXPERT_RANGE 0x1u /* route_map: topk_idx outside [0, E)      */
+#define MOE_DEVERR_POS_RANGE 0x2u    /* expand/combine: pos >= num_rows         */
+
+/*
+ * moe_topk_gate -- [TK] 2.1 Top-K Gating, plus the "Weight Normalization" that
+ * closes [TK]'s routing chain, read as the softmax over the selected scores.
+ *
+ * For every token t the k experts with the largest scores[t, :], in
+ * descending score order; equal scores go to the lower expert index (so the
+ * result is unique).  -0.0 and +0.0 compare equal; +-inf are ordinary values.
+ *   scores       [T, E] f32, read-only.
+ *   topk_idx     [T, k] i32 out (the page's int64 narrowed: E <= 1024).
+ *   topk_weights [T, k] f32 out, may be NULL when weight_mode is
+ *                MOE_WEIGHTS_NONE; with MOE_WEIGHTS_SOFTMAX_TOPK,
+ *                w[t,j] = exp(s_j - s_0) / sum_i exp(s_i - s_0) over the k
+ *                selected scores s_0 >= s_1 >= ... (fp32, expf); scores must
+ *                be finite.
+ * Requires 1 <= E <= MOE_MAX_EXPERTS, 1 <= k <= min(E, MOE_MAX_TOPK), T >= 0,
+ * scores 4-byte aligned.
+ */
+moe_status_t moe_topk_gate(const float *scores, int64_t num_tokens,
+                           int32_t num_experts, int32_t num_topk,
+                           int32_t *topk_idx, float *topk_weights,
+                           int32_t weight_mode, void *stream);
+
+/*
+ * moe_route_map_workspace_bytes -- device scratch moe_route_map needs for a
+ * problem of this size (a per-chunk histogram, E int32 per 128 tokens,
+ * rounded up to 256 bytes).  0 when num_tokens == 0.  Pure host function.
+ */
+size_t moe_route_map_workspace_bytes(int64_t num_tokens, int32_t num_experts,
+                                     int32_t num_topk);
+
+/*
+ * moe_route_map -- [PX] local dispatch: "count the tokens assigned to each
+ * expert and give each token a unique index in its expert's list", made
+ * stable and deterministic (the page's shared-memory atomics are not):
+ *   counts[e]     = #{(t,j) : topk_idx[t,j] == e}                 [E]   i32
+ *   offsets[e]    = sum_{e' < e} counts[e'], offsets[E] = T*k     [E+1] i32
+ *   pos[t,j]      = offsets[e] + #{(t',j') before (t,j) in row-major
+ *                   order with topk_idx[t',j'] == e}              [T,k] i32
+ *   sorted_src[r] = t*k + j for r = pos[t,j]   (inverse of pos)   [T*k] i32
+ * Rows of one expert are therefore in ascending token order.
+ *   workspace: at least moe_route_map_workspace_bytes(...) bytes of device
+ *   memory, 16-byte aligned; contents on entry are ignored; it is busy until
+ *   the work enqueued on `stream` completes.
+ * An index outside [0, E) sets MOE_DEVERR_EXPERT_RANGE; that copy is not
+ * counted, its pos is -1, and sorted_src keeps holes at its end.
+ * Requires the same E and k limits as moe_topk_gate and T*k < 2^31.
+ */
+moe_status_t moe_route_map(const int32_t *topk_idx, int64_t num_tokens,
+                           int32_t num_experts, int32_t num_topk,
+                           int32_t *counts, int32_t *offsets, int32_t *pos,
+                           int32_t *sorted_src, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
+ * moe_expand_cast_fp8 -- [TK] 3.2 per_token_cast fused with [TK] 2.2
+ * expand_to_fused.  For every token t and 128-channel group g of x[t, :]:
+ *   amax   = max |x| over the group (bf16 widened exactly to f32)
+ *   sf     = max(amax, 1e-4f) / 448   (f32, IEEE round-to-nearest-even;
+ *            1e-4 is [TK] 3.1's E4M3 clamp_min_value)
+ *   sf_inv = 1 / sf                   (f32, IEEE; "multiply by the inverse")
+ *   q      = E4M3(x * sf_inv)         (f32 product, round to nearest even,
+ *            saturating to +-448; the sign of zero is kept)
+ * and for every j with pos[t,j] >= 0 the row of codes goes to
+ * out[pos[t,j], :] and the group scales to out_sf[pos[t,j], :].  pos[t,j] < 0
+ * means "no copy" ([TK] 2.2).  Rows of out no pos names are not written.
+ *   x       [T, H] bf16, 16-byte aligned.      pos [T, k] i32.
+ *   out     [num_rows, H] u8, 16-byte aligned. out_sf [num_rows, H/128] f32.
+ * Requires H % 128 == 0, 1 <= k <= MOE_MAX_TOPK, group == 128 (else
+ * MOE_ERR_UNSUPPORTED).  pos >= num_rows sets MOE_DEVERR_POS_RANGE and is
+ * skipped.
+ */
+moe_status_t moe_expand_cast_fp8(const void *x, int64_t num_tokens,
+                                 int32_t hidden, int32_t num_topk,
+                                 const int32_t *pos, int64_t num_rows,
+                                 uint8_t *out, float *out_sf, int32_t group,
+                                 void *stream);
+
+/*
+ * swiglu_cast_fp8 -- [TK] 3.3, plain form (no clamp, no top-k weight).  For
+ * each row r and channel c < N, in f32:
+ *   g = x[r, c] (left half, the gate), u = x[r, N + c] (right half, up)
+ *   v = g / (1 + exp(-g)) * u
+ * then the per-128-channel cast of moe_expand_cast_fp8 on v.
+ *   x [M, 2N] bf16, 16-byte aligned; out [M, N] u8, 16-byte aligned;
+ *   out_sf [M, N/128] f32.
+ * Requires N % 128 == 0 and group == 128.  exp is CUDA's expf, so v may
+ * differ from a host expf in the last bits.
+ */
+moe_status_t swiglu_cast_fp8(const void *x, int64_t num_rows, int32_t n,
+                             uint8_t *out, float *out_sf, int32_t group,
+                             void *stream);
+
+/*
+ * moe_combine -- [PX] combine: "accumulate in registers using the token
+ * positions, then write the final tokens".  For every token t:
+ *   out[t, c] = sum_{j=0..k-1, pos[t,j] >= 0} topk_weights[t,j] * y[pos[t,j], c]
+ * accumulated in f32 in slot order j = 0..k-1 (fused multiply-add), then
+ * rounded to nearest even bf16 (MOE_OUT_BF16) or kept f32 (MOE_OUT_F32).
+ *   y   [num_rows, H] bf16, 16-byte aligned (the expert outputs in the
+ *       expert-sorted layout moe_route_map produced)
+ *   topk_weights [T, k] f32, pos [T, k] i32
+ *   out [T, H] bf16 or f32, 16-byte aligned
+ * Requires H % 8 == 0.  pos >= num_rows sets MOE_DEVERR_POS_RANGE and that
+ * copy contributes nothing.
+ */
+moe_status_t moe_combine(const void *y, const float *topk_weights,
+                         const int32_t *pos, int64_t num_tokens, int32_t hidden,
+                         int32_t num_topk, int64_t num_rows, void *out,
+                         int32_t out_dtype, void *stream);
+
+/*
+ * moe_peak_copy -- a plain 16-byte vectorised device-to-device copy of
+ * `bytes` bytes (a multiple of 16; both pointers 16-byte aligned), used to
+ * measure the HBM bandwidth the kernels above are held against.
+ */
+moe_status_t moe_peak_copy(const void *src, void *dst, size_t bytes, void *stream);
+
+/*
+ * moe_get_device_status -- synchronises `stream`, then reads and clears the
+ * current device's error word.  Returns MOE_OK when no bit was set,
+ * MOE_ERR_DEVICE when one was (the bits go to *error_bits if non-NULL), or
+ * MOE_ERR_CUDA if synchronising failed.
+ */
+moe_status_t moe_get_device_status(void *stream, uint32_t *error_bits);
+
+/* Static description of a status code (never NULL). */
+const char *moe_status_string(moe_status_t status);
+
+/* Text of the last CUDA error seen by this library on the calling thread. */
+const char *moe_last_cuda_error_string(void);
+
+/* MOE_ROUTE_ABI_VERSION of the loaded library. */
+int32_t moe_abi_version(void);
+
+/* Number of kernels this library has launched in this process so far. */
+uint64_t moe_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTE_H */

@@ -22,10 +22,9 @@ __all__ = ["ops", "workloads", "build"]
 
 
 def __getattr__(name):
+    import importlib
     if name == "ops":
-        from . import ops
-        return ops
+        return importlib.import_module(__name__ + ".ops")
     if name == "build":
-        from ._build import build
-        return build
+        return importlib.import_module(__name__ + "._build").build
     raise AttributeError(name)

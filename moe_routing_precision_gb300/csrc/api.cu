@@ -1,0 +1,221 @@
+// api.cu -- the extern "C" boundary declared in include/moe_route.h: host-side
+// argument checks, per-device launch context, and status reporting.
+//
+// Every entry validates its arguments before touching the GPU; a rejected call
+// launches nothing.  The only device state the library owns is one 32-bit
+// error word per device (a __device__ variable, no allocation).
+#include <atomic>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+__device__ unsigned g_device_error;
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  std::once_flag once;
+  cudaError_t init_status = cudaSuccess;
+  int num_sms = 0;
+  unsigned* err = nullptr;
+};
+DeviceState g_devices[kMaxDevices];
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_last_cuda_error[256] = "no CUDA error";
+
+moe_status_t cuda_fail(cudaError_t e) {
+  snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", cudaGetErrorName(e),
+           cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+// Launch context of the current device: SM count and the address of the
+// error word, looked up once per device.
+moe_status_t context(void* stream, LaunchCtx* ctx) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  DeviceState& d = g_devices[dev];
+  std::call_once(d.once, [&d, dev]() {
+    cudaError_t s = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (s == cudaSuccess) s = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_device_error);
+    d.init_status = s;
+  });
+  if (d.init_status != cudaSuccess) return cuda_fail(d.init_status);
+  ctx->stream = static_cast<cudaStream_t>(stream);
+  ctx->num_sms = d.num_sms;
+  ctx->err = d.err;
+  return MOE_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool experts_ok(int32_t E, int32_t k) {
+  return E >= 1 && E <= MOE_MAX_EXPERTS && k >= 1 && k <= MOE_MAX_TOPK && k <= E;
+}
+
+int64_t route_chunks(int64_t T) { return (T + kRouteChunkTokens - 1) / kRouteChunkTokens; }
+
+}  // namespace
+
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ROUTE_ABI_VERSION; }
+
+uint64_t moe_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* moe_last_cuda_error_string(void) { return g_last_cuda_error; }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: bad pointer, size, alignment or range";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: valid request not implemented";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or launch failed";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE: a kernel flagged out-of-range data";
+  }
+  return "unknown moe_status_t";
+}
+
+moe_status_t moe_topk_gate(const float* scores, int64_t num_tokens, int32_t num_experts,
+                           int32_t num_topk, int32_t* topk_idx, float* topk_weights,
+                           int32_t weight_mode, void* stream) {
+  if (num_tokens < 0 || !experts_ok(num_experts, num_topk)) return MOE_ERR_INVALID_ARG;
+  if (weight_mode != MOE_WEIGHTS_NONE && weight_mode != MOE_WEIGHTS_SOFTMAX_TOPK)
+    return MOE_ERR_INVALID_ARG;
+  if (num_tokens == 0) return MOE_OK;
+  if (!scores || !topk_idx || !aligned(scores, 4) || !aligned(topk_idx, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (weight_mode == MOE_WEIGHTS_SOFTMAX_TOPK && (!topk_weights || !aligned(topk_weights, 4)))
+    return MOE_ERR_INVALID_ARG;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  cudaError_t e = launch_topk_gate(c, scores, num_tokens, num_experts, num_topk, topk_idx,
+                                   weight_mode == MOE_WEIGHTS_SOFTMAX_TOPK ? topk_weights : nullptr);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+size_t moe_route_map_workspace_bytes(int64_t num_tokens, int32_t num_experts, int32_t num_topk) {
+  (void)num_topk;
+  if (num_tokens <= 0 || num_experts < 1) return 0;
+  const size_t bytes = (size_t)route_chunks(num_tokens) * (size_t)num_experts * sizeof(int32_t);
+  return (bytes + 255) / 256 * 256;
+}
+
+moe_status_t moe_route_map(const int32_t* topk_idx, int64_t num_tokens, int32_t num_experts,
+                           int32_t num_topk, int32_t* counts, int32_t* offsets, int32_t* pos,
+                           int32_t* sorted_src, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (num_tokens < 0 || !experts_ok(num_experts, num_topk)) return MOE_ERR_INVALID_ARG;
+  if (num_tokens * (int64_t)num_topk >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (num_tokens == 0) {
+    // nothing routed: counts and offsets are all zero
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * num_experts, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (num_experts + 1), st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+  }
+  if (!topk_idx || !pos || !sorted_src || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_idx, 4) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(pos, 4) ||
+      !aligned(sorted_src, 4) || !aligned(workspace, 16))
+    return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < moe_route_map_workspace_bytes(num_tokens, num_experts, num_topk))
+    return MOE_ERR_INVALID_ARG;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  cudaError_t e = launch_route_map(c, topk_idx, num_tokens, num_experts, num_topk, counts, offsets,
+                                   pos, sorted_src, static_cast<int32_t*>(workspace),
+                                   route_chunks(num_tokens));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status_t moe_expand_cast_fp8(const void* x, int64_t num_tokens, int32_t hidden,
+                                 int32_t num_topk, const int32_t* pos, int64_t num_rows,
+                                 uint8_t* out, float* out_sf, int32_t group, void* stream) {
+  if (group != MOE_CAST_GROUP) return MOE_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || num_rows < 0 || hidden < MOE_CAST_GROUP || hidden % MOE_CAST_GROUP != 0 ||
+      num_topk < 1 || num_topk > MOE_MAX_TOPK)
+    return MOE_ERR_INVALID_ARG;
+  if (num_rows >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
+  if (num_tokens == 0) return MOE_OK;
+  if (!x || !pos || (num_rows > 0 && (!out || !out_sf))) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(pos, 4) || !aligned(out, 16) || !aligned(out_sf, 4))
+    return MOE_ERR_INVALID_ARG;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  cudaError_t e =
+      launch_expand_cast(c, x, num_tokens, hidden, num_topk, pos, num_rows, out, out_sf);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status_t swiglu_cast_fp8(const void* x, int64_t num_rows, int32_t n, uint8_t* out,
+                             float* out_sf, int32_t group, void* stream) {
+  if (group != MOE_CAST_GROUP) return MOE_ERR_UNSUPPORTED;
+  if (num_rows < 0 || n < MOE_CAST_GROUP || n % MOE_CAST_GROUP != 0) return MOE_ERR_INVALID_ARG;
+  if (num_rows == 0) return MOE_OK;
+  if (!x || !out || !out_sf) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(out_sf, 4)) return MOE_ERR_INVALID_ARG;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  cudaError_t e = launch_swiglu_cast(c, x, num_rows, n, out, out_sf);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status_t moe_combine(const void* y, const float* topk_weights, const int32_t* pos,
+                         int64_t num_tokens, int32_t hidden, int32_t num_topk, int64_t num_rows,
+                         void* out, int32_t out_dtype, void* stream) {
+  if (num_tokens < 0 || num_rows < 0 || hidden < 8 || hidden % 8 != 0 || num_topk < 1 ||
+      num_topk > MOE_MAX_TOPK)
+    return MOE_ERR_INVALID_ARG;
+  if (out_dtype != MOE_OUT_BF16 && out_dtype != MOE_OUT_F32) return MOE_ERR_INVALID_ARG;
+  if (num_tokens == 0) return MOE_OK;
+  if (!topk_weights || !pos || !out || (num_rows > 0 && !y)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(y, 16) || !aligned(topk_weights, 4) || !aligned(pos, 4) || !aligned(out, 16))
+    return MOE_ERR_INVALID_ARG;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  cudaError_t e = launch_combine(c, y, topk_weights, pos, num_tokens, hidden, num_topk, num_rows,
+                                 out, out_dtype == MOE_OUT_F32);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status_t moe_peak_copy(const void* src, void* dst, size_t bytes, void* stream) {
+  if (bytes == 0) return MOE_OK;
+  if (!src || !dst || bytes % 16 != 0 || !aligned(src, 16) || !aligned(dst, 16))
+    return MOE_ERR_INVALID_ARG;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  cudaError_t e = launch_peak_copy(c, src, dst, bytes);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status_t moe_get_device_status(void* stream, uint32_t* error_bits) {
+  if (error_bits) *error_bits = 0;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned bits = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&bits, g_device_error, sizeof bits);
+  if (e == cudaSuccess && bits != 0) e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (error_bits) *error_bits = bits;
+  return bits ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+// common.cuh -- device helpers shared by the kernels of the MoE routing + FP8
+// path (sm_103a).  Nothing here is visible across the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "moe_route.h"
+
+namespace moe {
+
+// Scaling constants of the E4M3 per-group cast: the largest finite E4M3FN
+// magnitude and the scale floor ("clamp_min_value" for E4M3 in the TileKernels
+// article, section 3.1).
+constexpr float kE4M3Max = 448.0f;
+constexpr float kScaleFloor = 1e-4f;
+constexpr int kGroup = 128;
+
+// ---------------------------------------------------------------- memory ops
+
+// 16-byte streaming load of data read exactly once: non-coherent path, no L1
+// allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// 16-byte load through the normal cached path (data other CTAs re-read).
+__device__ __forceinline__ uint4 ld_v4(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// 16-byte store of data nobody re-reads in this kernel (evict-first).
+__device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_stream_f32(float* p, float v) {
+  asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// ---------------------------------------------------------------- bf16 / fp8
+
+// The two bf16 values packed in one 32-bit word, widened exactly to f32.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two f32 values -> two E4M3FN codes (round to nearest even, saturate to
+// +-448), `a` in the low byte.  This is the hardware conversion
+// (cvt.rn.satfinite.e4m3x2.f32) reached through the CUDA header intrinsic.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Scale of one group from its absolute maximum (f32, IEEE rounding).
+__device__ __forceinline__ float group_scale(float amax) {
+  return __fdiv_rn(fmaxf(amax, kScaleFloor), kE4M3Max);
+}
+
+// Quantise 16 f32 values with multiplier `inv`, pack the 16 codes.
+__device__ __forceinline__ uint4 quant16(const float (&v)[16], float inv) {
+  uint4 q;
+  q.x = e4m3x2(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv)) |
+        (e4m3x2(__fmul_rn(v[2], inv), __fmul_rn(v[3], inv)) << 16);
+  q.y = e4m3x2(__fmul_rn(v[4], inv), __fmul_rn(v[5], inv)) |
+        (e4m3x2(__fmul_rn(v[6], inv), __fmul_rn(v[7], inv)) << 16);
+  q.z = e4m3x2(__fmul_rn(v[8], inv), __fmul_rn(v[9], inv)) |
+        (e4m3x2(__fmul_rn(v[10], inv), __fmul_rn(v[11], inv)) << 16);
+  q.w = e4m3x2(__fmul_rn(v[12], inv), __fmul_rn(v[13], inv)) |
+        (e4m3x2(__fmul_rn(v[14], inv), __fmul_rn(v[15], inv)) << 16);
+  return q;
+}
+
+// Unpack 16 bf16 (two 16-byte words) to f32.
+__device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float (&v)[16]) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = bf16_lo(w[i]);
+    v[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+
+__device__ __forceinline__ float absmax16(const float (&v)[16]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+  return m;
+}
+
+// Max over the 8 lanes of an aligned 8-lane subgroup.
+__device__ __forceinline__ float max8(float m) {
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  return m;
+}
+
+__device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) {
+  if (err) atomicOr(err, bit);
+}
+
+}  // namespace moe
+
+// ------------------------------------------------------------- launch API
+// Each kernel file exposes one host launcher; api.cu validates and calls it.
+namespace moe {
+struct LaunchCtx {
+  cudaStream_t stream;
+  int num_sms;
+  unsigned* err;  // device error word
+};
+
+cudaError_t launch_topk_gate(const LaunchCtx& c, const float* scores, int64_t T, int E, int k,
+                             int32_t* idx, float* w);
+cudaError_t launch_route_map(const LaunchCtx& c, const int32_t* idx, int64_t T, int E, int k,
+                             int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* sorted_src,
+                             int32_t* ws, int64_t num_chunks);
+cudaError_t launch_expand_cast(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
+                               const int32_t* pos, int64_t R, uint8_t* out, float* out_sf);
+cudaError_t launch_swiglu_cast(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
+                               float* out_sf);
+cudaError_t launch_combine(const LaunchCtx& c, const void* y, const float* w, const int32_t* pos,
+                           int64_t T, int H, int k, int64_t R, void* out, bool out_f32);
+cudaError_t launch_peak_copy(const LaunchCtx& c, const void* src, void* dst, size_t bytes);
+
+// Tokens per route-map chunk (one histogram row of E counters per chunk).
+constexpr int kRouteChunkTokens = 128;
+
+// Kernel launch counter (api.cu).
+void count_launches(int n);
+}  // namespace moe

@@ -1,0 +1,137 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library builds for sm_103a, loads, exports every function the header
+declares with the Python binding's signature, and rejects bad arguments on the
+host before any CUDA call (these calls return before touching a device).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_routing_precision_gb300 import _build
+
+HEADER = os.path.join(_build.INCLUDE, "moe_route.h")
+
+
+@pytest.fixture(scope="session")
+def L():
+    _build.build()
+    from moe_routing_precision_gb300 import ops
+    return ops.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    keywords = {"if", "sizeof", "defined"}
+    return sorted(set(n for n in names if n not in keywords))
+
+
+def test_header_declares_the_five_ops():
+    names = _declared_functions()
+    for op in ("moe_topk_gate", "moe_route_map", "moe_expand_cast_fp8", "swiglu_cast_fp8",
+               "moe_combine"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    from moe_routing_precision_gb300 import ops
+    names = _declared_functions()
+    assert set(names) == set(ops.SIGNATURES), set(names) ^ set(ops.SIGNATURES)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_abi_version_and_status_strings(L):
+    assert L.moe_abi_version() == 1
+    for rc in range(5):
+        assert L.moe_status_string(rc)
+    assert b"unknown" in L.moe_status_string(99)
+
+
+def test_workspace_size(L):
+    assert L.moe_route_map_workspace_bytes(0, 256, 8) == 0
+    assert L.moe_route_map_workspace_bytes(1, 256, 8) == 1024
+    assert L.moe_route_map_workspace_bytes(65536, 256, 8) == 512 * 256 * 4
+    assert L.moe_route_map_workspace_bytes(129, 16, 2) % 256 == 0
+
+
+FAKE = 0x10000  # never dereferenced: every call below is rejected on the host
+INVALID, UNSUPPORTED = 1, 2
+
+
+def test_topk_gate_rejects_bad_arguments(L):
+    f = L.moe_topk_gate
+    assert f(FAKE, 4, 0, 1, FAKE, FAKE, 1, None) == INVALID          # E = 0
+    assert f(FAKE, 4, 1025, 1, FAKE, FAKE, 1, None) == INVALID       # E > max
+    assert f(FAKE, 4, 16, 17, FAKE, FAKE, 1, None) == INVALID        # k > E
+    assert f(FAKE, 4, 64, 33, FAKE, FAKE, 1, None) == INVALID        # k > 32
+    assert f(FAKE, 4, 16, 0, FAKE, FAKE, 1, None) == INVALID         # k = 0
+    assert f(FAKE, -1, 16, 2, FAKE, FAKE, 1, None) == INVALID        # T < 0
+    assert f(None, 4, 16, 2, FAKE, FAKE, 1, None) == INVALID         # null scores
+    assert f(FAKE, 4, 16, 2, FAKE, None, 1, None) == INVALID         # null weights
+    assert f(FAKE + 2, 4, 16, 2, FAKE, FAKE, 1, None) == INVALID     # misaligned
+    assert f(FAKE, 4, 16, 2, FAKE, FAKE, 7, None) == INVALID         # bad mode
+    assert f(None, 0, 16, 2, None, None, 1, None) == 0               # T = 0: no-op
+
+
+def test_route_map_rejects_bad_arguments(L):
+    f = L.moe_route_map
+    ws = L.moe_route_map_workspace_bytes(100, 16, 2)
+    assert f(FAKE, 100, 16, 2, FAKE, FAKE, FAKE, FAKE, FAKE, ws - 1, None) == INVALID
+    assert f(FAKE, 100, 16, 2, FAKE, FAKE, FAKE, FAKE, None, ws, None) == INVALID
+    assert f(FAKE, 100, 16, 2, FAKE, FAKE, FAKE, FAKE, FAKE + 4, ws, None) == INVALID
+    assert f(FAKE, 100, 16, 17, FAKE, FAKE, FAKE, FAKE, FAKE, ws, None) == INVALID
+    assert f(FAKE, 1 << 27, 16, 16, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == INVALID
+
+
+def test_expand_cast_rejects_bad_arguments(L):
+    f = L.moe_expand_cast_fp8
+    assert f(FAKE, 4, 256, 2, FAKE, 8, FAKE, FAKE, 64, None) == UNSUPPORTED   # group
+    assert f(FAKE, 4, 200, 2, FAKE, 8, FAKE, FAKE, 128, None) == INVALID      # H % 128
+    assert f(FAKE + 8, 4, 256, 2, FAKE, 8, FAKE, FAKE, 128, None) == INVALID  # x align
+    assert f(FAKE, 4, 256, 2, FAKE, 8, FAKE + 4, FAKE, 128, None) == INVALID  # out align
+    assert f(FAKE, 4, 256, 0, FAKE, 8, FAKE, FAKE, 128, None) == INVALID      # k = 0
+    assert f(FAKE, 4, 256, 2, None, 8, FAKE, FAKE, 128, None) == INVALID      # null pos
+    assert f(None, 0, 256, 2, None, 0, None, None, 128, None) == 0            # T = 0
+
+
+def test_swiglu_rejects_bad_arguments(L):
+    f = L.swiglu_cast_fp8
+    assert f(FAKE, 4, 2048, FAKE, FAKE, 32, None) == UNSUPPORTED
+    assert f(FAKE, 4, 100, FAKE, FAKE, 128, None) == INVALID
+    assert f(FAKE, 4, 2048, None, FAKE, 128, None) == INVALID
+    assert f(FAKE + 2, 4, 2048, FAKE, FAKE, 128, None) == INVALID
+    assert f(None, 0, 2048, None, None, 128, None) == 0
+
+
+def test_combine_rejects_bad_arguments(L):
+    f = L.moe_combine
+    assert f(FAKE, FAKE, FAKE, 4, 12, 2, 8, FAKE, 0, None) == INVALID      # H % 8
+    assert f(FAKE, FAKE, FAKE, 4, 256, 2, 8, FAKE, 5, None) == INVALID     # dtype
+    assert f(FAKE, FAKE, FAKE, 4, 256, 2, 8, FAKE + 8, 0, None) == INVALID  # out align
+    assert f(FAKE, None, FAKE, 4, 256, 2, 8, FAKE, 0, None) == INVALID
+    assert f(None, None, None, 0, 256, 2, 0, None, 0, None) == 0
+
+
+def test_peak_copy_rejects_bad_arguments(L):
+    assert L.moe_peak_copy(FAKE, FAKE, 17, None) == INVALID
+    assert L.moe_peak_copy(FAKE + 1, FAKE, 32, None) == INVALID
+    assert L.moe_peak_copy(None, None, 0, None) == 0
+
+
+def test_no_kernel_launched_by_rejected_calls(L):
+    assert L.moe_kernel_launch_count() == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    from moe_routing_precision_gb300 import ops
+    _build.build()
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.topk_gate(torch.zeros(4, 16), 2)
+    with pytest.raises(ValueError, match="CUDA"):
+        ops.swiglu_cast_fp8(torch.zeros(4, 256, dtype=torch.bfloat16))
