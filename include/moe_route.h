@@ -138,6 +138,35 @@ moe_status_t moe_route_map(const int32_t *topk_idx, int64_t num_tokens,
                            size_t workspace_bytes, void *stream);
 
 /*
+ * moe_route_map_noalloc -- moe_route_map for callers that cannot allocate
+ * device memory.  The pages have no counterpart: it exists for callers such
+ * as engine plugins or runtimes that hand out every device buffer from their
+ * own arena and forbid allocation while they run, so they cannot provide the
+ * workspace moe_route_map needs.  Same arguments and results as
+ * moe_route_map, minus the workspace; its histogram lives instead in one
+ * static device array of MOE_ROUTE_NOALLOC_SCRATCH_BYTES that every GPU
+ * loading this library holds until the process exits.
+ * - Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ * - Returns MOE_ERR_UNSUPPORTED, launching nothing, when the problem needs
+ *   more than that: moe_route_map_workspace_bytes(T, E, k) >
+ *   MOE_ROUTE_NOALLOC_SCRATCH_BYTES (T*E > 2^25).
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - All calls share the one array.  Nothing in it needs clearing (each call
+ *   writes every entry it reads), but calls that overlap on the GPU (other
+ *   streams, other threads) race on it and give wrong results: serialise them.
+ * - Expert indices outside [0, E) are skipped (their pos is -1) but, unlike
+ *   moe_route_map, not reported through moe_get_device_status.
+ */
+#define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (1u << 20)
+moe_status_t moe_route_map_noalloc(const int32_t *topk_idx, int64_t num_tokens,
+                                   int32_t num_experts, int32_t num_topk,
+                                   int32_t *counts, int32_t *offsets,
+                                   int32_t *pos, int32_t *sorted_src,
+                                   void *stream);
+
+/*
  * moe_expand_cast_fp8 -- [TK] 3.2 per_token_cast fused with [TK] 2.2
  * expand_to_fused.  For every token t and 128-channel group g of x[t, :]:
  *   amax   = max |x| over the group (bf16 widened exactly to f32)

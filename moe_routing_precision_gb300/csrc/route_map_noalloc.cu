@@ -1,0 +1,79 @@
+// route_map_noalloc.cu -- moe_route_map for callers that cannot allocate
+// device memory.
+//
+// Some callers own every byte of device memory themselves and may not call
+// cudaMalloc (or any allocator) while they run: inference-engine plugins whose
+// host framework hands out all buffers from its own arena, and runtimes that
+// fix their memory budget at start-up.  Such a caller can pass inputs and
+// outputs but has no way to provide moe_route_map's workspace.  This entry
+// point runs the same three route-map kernels with their per-chunk histogram
+// in a fixed file-scope device array instead.
+//
+// The array is a __device__ variable, so every GPU that loads this library
+// holds it (kRouteScratchBytes) until the process exits, whether or not the
+// entry point is ever called.  Host code must not hand the array's name to a
+// kernel: on the host that name is only a stand-in, not a device address.  The
+// device address is looked up with cudaGetSymbolAddress once per device, on
+// the first call made while that device is current.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+// 1 MiB: enough for the histogram of ceil(T/128) chunks x E experts int32,
+// i.e. T*E <= 2^25 (T = 131072 tokens at E = 256, T = 32768 at E = 1024).
+constexpr size_t kRouteScratchBytes = MOE_ROUTE_NOALLOC_SCRATCH_BYTES;
+__device__ __align__(256) unsigned char g_route_scratch[kRouteScratchBytes];
+
+constexpr int kMaxDevices = 64;
+struct ScratchSlot {
+  std::once_flag once;
+  cudaError_t status = cudaSuccess;
+  void* ptr = nullptr;
+  int num_sms = 0;
+};
+ScratchSlot g_slots[kMaxDevices];
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_route_map_noalloc(const int32_t* topk_idx, int64_t num_tokens,
+                                               int32_t num_experts, int32_t num_topk,
+                                               int32_t* counts, int32_t* offsets, int32_t* pos,
+                                               int32_t* sorted_src, void* stream) {
+  if (num_tokens < 0 || num_experts < 1 || num_experts > MOE_MAX_EXPERTS || num_topk < 1 ||
+      num_topk > MOE_MAX_TOPK || num_topk > num_experts)
+    return MOE_ERR_INVALID_ARG;
+  if (num_tokens * (int64_t)num_topk >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
+  if (num_tokens == 0) return moe_route_map(topk_idx, 0, num_experts, num_topk, counts, offsets,
+                                            pos, sorted_src, nullptr, 0, stream);
+  if (!topk_idx || !counts || !offsets || !pos || !sorted_src) return MOE_ERR_INVALID_ARG;
+  if (moe_route_map_workspace_bytes(num_tokens, num_experts, num_topk) > kRouteScratchBytes)
+    return MOE_ERR_UNSUPPORTED;  // beyond the static scratch: use moe_route_map
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  ScratchSlot& s = g_slots[dev];
+  std::call_once(s.once, [&s, dev]() {
+    // runs with `dev` current: these are that device's addresses
+    cudaError_t e = cudaGetSymbolAddress(&s.ptr, g_route_scratch);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    s.status = e;
+  });
+  if (s.status != cudaSuccess || s.ptr == nullptr) return MOE_ERR_CUDA;
+
+  LaunchCtx c;
+  c.stream = static_cast<cudaStream_t>(stream);
+  c.num_sms = s.num_sms;
+  c.err = nullptr;  // out-of-range experts are skipped (pos = -1) but not flagged
+  const int64_t chunks = (num_tokens + kRouteChunkTokens - 1) / kRouteChunkTokens;
+  // every histogram entry the kernels read is written first in the same call,
+  // so the scratch needs no clearing between calls
+  cudaError_t e = launch_route_map(c, topk_idx, num_tokens, num_experts, num_topk, counts, offsets,
+                                   pos, sorted_src, static_cast<int32_t*>(s.ptr), chunks);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -30,6 +30,7 @@ SIGNATURES = {
     "moe_topk_gate": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _P, _i32, _P]),
     "moe_route_map_workspace_bytes": (_sz, [_i64, _i32, _i32]),
     "moe_route_map": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _P, _P, _P, _P, _sz, _P]),
+    "moe_route_map_noalloc": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _P, _P, _P, _P]),
     "moe_expand_cast_fp8": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _i64, _P, _P, _i32, _P]),
     "swiglu_cast_fp8": (ctypes.c_int, [_P, _i64, _i32, _P, _P, _i32, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _i64, _i32, _i32, _i64, _P, _i32, _P]),
