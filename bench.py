@@ -160,6 +160,29 @@ def dist_env():
     return rank, world, local
 
 
+def shard_seed(rank: int) -> int:
+    """Weak scaling: every rank routes its own batch of the same shape, drawn
+    from its own seed; the path needs no exchange between ranks."""
+    return int(rank)
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    """The slowest rank's time (the job's time); a control-plane collective
+    only, outside every timed region."""
+    if world == 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, seconds: float) -> float:
+    """Units all ranks processed / the job's time."""
+    return units_per_rank * world / seconds
+
+
 # ---------------------------------------------------------------- GPU arm
 
 def gpu_arm(args):
@@ -177,24 +200,29 @@ def gpu_arm(args):
     build()
     L = ops.lib()
 
-    w = workloads.WORKLOADS[WORKLOAD]
+    w = workloads.WORKLOADS[args.workload]
     T, E, k, H, R, G = w.T, w.E, w.k, w.H, w.R, w.G
     N = SWIGLU_N
     # weak scaling: every rank routes its own batch (seed = rank), no collective
-    inp = workloads.make_inputs(w, seed=rank, device=dev, with_y=True, with_swiglu=True,
+    full = args.ops == "all"
+    inp = workloads.make_inputs(w, seed=shard_seed(rank), device=dev, with_y=full, with_swiglu=full,
                                 swiglu_rows=R, swiglu_n=N)
-    scores, x, y, hx = inp["scores"], inp["x"], inp["y"], inp["swiglu_x"]
+    ran = {"topk_gate", "route_map"} | ({"expand_cast_fp8"} if args.ops != "route" else set()) | \
+        ({"swiglu_cast_fp8", "combine"} if full else set())
+    scores, x = inp["scores"], inp["x"]
+    y, hx = inp.get("y"), inp.get("swiglu_x")
     i32 = dict(dtype=torch.int32, device=dev)
     idx = torch.empty(T, k, **i32)
     wt = torch.empty(T, k, dtype=torch.float32, device=dev)
     counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
     pos, src = torch.empty(T, k, **i32), torch.empty(R, **i32)
     ws = torch.empty(max(1, ops.route_map_workspace_bytes(T, E, k)), dtype=torch.uint8, device=dev)
-    q = torch.empty(R, H, dtype=torch.uint8, device=dev)
-    sf = torch.empty(R, G, dtype=torch.float32, device=dev)
-    q2 = torch.empty(R, N, dtype=torch.uint8, device=dev)
-    sf2 = torch.empty(R, N // 128, dtype=torch.float32, device=dev)
-    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    q = torch.empty(R if args.ops != "route" else 1, H, dtype=torch.uint8, device=dev)
+    sf = torch.empty(R if args.ops != "route" else 1, G, dtype=torch.float32, device=dev)
+    if full:
+        q2 = torch.empty(R, N, dtype=torch.uint8, device=dev)
+        sf2 = torch.empty(R, N // 128, dtype=torch.float32, device=dev)
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream or None
 
@@ -219,15 +247,19 @@ def gpu_arm(args):
                             pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
         if ev:
             ev[2].record(stream)
-        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
-                                  sf.data_ptr(), 128, sp), "expand")
+        if args.ops != "route":
+            chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
+                                      sf.data_ptr(), 128, sp), "expand")
         if ev:
             ev[3].record(stream)
-        chk(L.swiglu_cast_fp8(hx.data_ptr(), R, N, q2.data_ptr(), sf2.data_ptr(), 128, sp), "swiglu")
+        if full:
+            chk(L.swiglu_cast_fp8(hx.data_ptr(), R, N, q2.data_ptr(), sf2.data_ptr(), 128, sp),
+                "swiglu")
         if ev:
             ev[4].record(stream)
-        chk(L.moe_combine(y.data_ptr(), wt.data_ptr(), pos.data_ptr(), T, H, k, R, out.data_ptr(),
-                          0, sp), "combine")
+        if full:
+            chk(L.moe_combine(y.data_ptr(), wt.data_ptr(), pos.data_ptr(), T, H, k, R,
+                              out.data_ptr(), 0, sp), "combine")
         if ev:
             ev[5].record(stream)
 
@@ -271,11 +303,7 @@ def gpu_arm(args):
         raise RuntimeError("device error flagged during the timed region")
 
     def maxr(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(v, world, dev)
 
     step_ms = maxr(total_ms / K)
     rec_ms_mean = maxr(sum(rec_ms) / K)
@@ -283,7 +311,7 @@ def gpu_arm(args):
 
     # ---- e2e: the same metric through the C ABI from pinned host buffers
     e2e = None
-    if rank == 0 or world > 1:
+    if not args.no_e2e:
         e2e = e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, src,
                       ws, q, sf, T, E, k, H, R, chk, barrier, maxr)
 
@@ -296,7 +324,7 @@ def gpu_arm(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_leg(scores, x, k, E)
+        cpu = cpu_baseline_leg(scores, x, k, E, tokens=min(16384, T), total=T)
 
     if world > 1:
         dist.barrier()
@@ -308,6 +336,8 @@ def gpu_arm(args):
     B = algorithmic_bytes(T, E, k, H, N, R)
     breakdown = {}
     for n in ops_names:
+        if n not in ran:
+            continue
         ms = op_ms[n]
         gbs = B[n] / (ms * 1e-3) / 1e9
         breakdown[n] = {"ms": round(ms, 4), "algorithmic_bytes": B[n], "GB_s": round(gbs, 1),
@@ -317,24 +347,25 @@ def gpu_arm(args):
         "ms": round(rec_ms_mean, 4), "algorithmic_bytes": B["route_expand_cast"],
         "GB_s": round(rec_gbs, 1), "frac_of_peak": round(rec_gbs / peak, 4),
         "tokens_per_s": round(T * world / (rec_ms_mean * 1e-3), 1)}
-    dom = max((n for n in ops_names if n in KERNEL_OF_OP), key=lambda n: op_ms[n])
+    dom = max((n for n in ops_names if n in KERNEL_OF_OP and n in ran), key=lambda n: op_ms[n])
     dom_gbs = B[dom] / (op_ms[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": KERNEL_OF_OP[dom][0], "achieved": round(dom_gbs, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
                 "peak_source": peak_src, "traffic": ncu_traffic(dom),
                 "algorithmic_bytes_per_launch": B[dom]}
-    value = R * world / (rec_ms_mean * 1e-3)
+    value = job_throughput(R, world, rec_ms_mean * 1e-3)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3",
         "data": "synthetic (seeded torch.Generator, no dataset)",
-        "config": {"workload": "large prefill T=65536 E=256 k=8 H=7168 (+SwiGLU 2x2048 per routed "
+        "config": {"workload": f"{w.name}: T={T} E={E} k={k} H={H} (+SwiGLU 2x{N} per routed "
                                "row, combine y [T*k,H]); value = route+expand+cast",
                    "T": T, "E": E, "k": k, "H": H, "swiglu_N": N, "seed": "rank",
                    "parallelism": f"replicas x{world} (token-sharded, no collective)",
                    "l2": L2_NOTE},
         "value_scope": "T*k routed tokens / (topk_gate + route_map + expand_cast_fp8 time)",
+        "step_ops": args.ops,
         "route_expand_cast_GB_s": round(rec_gbs, 1),
         "route_expand_cast_frac_of_peak": round(rec_gbs / peak, 4),
         "step_routed_tokens_per_s": round(R * world / (step_ms * 1e-3), 1),
@@ -490,7 +521,7 @@ def extra_workloads(L, dev, stream, sp, chk, args):
     return res
 
 
-def cpu_baseline_leg(scores, x, k, E, tokens=16384):
+def cpu_baseline_leg(scores, x, k, E, tokens=16384, total=65536):
     """The oracle as it stands, single-threaded, on the first `tokens` tokens."""
     import oracle
     s = scores[:tokens].cpu().numpy()
@@ -501,7 +532,7 @@ def cpu_baseline_leg(scores, x, k, E, tokens=16384):
     oracle.expand_cast_fp8(xb, pos)
     dt = time.perf_counter() - t0
     return {"value": round(tokens * k / dt, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {tokens} of 65536 tokens of the large-prefill workload "
+            "sample": f"first {tokens} of {total} tokens of the benchmarked workload "
                       f"(topk_gate + route_map + expand_cast_fp8), {dt:.1f} s single-threaded"}
 
 
@@ -564,7 +595,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--extra-iters", type=int, default=30)
     ap.add_argument("--ref-tokens", type=int, default=2048)
+    ap.add_argument("--workload", choices=["prefill_64k", "skewed_8k", "decode_1k", "tiny"],
+                    default=WORKLOAD)
+    ap.add_argument("--ops", choices=["all", "route_expand_cast", "route"], default="all",
+                    help="run only part of the step (profiling); the reported line always "
+                         "names what ran")
     ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -83,6 +83,7 @@ typedef enum moe_out_dtype {
 /* Bits of the device error word (moe_get_device_status). */
 #define MOE_DEVERR_EXPERT_RANGE 0x1u /* route_map: topk_idx outside [0, E)      */
 #define MOE_DEVERR_POS_RANGE 0x2u    /* expand/combine: pos >= num_rows         */
+#define MOE_DEVERR_DUPLICATE_EXPERT 0x4u /* route_map: a token names an expert twice */
 
 /*
  * moe_topk_gate -- [TK] 2.1 Top-K Gating, plus the "Weight Normalization" that
@@ -108,8 +109,10 @@ moe_status_t moe_topk_gate(const float *scores, int64_t num_tokens,
 
 /*
  * moe_route_map_workspace_bytes -- device scratch moe_route_map needs for a
- * problem of this size (a per-chunk histogram, E int32 per 128 tokens,
- * rounded up to 256 bytes).  0 when num_tokens == 0.  Pure host function.
+ * problem of this size: a histogram row of E int32 per chunk of consecutive
+ * tokens (chunks of a multiple of 32 tokens, at most 512, aiming at about 128
+ * chunks), rounded up to 256 bytes.  0 when num_tokens == 0 or k is out of
+ * range.  Pure host function.
  */
 size_t moe_route_map_workspace_bytes(int64_t num_tokens, int32_t num_experts,
                                      int32_t num_topk);
@@ -127,8 +130,11 @@ size_t moe_route_map_workspace_bytes(int64_t num_tokens, int32_t num_experts,
  *   workspace: at least moe_route_map_workspace_bytes(...) bytes of device
  *   memory, 16-byte aligned; contents on entry are ignored; it is busy until
  *   the work enqueued on `stream` completes.
- * An index outside [0, E) sets MOE_DEVERR_EXPERT_RANGE; that copy is not
- * counted, its pos is -1, and sorted_src keeps holes at its end.
+ * Each token's k experts must be distinct (as moe_topk_gate produces them); a
+ * repeated expert sets MOE_DEVERR_DUPLICATE_EXPERT and leaves that token's
+ * results unspecified (no write leaves the output buffers).  An index outside
+ * [0, E) sets MOE_DEVERR_EXPERT_RANGE; that copy is not counted, its pos is
+ * -1, and sorted_src keeps holes at its end.
  * Requires the same E and k limits as moe_topk_gate and T*k < 2^31.
  */
 moe_status_t moe_route_map(const int32_t *topk_idx, int64_t num_tokens,
@@ -149,7 +155,8 @@ moe_status_t moe_route_map(const int32_t *topk_idx, int64_t num_tokens,
  * - Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
  * - Returns MOE_ERR_UNSUPPORTED, launching nothing, when the problem needs
  *   more than that: moe_route_map_workspace_bytes(T, E, k) >
- *   MOE_ROUTE_NOALLOC_SCRATCH_BYTES (T*E > 2^25).
+ *   MOE_ROUTE_NOALLOC_SCRATCH_BYTES.  Every problem with T <= 65536 fits
+ *   (any E, k); larger ones fit while ceil(T / 512) * E <= 2^18.
  * - The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture.
@@ -180,9 +187,9 @@ moe_status_t moe_route_map_noalloc(const int32_t *topk_idx, int64_t num_tokens,
  * means "no copy" ([TK] 2.2).  Rows of out no pos names are not written.
  *   x       [T, H] bf16, 16-byte aligned.      pos [T, k] i32.
  *   out     [num_rows, H] u8, 16-byte aligned. out_sf [num_rows, H/128] f32.
- * Requires H % 128 == 0, 1 <= k <= MOE_MAX_TOPK, group == 128 (else
- * MOE_ERR_UNSUPPORTED).  pos >= num_rows sets MOE_DEVERR_POS_RANGE and is
- * skipped.
+ * Requires H % 128 == 0, 1 <= k <= MOE_MAX_TOPK, num_rows < 2^31, group ==
+ * 128 and T * H/128 < 2^31 (else MOE_ERR_UNSUPPORTED).  pos >= num_rows sets
+ * MOE_DEVERR_POS_RANGE and is skipped.
  */
 moe_status_t moe_expand_cast_fp8(const void *x, int64_t num_tokens,
                                  int32_t hidden, int32_t num_topk,
@@ -198,8 +205,11 @@ moe_status_t moe_expand_cast_fp8(const void *x, int64_t num_tokens,
  * then the per-128-channel cast of moe_expand_cast_fp8 on v.
  *   x [M, 2N] bf16, 16-byte aligned; out [M, N] u8, 16-byte aligned;
  *   out_sf [M, N/128] f32.
- * Requires N % 128 == 0 and group == 128.  exp is CUDA's expf, so v may
- * differ from a host expf in the last bits.
+ * Requires N % 128 == 0, group == 128 and M * N/128 < 2^31 (else
+ * MOE_ERR_UNSUPPORTED).  exp and the division use the GPU's exp2 and
+ * reciprocal units (__expf, __fdividef), so v is within a few ulps of the
+ * correctly rounded f32 value, and an E4M3 code can differ by one step from a
+ * host evaluation when v / sf lies that close to a rounding midpoint.
  */
 moe_status_t swiglu_cast_fp8(const void *x, int64_t num_rows, int32_t n,
                              uint8_t *out, float *out_sf, int32_t group,
@@ -215,8 +225,8 @@ moe_status_t swiglu_cast_fp8(const void *x, int64_t num_rows, int32_t n,
  *       expert-sorted layout moe_route_map produced)
  *   topk_weights [T, k] f32, pos [T, k] i32
  *   out [T, H] bf16 or f32, 16-byte aligned
- * Requires H % 8 == 0.  pos >= num_rows sets MOE_DEVERR_POS_RANGE and that
- * copy contributes nothing.
+ * Requires H % 8 == 0 and T * H/8 < 2^31 (else MOE_ERR_UNSUPPORTED).
+ * pos >= num_rows sets MOE_DEVERR_POS_RANGE and that copy contributes nothing.
  */
 moe_status_t moe_combine(const void *y, const float *topk_weights,
                          const int32_t *pos, int64_t num_tokens, int32_t hidden,

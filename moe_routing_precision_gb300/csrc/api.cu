@@ -58,7 +58,6 @@ bool experts_ok(int32_t E, int32_t k) {
   return E >= 1 && E <= MOE_MAX_EXPERTS && k >= 1 && k <= MOE_MAX_TOPK && k <= E;
 }
 
-int64_t route_chunks(int64_t T) { return (T + kRouteChunkTokens - 1) / kRouteChunkTokens; }
 
 }  // namespace
 
@@ -107,9 +106,9 @@ moe_status_t moe_topk_gate(const float* scores, int64_t num_tokens, int32_t num_
 }
 
 size_t moe_route_map_workspace_bytes(int64_t num_tokens, int32_t num_experts, int32_t num_topk) {
-  (void)num_topk;
-  if (num_tokens <= 0 || num_experts < 1) return 0;
-  const size_t bytes = (size_t)route_chunks(num_tokens) * (size_t)num_experts * sizeof(int32_t);
+  if (num_tokens <= 0 || num_experts < 1 || num_topk < 1 || num_topk > MOE_MAX_TOPK) return 0;
+  const size_t bytes =
+      (size_t)route_num_chunks(num_tokens) * (size_t)num_experts * sizeof(int32_t);
   return (bytes + 255) / 256 * 256;
 }
 
@@ -138,7 +137,7 @@ moe_status_t moe_route_map(const int32_t* topk_idx, int64_t num_tokens, int32_t 
   if (s != MOE_OK) return s;
   cudaError_t e = launch_route_map(c, topk_idx, num_tokens, num_experts, num_topk, counts, offsets,
                                    pos, sorted_src, static_cast<int32_t*>(workspace),
-                                   route_chunks(num_tokens));
+                                   route_num_chunks(num_tokens));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
@@ -150,6 +149,7 @@ moe_status_t moe_expand_cast_fp8(const void* x, int64_t num_tokens, int32_t hidd
       num_topk < 1 || num_topk > MOE_MAX_TOPK)
     return MOE_ERR_INVALID_ARG;
   if (num_rows >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
+  if (num_tokens * (hidden / MOE_CAST_GROUP) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if (num_tokens == 0) return MOE_OK;
   if (!x || !pos || (num_rows > 0 && (!out || !out_sf))) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(pos, 4) || !aligned(out, 16) || !aligned(out_sf, 4))
@@ -166,6 +166,7 @@ moe_status_t swiglu_cast_fp8(const void* x, int64_t num_rows, int32_t n, uint8_t
                              float* out_sf, int32_t group, void* stream) {
   if (group != MOE_CAST_GROUP) return MOE_ERR_UNSUPPORTED;
   if (num_rows < 0 || n < MOE_CAST_GROUP || n % MOE_CAST_GROUP != 0) return MOE_ERR_INVALID_ARG;
+  if (num_rows * (n / MOE_CAST_GROUP) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if (num_rows == 0) return MOE_OK;
   if (!x || !out || !out_sf) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(out, 16) || !aligned(out_sf, 4)) return MOE_ERR_INVALID_ARG;
@@ -183,6 +184,7 @@ moe_status_t moe_combine(const void* y, const float* topk_weights, const int32_t
       num_topk > MOE_MAX_TOPK)
     return MOE_ERR_INVALID_ARG;
   if (out_dtype != MOE_OUT_BF16 && out_dtype != MOE_OUT_F32) return MOE_ERR_INVALID_ARG;
+  if (num_tokens * (hidden / 8) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if (num_tokens == 0) return MOE_OK;
   if (!topk_weights || !pos || !out || (num_rows > 0 && !y)) return MOE_ERR_INVALID_ARG;
   if (!aligned(y, 16) || !aligned(topk_weights, 4) || !aligned(pos, 4) || !aligned(out, 16))

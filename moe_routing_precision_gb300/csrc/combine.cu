@@ -32,14 +32,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <bool kOutF32>
 __global__ void __launch_bounds__(kThreads) combine_kernel(
     const uint16_t* __restrict__ y, const float* __restrict__ w, const int32_t* __restrict__ pos,
-    int64_t T, int H, int k, int64_t R, void* __restrict__ out, unsigned* err) {
+    uint32_t slices, int H, int k, int64_t R, void* __restrict__ out, FastDiv fdS, unsigned* err) {
   const int S = H >> 3;  // 8-channel slices per token
-  const int64_t slices = T * S;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const uint32_t stride = gridDim.x * blockDim.x;
   bool bad = false;
-  for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < slices; s += stride) {
-    const int64_t t = s / S;
-    const int c = (int)(s - t * S) * 8;
+  for (uint32_t s = blockIdx.x * blockDim.x + threadIdx.x; s < slices; s += stride) {
+    const int64_t t = fdS.div(s);
+    const int c = (int)(s - (uint32_t)t * S) * 8;
     const int32_t* prow = pos + t * k;
     const float* wrow = w + t * k;
     float acc[8];
@@ -95,8 +94,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
 template <bool kOutF32>
 cudaError_t launch_t(const LaunchCtx& c, const void* y, const float* w, const int32_t* pos,
                      int64_t T, int H, int k, int64_t R, void* out) {
-  const int64_t slices = T * (H / 8);
-  const int64_t need = (slices + kThreads - 1) / kThreads;
+  const uint32_t slices = (uint32_t)(T * (H / 8));  // < 2^31, checked by the caller
+  const int64_t need = ((int64_t)slices + kThreads - 1) / kThreads;
   int per_sm = 0;
   cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<kOutF32>,
                                                                  kThreads, 0);
@@ -104,7 +103,8 @@ cudaError_t launch_t(const LaunchCtx& c, const void* y, const float* w, const in
   const int64_t cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
   const int blocks = (int)(need < cap ? need : cap);
   combine_kernel<kOutF32><<<blocks, kThreads, 0, c.stream>>>(
-      static_cast<const uint16_t*>(y), w, pos, T, H, k, R, out, c.err);
+      static_cast<const uint16_t*>(y), w, pos, slices, H, k, R, out, FastDiv((uint32_t)(H / 8)),
+      c.err);
   count_launches(1);
   return cudaGetLastError();
 }

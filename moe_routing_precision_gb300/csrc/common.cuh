@@ -98,6 +98,28 @@ __device__ __forceinline__ float absmax16(const float (&v)[16]) {
   return m;
 }
 
+// The same two steps straight from 16 packed bf16 (two 16-byte words),
+// unpacking on the fly so the caller keeps 8 registers instead of 16.
+__device__ __forceinline__ float absmax16_bf16(const uint4& a, const uint4& b) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  return m;
+}
+
+__device__ __forceinline__ uint4 quant16_bf16(const uint4& a, const uint4& b, float inv) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w0 = w[2 * i], w1 = w[2 * i + 1];
+    c[i] = e4m3x2(__fmul_rn(bf16_lo(w0), inv), __fmul_rn(bf16_hi(w0), inv)) |
+           (e4m3x2(__fmul_rn(bf16_lo(w1), inv), __fmul_rn(bf16_hi(w1), inv)) << 16);
+  }
+  return make_uint4(c[0], c[1], c[2], c[3]);
+}
+
 // Max over the 8 lanes of an aligned 8-lane subgroup.
 __device__ __forceinline__ float max8(float m) {
   m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
@@ -105,6 +127,27 @@ __device__ __forceinline__ float max8(float m) {
   m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
   return m;
 }
+
+// Unsigned 32-bit division by a divisor fixed at launch, as one multiply-high
+// and two shifts (Granlund and Montgomery, "Division by invariant integers
+// using multiplication", PLDI 1994, round-up variant): for d with
+// 2^(l-1) < d <= 2^l, m = floor(2^32 (2^l - d) / d) + 1 and
+// n / d = (t + ((n - t) >> min(l,1))) >> max(l-1,0) with t = mulhi(n, m).
+struct FastDiv {
+  uint32_t d = 1, m = 1, s1 = 0, s2 = 0;
+  FastDiv() = default;
+  __host__ explicit FastDiv(uint32_t div) : d(div) {
+    uint32_t l = 0;
+    while (l < 32 && (1ull << l) < div) ++l;
+    m = (uint32_t)(((1ull << 32) * ((1ull << l) - div)) / div + 1);
+    s1 = l < 1 ? l : 1;
+    s2 = l > 0 ? l - 1 : 0;
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    const uint32_t t = __umulhi(n, m);
+    return (t + ((n - t) >> s1)) >> s2;
+  }
+};
 
 __device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) {
   if (err) atomicOr(err, bit);
@@ -134,8 +177,22 @@ cudaError_t launch_combine(const LaunchCtx& c, const void* y, const float* w, co
                            int64_t T, int H, int k, int64_t R, void* out, bool out_f32);
 cudaError_t launch_peak_copy(const LaunchCtx& c, const void* src, void* dst, size_t bytes);
 
-// Tokens per route-map chunk (one histogram row of E counters per chunk).
-constexpr int kRouteChunkTokens = 128;
+// Route-map chunking: a chunk is a run of consecutive tokens, a multiple of
+// 32 (one bitmap word per expert per 32 tokens) and at most
+// kRouteMaxChunkTokens, aiming at about kRouteTargetChunks chunks (one wave
+// of CTAs); one histogram row of E counters per chunk in the workspace.
+constexpr int kRouteTargetChunks = 128;
+constexpr int kRouteMaxChunkTokens = 512;
+inline int64_t route_chunk_tokens(int64_t T) {
+  int64_t c = (T + kRouteTargetChunks - 1) / kRouteTargetChunks;
+  c = (c + 31) / 32 * 32;
+  if (c > kRouteMaxChunkTokens) c = kRouteMaxChunkTokens;
+  return c < 32 ? 32 : c;
+}
+inline int64_t route_num_chunks(int64_t T) {
+  const int64_t c = route_chunk_tokens(T);
+  return (T + c - 1) / c;
+}
 
 // Kernel launch counter (api.cu).
 void count_launches(int n);

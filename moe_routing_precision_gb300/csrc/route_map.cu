@@ -8,73 +8,55 @@
 // here every slot is fixed by the row-major (token, slot) order, so the
 // result is deterministic and stable (ascending token within an expert).
 //
-// Three launches over chunks of kRouteChunkTokens tokens:
+// Two launches over chunks of consecutive tokens (a multiple of 32 tokens, at
+// most 512, about 128 chunks):
 //   1. route_count_kernel: one CTA per chunk builds the chunk's histogram in
 //      shared memory (order-free atomics) -> hist[chunk][E] in the workspace.
-//   2. route_scan_kernel: one CTA per 32 experts scans its columns of hist
-//      down the chunks (exclusive) and writes counts[e].
-//   3. route_rank_kernel: one CTA per chunk scans counts into offsets (in
-//      shared memory), ranks its copies stably within the chunk with
-//      __match_any_sync + per-warp counters, and writes pos and sorted_src.
+//   2. route_rank_kernel: one CTA per chunk sums the histogram columns (all
+//      chunks for the totals, earlier chunks for its own base) and scans the
+//      totals into offsets, all in shared memory.  Warp w owns the chunk's
+//      w-th run of 32 tokens and sets bit `lane` of word[w][e] for each expert
+//      e its lane's token picked; a copy's rank among its expert's copies is
+//      then (copies in earlier words) + popc(word & lanes-below), which is
+//      the row-major order because a token's k experts are distinct.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kCountThreads = 256;
-constexpr int kRankWarps = 16;
+constexpr int kCountThreads = 512;
+constexpr int kRankWarps = kRouteMaxChunkTokens / 32;  // 16: one 32-token word each
 constexpr int kRankThreads = kRankWarps * 32;
-// Copies a lane ranks per chunk: kRouteChunkTokens * k / kRankThreads rounds
-// at most (k <= 32 -> 128 * 32 / 512 = 8).
-constexpr int kMaxRounds = (kRouteChunkTokens * 32) / kRankThreads;
 
 __global__ void __launch_bounds__(kCountThreads) route_count_kernel(
-    const int32_t* __restrict__ idx, int64_t R, int E, int k, int32_t* __restrict__ hist,
+    const int32_t* __restrict__ idx, int64_t R, int E, int chunk_pairs, int32_t* __restrict__ hist,
     unsigned* err) {
   extern __shared__ int32_t s_hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
   __syncthreads();
-  const int64_t p0 = (int64_t)blockIdx.x * kRouteChunkTokens * k;
-  const int64_t p1 = min(p0 + (int64_t)kRouteChunkTokens * k, R);
+  const int64_t p0 = (int64_t)blockIdx.x * chunk_pairs;
+  const int64_t p1 = min(p0 + chunk_pairs, R);
   bool bad = false;
-  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
-    const int e = __ldg(idx + p);
-    if ((unsigned)e < (unsigned)E)
-      atomicAdd(&s_hist[e], 1);
-    else
-      bad = true;
+  // eight loads in flight per thread, then the shared-memory increments
+  for (int64_t base = p0 + threadIdx.x; base < p1; base += 8 * (int64_t)blockDim.x) {
+    int e[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t p = base + (int64_t)u * blockDim.x;
+      e[u] = (p < p1) ? __ldg(idx + p) : -1;
+      if (p < p1 && (unsigned)e[u] >= (unsigned)E) {
+        bad = true;
+        e[u] = -1;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (e[u] >= 0) atomicAdd(&s_hist[e[u]], 1);
   }
   if (bad) flag_error(err, MOE_DEVERR_EXPERT_RANGE);
   __syncthreads();
   int32_t* out = hist + (int64_t)blockIdx.x * E;
   for (int e = threadIdx.x; e < E; e += blockDim.x) out[e] = s_hist[e];
-}
-
-// blockDim = (32, 32): x = expert within the CTA's 32, y = one of 32 runs of
-// consecutive chunks.  hist[c][e] becomes the number of copies of e in chunks
-// before c (exclusive down the column); counts[e] gets the column total.
-__global__ void __launch_bounds__(1024) route_scan_kernel(int32_t* __restrict__ hist,
-                                                          int64_t num_chunks, int E,
-                                                          int32_t* __restrict__ counts) {
-  __shared__ int32_t part[32][33];
-  const int e = blockIdx.x * 32 + threadIdx.x;
-  const int64_t per = (num_chunks + 31) / 32;
-  const int64_t c0 = threadIdx.y * per;
-  const int64_t c1 = min(c0 + per, num_chunks);
-  int32_t sum = 0;
-  if (e < E)
-    for (int64_t c = c0; c < c1; ++c) sum += hist[c * E + e];
-  part[threadIdx.y][threadIdx.x] = sum;
-  __syncthreads();
-  int32_t run = 0;
-  for (int y = 0; y < (int)threadIdx.y; ++y) run += part[y][threadIdx.x];
-  if (threadIdx.y == 31 && e < E) counts[e] = run + sum;
-  if (e < E)
-    for (int64_t c = c0; c < c1; ++c) {
-      const int32_t v = hist[c * E + e];
-      hist[c * E + e] = run;
-      run += v;
-    }
 }
 
 __device__ __forceinline__ int32_t warp_incl_scan(int32_t v, int lane) {
@@ -87,23 +69,112 @@ __device__ __forceinline__ int32_t warp_incl_scan(int32_t v, int lane) {
 }
 
 __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(
-    const int32_t* __restrict__ idx, int64_t R, int E, int k, const int32_t* __restrict__ counts,
-    const int32_t* __restrict__ chunk_base, int32_t* __restrict__ offsets, int32_t* __restrict__ pos,
-    int32_t* __restrict__ sorted_src, unsigned* err) {
+    const int32_t* __restrict__ idx, int64_t T, int E, int k, int chunk_tokens, int num_chunks,
+    const int32_t* __restrict__ hist, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ pos, int32_t* __restrict__ sorted_src, unsigned* err) {
   extern __shared__ int32_t smem[];
-  int32_t* s_off = smem;                 // [E] expert offsets
-  int32_t* s_wcnt = smem + E;            // [kRankWarps][E] per-warp counters
+  int32_t* s_off = smem;                                     // [E] totals, then offsets
+  int32_t* s_base = smem + E;                                // [E] copies in earlier chunks
+  uint32_t* s_word = reinterpret_cast<uint32_t*>(smem + 2 * E);  // [kRankWarps][E] bitmaps
+  int32_t* s_wpre = smem + (2 + kRankWarps) * E;             // [kRankWarps][E] word prefixes
   __shared__ int32_t s_warp_tot[kRankWarps];
   __shared__ int32_t s_carry;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x;
+  const int64_t R = T * k;
+  const int64_t t = (int64_t)b * chunk_tokens + warp * 32 + lane;  // this lane's token
+  const bool tok = (warp * 32 < chunk_tokens) && t < T;
 
-  // ---- offsets: exclusive scan of counts[0..E) in chunks of kRankThreads
+  // the first 8 expert ids of this lane's token, loaded before anything else
+  int ids[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) ids[j] = (tok && j < k) ? __ldg(idx + t * k + j) : -1;
+
+  for (int i = tid; i < kRankWarps * E; i += kRankThreads) s_word[i] = 0u;
+  for (int e = tid; e < E; e += kRankThreads) {
+    s_off[e] = 0;
+    s_base[e] = 0;
+  }
+  __syncthreads();
+
+  // ---- bitmap words: bit `lane` of word[warp][e] <=> this lane's token picked e
+  if (tok) {
+    bool dup = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if ((unsigned)ids[j] < (unsigned)E)
+        dup |= (atomicOr(&s_word[warp * E + ids[j]], 1u << lane) >> lane) & 1u;
+    for (int j = 8; j < k; ++j) {
+      const int e = __ldg(idx + t * k + j);
+      if ((unsigned)e < (unsigned)E)
+        dup |= (atomicOr(&s_word[warp * E + e], 1u << lane) >> lane) & 1u;
+    }
+    // a token naming one expert twice cannot be ranked this way (top-k never
+    // produces it): flag it; the slot bound check below keeps writes in range
+    if (dup) flag_error(err, MOE_DEVERR_DUPLICATE_EXPERT);
+  }
+
+  // ---- column sums of the histogram: totals and this chunk's base.  Every
+  // CTA reads the whole histogram, so each starts at a different row to spread
+  // the reads over L2; 16-byte loads (E % 4 == 0), 16 in flight per thread.
+  {
+    const int V4 = (E % 4 == 0) ? 4 : 1;  // columns per load
+    const int ncol = E / V4;
+    const int cols = ncol < kRankThreads ? ncol : kRankThreads;
+    const int phases = kRankThreads / cols;
+    const int col = tid % cols;
+    const int ph = tid / cols;
+    const int nrows = (num_chunks - ph + phases - 1) / phases;  // rows in this phase
+    if (ph < phases && nrows > 0) {
+      const int start = (b / phases) % nrows;
+      for (int c4 = col; c4 < ncol; c4 += cols) {
+        int4 tot = make_int4(0, 0, 0, 0), base = tot;
+        for (int i0 = 0; i0 < nrows; i0 += 16) {
+          int4 v[16];
+          int cc[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            int i = start + i0 + u;
+            if (i >= nrows) i -= nrows;
+            cc[u] = ph + i * phases;
+            v[u] = make_int4(0, 0, 0, 0);
+            if (i0 + u < nrows) {
+              const int32_t* src = hist + (int64_t)cc[u] * E + c4 * V4;
+              if (V4 == 4)
+                v[u] = __ldg(reinterpret_cast<const int4*>(src));
+              else
+                v[u].x = __ldg(src);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const bool before = i0 + u < nrows && cc[u] < b;
+            tot.x += v[u].x; tot.y += v[u].y; tot.z += v[u].z; tot.w += v[u].w;
+            if (before) {
+              base.x += v[u].x; base.y += v[u].y; base.z += v[u].z; base.w += v[u].w;
+            }
+          }
+        }
+        const int e = c4 * V4;
+        atomicAdd(&s_off[e], tot.x);
+        atomicAdd(&s_base[e], base.x);
+        if (V4 == 4) {
+          atomicAdd(&s_off[e + 1], tot.y); atomicAdd(&s_base[e + 1], base.y);
+          atomicAdd(&s_off[e + 2], tot.z); atomicAdd(&s_base[e + 2], base.z);
+          atomicAdd(&s_off[e + 3], tot.w); atomicAdd(&s_base[e + 3], base.w);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- offsets: exclusive scan of the totals, kRankThreads at a time
   if (tid == 0) s_carry = 0;
   __syncthreads();
   for (int base = 0; base < E; base += kRankThreads) {
     const int e = base + tid;
-    const int32_t v = (e < E) ? __ldg(counts + e) : 0;
+    const int32_t v = (e < E) ? s_off[e] : 0;
     const int32_t incl = warp_incl_scan(v, lane);
     if (lane == 31) s_warp_tot[warp] = incl;
     __syncthreads();
@@ -115,86 +186,53 @@ __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(
     __syncthreads();
     const int32_t excl = s_carry + s_warp_tot[warp] + incl - v;
     if (e < E) s_off[e] = excl;
+    if (b == 0 && e < E) counts[e] = v;
     __syncthreads();
     if (tid == kRankThreads - 1) s_carry = excl + v;
     __syncthreads();
   }
-  if (blockIdx.x == 0) {
+  if (b == 0) {
     for (int e = tid; e < E; e += kRankThreads) offsets[e] = s_off[e];
     if (tid == 0) offsets[E] = s_carry;
   }
-  for (int i = tid; i < kRankWarps * E; i += kRankThreads) s_wcnt[i] = 0;
-  __syncthreads();
-
-  // ---- stable ranks inside the chunk: warp w owns a contiguous run of copies
-  const int64_t p0 = (int64_t)blockIdx.x * kRouteChunkTokens * k;
-  const int64_t p1 = min(p0 + (int64_t)kRouteChunkTokens * k, R);
-  const int64_t n = p1 - p0;
-  const int64_t per_warp = ((n + kRankWarps * 32 - 1) / (kRankWarps * 32)) * 32;
-  const int64_t w0 = p0 + warp * per_warp;
-  const int rounds = (int)(per_warp / 32);
-  int32_t* wcnt = s_wcnt + warp * E;
-  const unsigned lt_mask = (1u << lane) - 1u;
-  int32_t r_e[kMaxRounds];
-  int32_t r_rank[kMaxRounds];
-#pragma unroll
-  for (int r = 0; r < kMaxRounds; ++r) {
-    r_e[r] = -1;
-    r_rank[r] = 0;
-    if (r < rounds) {
-      const int64_t p = w0 + r * 32 + lane;
-      const bool valid = p < p1;
-      const int e = valid ? __ldg(idx + p) : -1;
-      const bool ok = valid && (unsigned)e < (unsigned)E;
-      // invalid lanes get a key no other lane has
-      const unsigned key = ok ? (unsigned)e : (0x80000000u | (unsigned)lane);
-      const unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
-      int32_t before = 0;
-      if (ok) before = wcnt[e];
-      __syncwarp();
-      if (ok && (peers & lt_mask) == 0) wcnt[e] = before + __popc(peers);
-      __syncwarp();
-      if (ok) {
-        r_e[r] = e;
-        r_rank[r] = before + __popc(peers & lt_mask);
-      } else if (valid) {
-        r_e[r] = -2;  // out-of-range expert: dropped copy
-      }
-    }
-  }
-  __syncthreads();
-  // exclusive scan of the per-warp counters, per expert
+  // ---- start of each word's copies of e: offset + chunk base + earlier words
   for (int e = tid; e < E; e += kRankThreads) {
-    int32_t run = 0;
+    int32_t run = s_off[e] + s_base[e];
 #pragma unroll
     for (int w = 0; w < kRankWarps; ++w) {
-      const int32_t v = s_wcnt[w * E + e];
-      s_wcnt[w * E + e] = run;
-      run += v;
+      s_wpre[w * E + e] = run;
+      run += __popc(s_word[w * E + e]);
     }
   }
   __syncthreads();
-  const int32_t* cbase = chunk_base + (int64_t)blockIdx.x * E;
+
+  // ---- positions
+  if (tok) {
+    const uint32_t below = (1u << lane) - 1u;
+    bool bad = false;
+    for (int j = 0; j < k; ++j) {
+      const int64_t p = t * k + j;
+      int e = -1;
 #pragma unroll
-  for (int r = 0; r < kMaxRounds; ++r) {
-    if (r < rounds) {
-      const int64_t p = w0 + r * 32 + lane;
-      const int e = r_e[r];
-      if (e >= 0) {
-        const int32_t slot = s_off[e] + __ldg(cbase + e) + wcnt[e] + r_rank[r];
-        // slot < R whenever topk_idx is unchanged since the count kernel read
-        // it; a caller who rewrote it in between gets a flag, not a wild write
-        if ((unsigned)slot < (unsigned)R) {
-          pos[p] = slot;
-          sorted_src[slot] = (int32_t)p;
-        } else {
-          pos[p] = -1;
-          flag_error(err, MOE_DEVERR_EXPERT_RANGE);
-        }
-      } else if (e == -2) {
+      for (int u = 0; u < 8; ++u)
+        if (u == j) e = ids[u];
+      if (j >= 8) e = __ldg(idx + p);
+      if ((unsigned)e >= (unsigned)E) {
+        pos[p] = -1;  // out-of-range expert (flagged by the count kernel)
+        continue;
+      }
+      const int32_t slot = s_wpre[warp * E + e] + __popc(s_word[warp * E + e] & below);
+      // slot < R whenever topk_idx is unchanged since the count kernel read
+      // it; a caller who rewrote it in between gets a flag, not a wild write
+      if ((unsigned)slot < (unsigned)R) {
+        pos[p] = slot;
+        sorted_src[slot] = (int32_t)p;
+      } else {
         pos[p] = -1;
+        bad = true;
       }
     }
+    if (bad) flag_error(err, MOE_DEVERR_EXPERT_RANGE);
   }
 }
 
@@ -204,23 +242,21 @@ cudaError_t launch_route_map(const LaunchCtx& c, const int32_t* idx, int64_t T, 
                              int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* sorted_src,
                              int32_t* ws, int64_t num_chunks) {
   const int64_t R = T * k;
+  const int chunk_tokens = (int)route_chunk_tokens(T);
   const size_t count_smem = sizeof(int32_t) * E;
-  route_count_kernel<<<(unsigned)num_chunks, kCountThreads, count_smem, c.stream>>>(idx, R, E, k, ws,
-                                                                                  c.err);
+  route_count_kernel<<<(unsigned)num_chunks, kCountThreads, count_smem, c.stream>>>(
+      idx, R, E, chunk_tokens * k, ws, c.err);
   cudaError_t st = cudaGetLastError();
   if (st != cudaSuccess) return st;
-  route_scan_kernel<<<(E + 31) / 32, dim3(32, 32), 0, c.stream>>>(ws, num_chunks, E, counts);
-  st = cudaGetLastError();
-  if (st != cudaSuccess) return st;
-  const size_t rank_smem = sizeof(int32_t) * (size_t)E * (1 + kRankWarps);
+  const size_t rank_smem = sizeof(int32_t) * (size_t)E * (2 + 2 * kRankWarps);
   if (rank_smem > 48 * 1024) {
     st = cudaFuncSetAttribute(route_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)rank_smem);
     if (st != cudaSuccess) return st;
   }
   route_rank_kernel<<<(unsigned)num_chunks, kRankThreads, rank_smem, c.stream>>>(
-      idx, R, E, k, counts, ws, offsets, pos, sorted_src, c.err);
-  count_launches(3);
+      idx, T, E, k, chunk_tokens, (int)num_chunks, ws, counts, offsets, pos, sorted_src, c.err);
+  count_launches(2);
   return cudaGetLastError();
 }
 

@@ -22,8 +22,9 @@
 namespace moe {
 namespace {
 
-// 1 MiB: enough for the histogram of ceil(T/128) chunks x E experts int32,
-// i.e. T*E <= 2^25 (T = 131072 tokens at E = 256, T = 32768 at E = 1024).
+// 1 MiB: the histogram is one row of E int32 per chunk, and there are at most
+// 128 chunks until a chunk reaches 512 tokens, so every problem with
+// T <= 65536 fits (any E), and larger ones while ceil(T/512) * E <= 2^18.
 constexpr size_t kRouteScratchBytes = MOE_ROUTE_NOALLOC_SCRATCH_BYTES;
 __device__ __align__(256) unsigned char g_route_scratch[kRouteScratchBytes];
 
@@ -70,7 +71,7 @@ extern "C" moe_status_t moe_route_map_noalloc(const int32_t* topk_idx, int64_t n
   c.stream = static_cast<cudaStream_t>(stream);
   c.num_sms = s.num_sms;
   c.err = nullptr;  // out-of-range experts are skipped (pos = -1) but not flagged
-  const int64_t chunks = (num_tokens + kRouteChunkTokens - 1) / kRouteChunkTokens;
+  const int64_t chunks = route_num_chunks(num_tokens);
   // every histogram entry the kernels read is written first in the same call,
   // so the scratch needs no clearing between calls
   cudaError_t e = launch_route_map(c, topk_idx, num_tokens, num_experts, num_topk, counts, offsets,

@@ -6,10 +6,13 @@
 // The weights are the softmax over the k selected scores (the "Weight
 // Normalization" that closes the routing chain at the top of section 2).
 //
-// GB300 form: each lane keeps E/32 scores as order-preserving 32-bit keys,
-// so one round is a lane-local max, one redux.sync max (value) and one
-// redux.sync min (lowest index among the lanes holding that value) -- two
-// warp instructions instead of a 5-step shuffle butterfly on (value, index).
+// GB300 forms: scores become order-preserving 32-bit integer keys so that a
+// warp reduction is one redux.sync instruction.  For E <= 256 each lane sorts
+// its E/32 candidates once and the k rounds merge the 32 sorted lists (the
+// "sorted-list form" below); otherwise each round rescans the lane's keys
+// (lane-local max, redux.sync max on the value, redux.sync min on the index
+// among lanes holding it) -- two warp instructions per round either way, in
+// place of a 5-step shuffle butterfly on (value, index).
 #include "common.cuh"
 
 namespace moe {
@@ -86,6 +89,181 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float* __restrict_
   }
 }
 
+// ---- filtered form (E <= 256) -----------------------------------------------
+//
+// Every candidate is packed as a 64-bit integer (score key << 32 | ~expert):
+// the larger packed value is the larger score, or on equal scores the lower
+// expert, so the packed order is exactly the selection order.
+//
+// Fast path: theta = the k-th largest of the 32 lane maxima.  At least k
+// distinct experts score >= theta, so every top-k expert does too; the lanes
+// compact their experts scoring >= theta (usually 8-16 of them) one per lane,
+// and k rounds of two redux.sync (max score, then max ~expert among the tied)
+// pick the winners.
+// Fallback (more than 32 candidates, i.e. heavy ties): each lane sorts its V
+// packed candidates and the rounds merge the 32 sorted lists, the winning lane
+// advancing its head from shared memory.  Sorting networks: the optimal
+// 19-comparator network for 8 inputs (Knuth, TAOCP vol. 3, 5.3.4) and the
+// 5-comparator one for 4.
+__device__ __forceinline__ void cex(unsigned long long& a, unsigned long long& b) {
+  const unsigned long long hi = a > b ? a : b;
+  const unsigned long long lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+
+template <int V>
+__device__ __forceinline__ void sort_desc(unsigned long long (&p)[V]) {
+  if constexpr (V == 2) {
+    cex(p[0], p[1]);
+  } else if constexpr (V == 4) {
+    cex(p[0], p[1]); cex(p[2], p[3]); cex(p[0], p[2]); cex(p[1], p[3]); cex(p[1], p[2]);
+  } else if constexpr (V == 8) {
+    cex(p[0], p[2]); cex(p[1], p[3]); cex(p[4], p[6]); cex(p[5], p[7]);
+    cex(p[0], p[4]); cex(p[1], p[5]); cex(p[2], p[6]); cex(p[3], p[7]);
+    cex(p[0], p[1]); cex(p[2], p[3]); cex(p[4], p[5]); cex(p[6], p[7]);
+    cex(p[2], p[4]); cex(p[3], p[5]);
+    cex(p[1], p[4]); cex(p[3], p[6]);
+    cex(p[1], p[2]); cex(p[3], p[4]); cex(p[5], p[6]);
+  }
+}
+
+constexpr int kSortedWarps = 8;
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// V slots per lane.  VEC: E % 128 == 0, lane l loads experts h*128 + 4l + j
+// (16-byte loads); otherwise expert i*32 + l in slot i.
+template <int V, bool VEC>
+__global__ void __launch_bounds__(kSortedWarps * 32) topk_gate_sorted_kernel(
+    const float* __restrict__ scores, int64_t T, int E, int k, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w) {
+  __shared__ unsigned long long s_list[kSortedWarps][V][32];
+  __shared__ unsigned long long s_cand[kSortedWarps][32];
+  const int lane = threadIdx.x & 31;
+  const int wib = threadIdx.x >> 5;
+  const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    const float* row = scores + t * E;
+    unsigned long long p[V];
+    if constexpr (VEC) {
+#pragma unroll
+      for (int h = 0; h < V / 4; ++h) {
+        const float4 f = __ldcs(reinterpret_cast<const float4*>(row + h * 128 + 4 * lane));
+        const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t e = (uint32_t)(h * 128 + 4 * lane + j);
+          p[h * 4 + j] = ((unsigned long long)score_key(fv[j]) << 32) | (uint32_t)~e;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int e = i * 32 + lane;
+        p[i] = (e < E) ? (((unsigned long long)score_key(__ldcs(row + e)) << 32) |
+                          (uint32_t)~(uint32_t)e)
+                       : 0ull;  // absent slot: below every real score
+      }
+    }
+    uint32_t my_key = 0, my_e = 0, top_key = 0;
+    // ---- candidate filter: theta = k-th largest of the 32 lane maxima; every
+    // top-k element scores >= theta (k distinct lane maxima do)
+    uint32_t lmax = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i) lmax = max(lmax, (uint32_t)(p[i] >> 32));
+    uint32_t theta = 0;
+    {
+      uint32_t lm = lmax;
+      for (int r = 0; r < k; ++r) {
+        theta = __reduce_max_sync(0xFFFFFFFFu, lm);
+        const unsigned holders = __ballot_sync(0xFFFFFFFFu, lm == theta);
+        if (lane == __ffs(holders) - 1) lm = 0u;  // retire one holder
+      }
+    }
+    unsigned cmask = 0;  // this lane's candidates (absent slots are 0)
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (p[i] != 0ull && (uint32_t)(p[i] >> 32) >= theta) cmask |= 1u << i;
+    const int nc = __popc(cmask);
+    const int C = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)nc);
+    __syncwarp();  // the previous token's rounds are done with shared memory
+    if (C <= 32) {
+      // compact the candidates one per lane, then k exact rounds on them
+      const int first = warp_incl_scan(nc, lane) - nc;
+      int slot = first;
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        if (cmask & (1u << i)) s_cand[wib][slot++] = p[i];
+      __syncwarp();
+      unsigned long long cand = (lane < C) ? s_cand[wib][lane] : 0ull;
+      for (int r = 0; r < k; ++r) {
+        const uint32_t ck = (uint32_t)(cand >> 32), cl = (uint32_t)cand;
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, ck);
+        const uint32_t wl = __reduce_max_sync(0xFFFFFFFFu, ck == m ? cl : 0u);
+        if (r == 0) top_key = m;
+        if (lane == r) {
+          my_key = m;
+          my_e = ~wl;
+        }
+        if (ck == m && cl == wl) cand = 0ull;
+      }
+    } else {
+      // many ties: sort each lane's list and merge the 32 lists
+      sort_desc<V>(p);
+#pragma unroll
+      for (int i = 1; i < V; ++i) s_list[wib][i][lane] = p[i];
+      __syncwarp();
+      unsigned long long head = p[0];
+      int taken = 0;
+      for (int r = 0; r < k; ++r) {
+        const uint32_t hk = (uint32_t)(head >> 32);
+        const uint32_t hl = (uint32_t)head;
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, hk);
+        const uint32_t wl = __reduce_max_sync(0xFFFFFFFFu, hk == m ? hl : 0u);
+        if (r == 0) top_key = m;
+        if (lane == r) {
+          my_key = m;
+          my_e = ~wl;
+        }
+        if (hk == m && hl == wl) {  // this lane supplied the winner
+          ++taken;
+          head = (taken < V) ? s_list[wib][taken][lane] : 0ull;
+        }
+      }
+    }
+    if (lane < k) topk_idx[t * k + lane] = (int32_t)my_e;
+    if (topk_w != nullptr) {
+      const float s0 = key_score(top_key);
+      const float ex = (lane < k) ? expf(key_score(my_key) - s0) : 0.0f;
+      float sum = ex;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+      if (lane < k) topk_w[t * k + lane] = __fdiv_rn(ex, sum);
+    }
+  }
+}
+
+template <int V, bool VEC>
+cudaError_t launch_sorted(const LaunchCtx& c, const float* scores, int64_t T, int E, int k,
+                          int32_t* idx, float* w) {
+  const int64_t need = (T + kSortedWarps - 1) / kSortedWarps;
+  const int64_t cap = (int64_t)c.num_sms * 8;
+  const int blocks = (int)(need < cap ? need : cap);
+  topk_gate_sorted_kernel<V, VEC><<<blocks, kSortedWarps * 32, 0, c.stream>>>(scores, T, E, k,
+                                                                            idx, w);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+// rescan form (E <= 32, E > 256)
 template <int V>
 cudaError_t launch_v(const LaunchCtx& c, const float* scores, int64_t T, int E, int k,
                      int32_t* idx, float* w) {
@@ -102,10 +280,13 @@ cudaError_t launch_v(const LaunchCtx& c, const float* scores, int64_t T, int E, 
 
 cudaError_t launch_topk_gate(const LaunchCtx& c, const float* scores, int64_t T, int E, int k,
                              int32_t* idx, float* w) {
+  const bool vec = (E % 128 == 0) && (reinterpret_cast<uintptr_t>(scores) % 16 == 0);
   if (E <= 32) return launch_v<1>(c, scores, T, E, k, idx, w);
-  if (E <= 64) return launch_v<2>(c, scores, T, E, k, idx, w);
-  if (E <= 128) return launch_v<4>(c, scores, T, E, k, idx, w);
-  if (E <= 256) return launch_v<8>(c, scores, T, E, k, idx, w);
+  if (E <= 64) return launch_sorted<2, false>(c, scores, T, E, k, idx, w);
+  if (E <= 128) return vec ? launch_sorted<4, true>(c, scores, T, E, k, idx, w)
+                           : launch_sorted<4, false>(c, scores, T, E, k, idx, w);
+  if (E <= 256) return vec ? launch_sorted<8, true>(c, scores, T, E, k, idx, w)
+                           : launch_sorted<8, false>(c, scores, T, E, k, idx, w);
   if (E <= 512) return launch_v<16>(c, scores, T, E, k, idx, w);
   return launch_v<32>(c, scores, T, E, k, idx, w);
 }

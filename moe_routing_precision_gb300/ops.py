@@ -20,7 +20,7 @@ from ._build import LIB_PATH
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(5)
 MOE_WEIGHTS_NONE, MOE_WEIGHTS_SOFTMAX_TOPK = 0, 1
 MOE_OUT_BF16, MOE_OUT_F32 = 0, 1
-MOE_DEVERR_EXPERT_RANGE, MOE_DEVERR_POS_RANGE = 0x1, 0x2
+MOE_DEVERR_EXPERT_RANGE, MOE_DEVERR_POS_RANGE, MOE_DEVERR_DUPLICATE_EXPERT = 0x1, 0x2, 0x4
 GROUP = 128
 
 # Every symbol declared in include/moe_route.h, with its ctypes signature.

@@ -55,8 +55,14 @@ def test_abi_version_and_status_strings(L):
 def test_workspace_size(L):
     assert L.moe_route_map_workspace_bytes(0, 256, 8) == 0
     assert L.moe_route_map_workspace_bytes(1, 256, 8) == 1024
-    assert L.moe_route_map_workspace_bytes(65536, 256, 8) == 512 * 256 * 4
+    # about 128 chunks of a multiple of 32 tokens: 512 tokens per chunk at T=65536
+    assert L.moe_route_map_workspace_bytes(65536, 256, 8) == 128 * 256 * 4
+    # chunks stop growing at 512 tokens: T=2^21 -> 4096 chunks
+    assert L.moe_route_map_workspace_bytes(1 << 21, 256, 8) == 4096 * 256 * 4
+    # small T: 32-token chunks
+    assert L.moe_route_map_workspace_bytes(100, 16, 2) == 256
     assert L.moe_route_map_workspace_bytes(129, 16, 2) % 256 == 0
+    assert L.moe_route_map_workspace_bytes(100, 16, 0) == 0
 
 
 FAKE = 0x10000  # never dereferenced: every call below is rejected on the host

@@ -114,6 +114,12 @@ def test_route_map_flags_out_of_range_expert():
     assert sorted(p[p >= 0].tolist()) == [0, 1, 2, 3]
 
 
+def test_route_map_flags_repeated_expert():
+    idx = torch.tensor([[0, 1], [2, 2], [3, 4]], dtype=torch.int32, device=DEV)
+    ops.route_map(idx, 8)
+    assert ops.device_status() & ops.MOE_DEVERR_DUPLICATE_EXPERT
+
+
 # ---------------------------------------------------------------- expand + cast
 
 @pytest.mark.parametrize("T,H,k", [(1, 128, 1), (3, 384, 2), (33, 256, 8), (64, 256, 2),

@@ -80,7 +80,7 @@ def test_noalloc_matches_route_map_on_two_calls_in_a_row(L):
 
 def test_noalloc_refuses_problems_beyond_its_scratch(L):
     E, k = 256, 8
-    T = SCRATCH_BYTES // (E * 4) * 128 + 1      # one chunk more than fits
+    T = (SCRATCH_BYTES // (E * 4) + 1) * 512   # one 512-token chunk more than fits
     assert L.moe_route_map_workspace_bytes(T, E, k) > SCRATCH_BYTES
     launches = L.moe_kernel_launch_count()
     rc = L.moe_route_map_noalloc(ctypes.c_void_p(0x10000), T, E, k, ctypes.c_void_p(0x10000),
