@@ -33,6 +33,7 @@ template <bool kOutF32>
 __global__ void __launch_bounds__(kThreads) combine_kernel(
     const uint16_t* __restrict__ y, const float* __restrict__ w, const int32_t* __restrict__ pos,
     uint32_t slices, int H, int k, int64_t R, void* __restrict__ out, FastDiv fdS, unsigned* err) {
+  pdl_enter();
   const int S = H >> 3;  // 8-channel slices per token
   const uint32_t stride = gridDim.x * blockDim.x;
   bool bad = false;
@@ -102,11 +103,9 @@ cudaError_t launch_t(const LaunchCtx& c, const void* y, const float* w, const in
   if (st != cudaSuccess) return st;
   const int64_t cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
   const int blocks = (int)(need < cap ? need : cap);
-  combine_kernel<kOutF32><<<blocks, kThreads, 0, c.stream>>>(
-      static_cast<const uint16_t*>(y), w, pos, slices, H, k, R, out, FastDiv((uint32_t)(H / 8)),
-      c.err);
-  count_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel<kOutF32>, blocks, kThreads, 0, c.stream,
+                    static_cast<const uint16_t*>(y), w, pos, slices, H, k, R, out,
+                    FastDiv((uint32_t)(H / 8)), c.err);
 }
 
 }  // namespace

@@ -149,6 +149,17 @@ struct FastDiv {
   }
 };
 
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialization and starts with pdl_enter(), which
+// waits until the previous kernel on the stream has finished and its writes
+// are visible, before any global memory access: stream order is unchanged for
+// the data.  A kernel's CTAs release the next kernel as they exit (the
+// implicit trigger), so the next launch is processed while the last CTAs
+// drain instead of after the whole grid retires.  (Releasing it at kernel
+// entry instead let waiting CTAs of the next kernel take SMs early and
+// unbalanced the one-CTA-per-SM expand grid on GB300.)
+__device__ __forceinline__ void pdl_enter() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) {
   if (err) atomicOr(err, bit);
 }
@@ -196,4 +207,23 @@ inline int64_t route_num_chunks(int64_t T) {
 
 // Kernel launch counter (api.cu).
 void count_launches(int n);
+
+// Launch `kernel` on `stream` with programmatic stream serialization (see
+// pdl_enter) and count it.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  count_launches(1);
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 }  // namespace moe

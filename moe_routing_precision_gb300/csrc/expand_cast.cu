@@ -60,6 +60,7 @@ template <bool G4>
 __global__ void __launch_bounds__(kThreads) expand_cast_kernel(
     const uint16_t* __restrict__ x, uint32_t units, int H, int k, const int32_t* __restrict__ pos,
     int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf, FastDiv fdG, unsigned* err) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int sub = lane >> 3;  // unit within the warp's tile
   const int l8 = lane & 7;    // 16-channel slice within the group
@@ -125,6 +126,7 @@ template <bool G4>
 __global__ void __launch_bounds__(1024) expand_cast_rows_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
     int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf, int tpc, unsigned* err) {
+  pdl_enter();
   const int P = H >> 4;  // threads per token
   const int G = H >> 7;
   const int tid = threadIdx.x;
@@ -208,10 +210,8 @@ cudaError_t launch_rows(const LaunchCtx& c, const void* x, int64_t T, int H, int
   const int64_t cap = (int64_t)c.num_sms * ctas_per_sm;
   const int blocks = (int)(groups < cap ? groups : cap);
   const int threads = (P * tpc + 31) / 32 * 32;  // whole warps: the shuffles use full masks
-  expand_cast_rows_kernel<G4><<<blocks, threads, 0, c.stream>>>(
-      static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, tpc, c.err);
-  count_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(expand_cast_rows_kernel<G4>, blocks, threads, 0, c.stream,
+                    static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, tpc, c.err);
 }
 
 template <bool G4>
@@ -227,11 +227,9 @@ cudaError_t launch_g(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
   if (st != cudaSuccess) return st;
   const int64_t cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
   const int blocks = (int)(need < cap ? need : cap);
-  expand_cast_kernel<G4><<<blocks, kThreads, 0, c.stream>>>(
-      static_cast<const uint16_t*>(x), units, H, k, pos, R, out, out_sf, FastDiv((uint32_t)G),
-      c.err);
-  count_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(expand_cast_kernel<G4>, blocks, kThreads, 0, c.stream,
+                    static_cast<const uint16_t*>(x), units, H, k, pos, R, out, out_sf,
+                    FastDiv((uint32_t)G), c.err);
 }
 
 }  // namespace

@@ -11,6 +11,7 @@ constexpr int kUnroll = 4;
 
 __global__ void __launch_bounds__(kThreads) peak_copy_kernel(const uint4* __restrict__ src,
                                                              uint4* __restrict__ dst, int64_t n) {
+  pdl_enter();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (; i + (kUnroll - 1) * stride < n; i += kUnroll * stride) {
@@ -34,10 +35,8 @@ cudaError_t launch_peak_copy(const LaunchCtx& c, const void* src, void* dst, siz
   const int64_t need = (n + kThreads - 1) / kThreads;
   const int64_t cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
   const int blocks = (int)(need < cap ? need : cap);
-  peak_copy_kernel<<<blocks, kThreads, 0, c.stream>>>(static_cast<const uint4*>(src),
-                                                      static_cast<uint4*>(dst), n);
-  count_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(peak_copy_kernel, blocks, kThreads, 0, c.stream,
+                    static_cast<const uint4*>(src), static_cast<uint4*>(dst), n);
 }
 
 }  // namespace moe

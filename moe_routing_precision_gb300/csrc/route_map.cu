@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(kCountThreads) route_count_kernel(
     const int32_t* __restrict__ idx, int64_t R, int E, int chunk_pairs, int32_t* __restrict__ hist,
     unsigned* err) {
   extern __shared__ int32_t s_hist[];
+  pdl_enter();
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
   __syncthreads();
   const int64_t p0 = (int64_t)blockIdx.x * chunk_pairs;
@@ -79,6 +80,7 @@ __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(
   int32_t* s_wpre = smem + (2 + kRankWarps) * E;             // [kRankWarps][E] word prefixes
   __shared__ int32_t s_warp_tot[kRankWarps];
   __shared__ int32_t s_carry;
+  pdl_enter();
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x;
@@ -244,9 +246,8 @@ cudaError_t launch_route_map(const LaunchCtx& c, const int32_t* idx, int64_t T, 
   const int64_t R = T * k;
   const int chunk_tokens = (int)route_chunk_tokens(T);
   const size_t count_smem = sizeof(int32_t) * E;
-  route_count_kernel<<<(unsigned)num_chunks, kCountThreads, count_smem, c.stream>>>(
-      idx, R, E, chunk_tokens * k, ws, c.err);
-  cudaError_t st = cudaGetLastError();
+  cudaError_t st = launch_pdl(route_count_kernel, (unsigned)num_chunks, kCountThreads, count_smem,
+                              c.stream, idx, R, E, chunk_tokens * k, ws, c.err);
   if (st != cudaSuccess) return st;
   const size_t rank_smem = sizeof(int32_t) * (size_t)E * (2 + 2 * kRankWarps);
   if (rank_smem > 48 * 1024) {
@@ -254,10 +255,9 @@ cudaError_t launch_route_map(const LaunchCtx& c, const int32_t* idx, int64_t T, 
                               (int)rank_smem);
     if (st != cudaSuccess) return st;
   }
-  route_rank_kernel<<<(unsigned)num_chunks, kRankThreads, rank_smem, c.stream>>>(
-      idx, T, E, k, chunk_tokens, (int)num_chunks, ws, counts, offsets, pos, sorted_src, c.err);
-  count_launches(2);
-  return cudaGetLastError();
+  return launch_pdl(route_rank_kernel, (unsigned)num_chunks, kRankThreads, rank_smem, c.stream,
+                    idx, T, E, k, chunk_tokens, (int)num_chunks, ws, counts, offsets, pos,
+                    sorted_src, c.err);
 }
 
 }  // namespace moe

@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_cast_kernel(const uint16_t* _
                                                                uint8_t* __restrict__ out,
                                                                float* __restrict__ out_sf,
                                                                FastDiv fdG) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int sub = lane >> 3;
   const int l8 = lane & 7;
@@ -83,10 +84,8 @@ cudaError_t launch_swiglu_cast(const LaunchCtx& c, const void* x, int64_t M, int
   if (st != cudaSuccess) return st;
   const int64_t cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
   const int blocks = (int)(need < cap ? need : cap);
-  swiglu_cast_kernel<<<blocks, kThreads, 0, c.stream>>>(static_cast<const uint16_t*>(x), units, N,
-                                                         out, out_sf, FastDiv((uint32_t)G));
-  count_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(swiglu_cast_kernel, blocks, kThreads, 0, c.stream,
+                    static_cast<const uint16_t*>(x), units, N, out, out_sf, FastDiv((uint32_t)G));
 }
 
 }  // namespace moe

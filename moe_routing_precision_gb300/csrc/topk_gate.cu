@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float* __restrict_
                                                         int64_t T, int E, int k,
                                                         int32_t* __restrict__ topk_idx,
                                                         float* __restrict__ topk_w) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
@@ -98,8 +99,8 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float* __restrict_
 // Fast path: theta = the k-th largest of the 32 lane maxima.  At least k
 // distinct experts score >= theta, so every top-k expert does too; the lanes
 // compact their experts scoring >= theta (usually 8-16 of them) one per lane,
-// and k rounds of two redux.sync (max score, then max ~expert among the tied)
-// pick the winners.
+// and each candidate's rank (how many candidates beat it) is its output slot
+// if below k.
 // Fallback (more than 32 candidates, i.e. heavy ties): each lane sorts its V
 // packed candidates and the rounds merge the 32 sorted lists, the winning lane
 // advancing its head from shared memory.  Sorting networks: the optimal
@@ -140,13 +141,15 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 }
 
 // V slots per lane.  VEC: E % 128 == 0, lane l loads experts h*128 + 4l + j
-// (16-byte loads); otherwise expert i*32 + l in slot i.
-template <int V, bool VEC>
+// (16-byte loads); otherwise expert i*32 + l in slot i.  KMAX >= k bounds the
+// unrolled rounds.
+template <int V, bool VEC, int KMAX>
 __global__ void __launch_bounds__(kSortedWarps * 32) topk_gate_sorted_kernel(
     const float* __restrict__ scores, int64_t T, int E, int k, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w) {
   __shared__ unsigned long long s_list[kSortedWarps][V][32];
   __shared__ unsigned long long s_cand[kSortedWarps][32];
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -173,7 +176,10 @@ __global__ void __launch_bounds__(kSortedWarps * 32) topk_gate_sorted_kernel(
                        : 0ull;  // absent slot: below every real score
       }
     }
-    uint32_t my_key = 0, my_e = 0, top_key = 0;
+    // Each lane ends with at most one output: slot out_j (-1: none) holding
+    // expert out_e with score key out_key.
+    int out_j = -1;
+    uint32_t out_key = 0, out_e = 0;
     // ---- candidate filter: theta = k-th largest of the 32 lane maxima; every
     // top-k element scores >= theta (k distinct lane maxima do)
     uint32_t lmax = 0;
@@ -182,10 +188,13 @@ __global__ void __launch_bounds__(kSortedWarps * 32) topk_gate_sorted_kernel(
     uint32_t theta = 0;
     {
       uint32_t lm = lmax;
-      for (int r = 0; r < k; ++r) {
-        theta = __reduce_max_sync(0xFFFFFFFFu, lm);
-        const unsigned holders = __ballot_sync(0xFFFFFFFFu, lm == theta);
-        if (lane == __ffs(holders) - 1) lm = 0u;  // retire one holder
+#pragma unroll
+      for (int r = 0; r < KMAX; ++r) {
+        if (r < k) {
+          theta = __reduce_max_sync(0xFFFFFFFFu, lm);
+          const unsigned holders = __ballot_sync(0xFFFFFFFFu, lm == theta);
+          if (lane == __ffs(holders) - 1) lm = 0u;  // retire one holder
+        }
       }
     }
     unsigned cmask = 0;  // this lane's candidates (absent slots are 0)
@@ -194,26 +203,22 @@ __global__ void __launch_bounds__(kSortedWarps * 32) topk_gate_sorted_kernel(
       if (p[i] != 0ull && (uint32_t)(p[i] >> 32) >= theta) cmask |= 1u << i;
     const int nc = __popc(cmask);
     const int C = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)nc);
-    __syncwarp();  // the previous token's rounds are done with shared memory
+    __syncwarp();  // the previous token is done with shared memory
     if (C <= 32) {
-      // compact the candidates one per lane, then k exact rounds on them
-      const int first = warp_incl_scan(nc, lane) - nc;
-      int slot = first;
+      // compact the candidates one per lane; each counts the candidates that
+      // beat it, and that count is its output slot
+      int slot = warp_incl_scan(nc, lane) - nc;
 #pragma unroll
       for (int i = 0; i < V; ++i)
         if (cmask & (1u << i)) s_cand[wib][slot++] = p[i];
       __syncwarp();
-      unsigned long long cand = (lane < C) ? s_cand[wib][lane] : 0ull;
-      for (int r = 0; r < k; ++r) {
-        const uint32_t ck = (uint32_t)(cand >> 32), cl = (uint32_t)cand;
-        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, ck);
-        const uint32_t wl = __reduce_max_sync(0xFFFFFFFFu, ck == m ? cl : 0u);
-        if (r == 0) top_key = m;
-        if (lane == r) {
-          my_key = m;
-          my_e = ~wl;
-        }
-        if (ck == m && cl == wl) cand = 0ull;
+      const unsigned long long cand = (lane < C) ? s_cand[wib][lane] : 0ull;
+      int rank = 0;
+      for (int j = 0; j < C; ++j) rank += (s_cand[wib][j] > cand) ? 1 : 0;
+      if (lane < C && rank < k) {
+        out_j = rank;
+        out_key = (uint32_t)(cand >> 32);
+        out_e = ~(uint32_t)cand;
       }
     } else {
       // many ties: sort each lane's list and merge the 32 lists
@@ -228,10 +233,10 @@ __global__ void __launch_bounds__(kSortedWarps * 32) topk_gate_sorted_kernel(
         const uint32_t hl = (uint32_t)head;
         const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, hk);
         const uint32_t wl = __reduce_max_sync(0xFFFFFFFFu, hk == m ? hl : 0u);
-        if (r == 0) top_key = m;
         if (lane == r) {
-          my_key = m;
-          my_e = ~wl;
+          out_j = r;
+          out_key = m;
+          out_e = ~wl;
         }
         if (hk == m && hl == wl) {  // this lane supplied the winner
           ++taken;
@@ -239,14 +244,15 @@ __global__ void __launch_bounds__(kSortedWarps * 32) topk_gate_sorted_kernel(
         }
       }
     }
-    if (lane < k) topk_idx[t * k + lane] = (int32_t)my_e;
+    if (out_j >= 0) topk_idx[t * k + out_j] = (int32_t)out_e;
     if (topk_w != nullptr) {
+      const uint32_t top_key = __reduce_max_sync(0xFFFFFFFFu, out_j >= 0 ? out_key : 0u);
       const float s0 = key_score(top_key);
-      const float ex = (lane < k) ? expf(key_score(my_key) - s0) : 0.0f;
+      const float ex = (out_j >= 0) ? expf(key_score(out_key) - s0) : 0.0f;
       float sum = ex;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-      if (lane < k) topk_w[t * k + lane] = __fdiv_rn(ex, sum);
+      if (out_j >= 0) topk_w[t * k + out_j] = __fdiv_rn(ex, sum);
     }
   }
 }
@@ -257,10 +263,11 @@ cudaError_t launch_sorted(const LaunchCtx& c, const float* scores, int64_t T, in
   const int64_t need = (T + kSortedWarps - 1) / kSortedWarps;
   const int64_t cap = (int64_t)c.num_sms * 8;
   const int blocks = (int)(need < cap ? need : cap);
-  topk_gate_sorted_kernel<V, VEC><<<blocks, kSortedWarps * 32, 0, c.stream>>>(scores, T, E, k,
-                                                                            idx, w);
-  count_launches(1);
-  return cudaGetLastError();
+  if (k <= 8)
+    return launch_pdl(topk_gate_sorted_kernel<V, VEC, 8>, blocks, kSortedWarps * 32, 0, c.stream,
+                      scores, T, E, k, idx, w);
+  return launch_pdl(topk_gate_sorted_kernel<V, VEC, 32>, blocks, kSortedWarps * 32, 0, c.stream,
+                    scores, T, E, k, idx, w);
 }
 
 // rescan form (E <= 32, E > 256)
@@ -271,9 +278,7 @@ cudaError_t launch_v(const LaunchCtx& c, const float* scores, int64_t T, int E, 
   const int64_t need = (T + 7) / 8;
   const int64_t cap = (int64_t)c.num_sms * 8;
   const int blocks = (int)(need < cap ? need : cap);
-  topk_gate_kernel<V><<<blocks, threads, 0, c.stream>>>(scores, T, E, k, idx, w);
-  count_launches(1);
-  return cudaGetLastError();
+  return launch_pdl(topk_gate_kernel<V>, blocks, threads, 0, c.stream, scores, T, E, k, idx, w);
 }
 
 }  // namespace
