@@ -61,9 +61,9 @@ def algorithmic_bytes(T, E, k, H, N=SWIGLU_N, M=None):
     return b
 
 
-KERNEL_OF_OP = {  # op -> (kernel name in ncu, source file)
-    "topk_gate": ("topk_gate_kernel", "topk_gate.cu"),
-    "expand_cast_fp8": ("expand_cast_kernel", "expand_cast.cu"),
+KERNEL_OF_OP = {  # op -> (kernel name in ncu, source file), for E <= 256 and H <= 16384
+    "topk_gate": ("topk_gate_sorted_kernel", "topk_gate.cu"),
+    "expand_cast_fp8": ("expand_cast_bulk_kernel", "expand_cast.cu"),
     "swiglu_cast_fp8": ("swiglu_cast_kernel", "swiglu_cast.cu"),
     "combine": ("combine_kernel", "combine.cu"),
 }

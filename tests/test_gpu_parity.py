@@ -159,8 +159,9 @@ def test_expand_cast_extreme_values():
     assert_f32_bits_equal(np_(sf), o_sf, "extreme sf")
 
 
-def test_expand_dropped_copies_and_untouched_rows():
-    T, H, k, R = 40, 256, 4, 200
+@pytest.mark.parametrize("H", [256, 512])   # row form (H/128 = 2), bulk-store form (H/128 = 4)
+def test_expand_dropped_copies_and_untouched_rows(H):
+    T, k, R = 40, 4, 200
     x = workloads.random_small(T, 16, k, H, seed=3)["x"]
     g = torch.Generator().manual_seed(5)
     pos = torch.randperm(R, generator=g)[:T * k].to(torch.int32).view(T, k)
@@ -173,12 +174,13 @@ def test_expand_dropped_copies_and_untouched_rows():
     assert_f32_bits_equal(np_(sf), o_sf, "expand sf with holes")
 
 
-def test_expand_flags_pos_out_of_range():
-    T, H, k = 4, 256, 2
+@pytest.mark.parametrize("H", [256, 512])
+def test_expand_flags_pos_out_of_range(H):
+    T, k = 4, 2
     x = workloads.random_small(T, 16, k, H, seed=4)["x"].to(DEV)
     pos = torch.tensor([[0, 1], [2, 3], [4, 8], [5, 6]], dtype=torch.int32, device=DEV)
     q = torch.zeros(8, H, dtype=torch.uint8, device=DEV)
-    sf = torch.zeros(8, 2, device=DEV)
+    sf = torch.zeros(8, H // 128, device=DEV)
     ops.expand_cast_fp8(x, pos, 8, out=q, out_sf=sf)
     assert ops.device_status() == ops.MOE_DEVERR_POS_RANGE
     assert int(q[7].sum()) == 0
