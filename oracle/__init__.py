@@ -57,6 +57,8 @@ def _load():
                 "oracle_bf16_from_double": (ctypes.c_uint16, [ctypes.c_double]),
                 "oracle_topk_gate": (ctypes.c_int, [P, i64, i32, i32, P, P]),
                 "oracle_route_map": (ctypes.c_int, [P, i64, i32, i32, P, P, P, P]),
+                "oracle_route_map_aligned": (ctypes.c_int, [P, i64, i32, i32, i32, i64, P, P, P, P]),
+                "oracle_expand_cast_fp8_padded": (ctypes.c_int, [P, i64, i32, i32, P, P, i64, i32, P, P]),
                 "oracle_per_token_cast": (ctypes.c_int, [P, i64, i32, i32, P, P]),
                 "oracle_expand_cast_fp8": (ctypes.c_int, [P, i64, i32, i32, P, i64, i32, P, P]),
                 "oracle_swiglu_values": (ctypes.c_int, [P, i64, i32, P]),
@@ -181,6 +183,40 @@ def route_map(topk_idx, num_experts: int):
     return counts, offsets, pos, src
 
 
+def route_map_aligned(topk_idx, num_experts: int, align: int, num_rows: int | None = None):
+    """Padded expert layout: segments rounded up to `align` rows; padding
+    rows and the tail up to num_rows (default T*k + E*(align-1)) have
+    sorted_src = -1.  -> (counts, offsets [E+1], pos [T,k], sorted_src [num_rows])."""
+    idx = _as(topk_idx, np.int32)
+    T, k = idx.shape
+    E = int(num_experts)
+    R = T * k + E * (align - 1) if num_rows is None else int(num_rows)
+    counts = np.empty(E, dtype=np.int32)
+    offsets = np.empty(E + 1, dtype=np.int32)
+    pos = np.empty((T, k), dtype=np.int32)
+    src = np.empty(R, dtype=np.int32)
+    _check(_load().oracle_route_map_aligned(_ptr(idx), T, E, k, int(align), R, _ptr(counts),
+                                            _ptr(offsets), _ptr(pos), _ptr(src)),
+           "route_map_aligned")
+    return counts, offsets, pos, src
+
+
+def expand_cast_fp8_padded(x_bits, pos, sorted_src, group: int = 128, fill: int = 0xAB):
+    """Expand into the padded layout, zero-filling the rows with sorted_src < 0
+    (rows named by pos are written; nothing else should remain at `fill`)."""
+    x = _as(x_bits, np.uint16)
+    p = _as(pos, np.int32)
+    src = _as(sorted_src, np.int32)
+    T, H = x.shape
+    k = p.shape[1]
+    R = src.shape[0]
+    q = np.full((R, H), fill, dtype=np.uint8)
+    sf = np.full((R, H // group), np.nan, dtype=np.float32)
+    _check(_load().oracle_expand_cast_fp8_padded(_ptr(x), T, H, k, _ptr(p), _ptr(src), R, group,
+                                                 _ptr(q), _ptr(sf)), "expand_cast_fp8_padded")
+    return q, sf
+
+
 def per_token_cast(x_bits, group: int = 128):
     """TileKernels page, 3.2 per_token_cast: x [T, H] bf16 bits (uint16) ->
     (q [T, H] uint8 E4M3 codes, sf [T, H/group] float32)."""
@@ -251,7 +287,8 @@ def combine(y_bits, w, pos, num_rows: int | None = None):
 
 __all__ = [
     "build", "OracleError", "bf16_bits", "e4m3_value", "e4m3_decode", "e4m3_decode_fast",
-    "e4m3_encode", "bf16_from_double", "topk_gate", "route_map", "per_token_cast",
+    "e4m3_encode", "bf16_from_double", "topk_gate", "route_map", "route_map_aligned",
+    "expand_cast_fp8_padded", "per_token_cast",
     "expand_cast_fp8", "swiglu_values", "swiglu_cast_fp8", "combine",
 ]
 

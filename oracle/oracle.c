@@ -286,6 +286,57 @@ int oracle_route_map(const int32_t *topk_idx, int64_t T, int32_t E, int32_t k,
     return 0;
 }
 
+/* Padded expert layout ("CuTeDSL at Perplexity", dispatch: tokens are
+ * optionally copied into padded buffers for the MoE GEMM; TileKernels page,
+ * section 2.2: expand_to_fused zero-fills the rows no token lands on).  Each
+ * expert's segment is rounded up to a multiple of `align` rows:
+ *   offsets[0] = 0, offsets[e+1] = offsets[e] + align * ceil(counts[e] / align)
+ * pos[t,j] = offsets[e] + (copies of e before (t,j) in row-major order), and
+ * sorted_src[r] = t*k + j for r = pos[t,j], -1 for every other row in
+ * [0, num_rows).  num_rows < offsets[E] is rc 1; an index outside [0, E) is
+ * rc 2.  align = 1 is oracle_route_map with the -1 tail. */
+int oracle_route_map_aligned(const int32_t *topk_idx, int64_t T, int32_t E, int32_t k,
+                             int32_t align, int64_t num_rows, int32_t *counts,
+                             int32_t *offsets, int32_t *pos, int32_t *sorted_src)
+{
+    int64_t R, p, r;
+    int32_t e;
+    int64_t *cursor;
+
+    if (T < 0 || E < 1 || k < 1 || align < 1 || num_rows < 0)
+        return 1;
+    R = T * (int64_t)k;
+    for (e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (p = 0; p < R; ++p) {
+        int32_t x = topk_idx[p];
+        if (x < 0 || x >= E)
+            return 2;
+        counts[x] += 1;
+    }
+    offsets[0] = 0;
+    for (e = 0; e < E; ++e) {
+        int64_t padded = ((int64_t)counts[e] + align - 1) / align * align;
+        offsets[e + 1] = (int32_t)(offsets[e] + padded);
+    }
+    if (num_rows < offsets[E])
+        return 1;
+    for (r = 0; r < num_rows; ++r)
+        sorted_src[r] = -1;
+    cursor = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+    if (!cursor)
+        return 1;
+    for (p = 0; p < R; ++p) {
+        int32_t x = topk_idx[p];
+        int64_t slot = offsets[x] + cursor[x];
+        cursor[x] += 1;
+        pos[p] = (int32_t)slot;
+        sorted_src[slot] = (int32_t)p;
+    }
+    free(cursor);
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* The per-group FP8 cast (TileKernels page, sections 3.1 and 3.2)            */
 /* ------------------------------------------------------------------------ */
@@ -387,6 +438,30 @@ int oracle_expand_cast_fp8(const uint16_t *x, int64_t T, int32_t H, int32_t k,
     free(qrow);
     free(sfrow);
     return 0;
+}
+
+/* Expand into a padded layout in one pass (TileKernels page, section 2.2:
+ * the same launch copies the valid rows and zero-fills the invalid ones):
+ * every row r of [0, num_rows) with sorted_src[r] < 0 becomes all-zero codes
+ * and all-zero scales; the other rows are written as oracle_expand_cast_fp8
+ * writes them. */
+int oracle_expand_cast_fp8_padded(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                                  const int32_t *pos, const int32_t *sorted_src,
+                                  int64_t num_rows, int32_t group, uint8_t *out,
+                                  float *out_sf)
+{
+    int64_t r;
+    int32_t G;
+    if (T < 0 || k < 1 || group < 1 || H < group || H % group != 0 || num_rows < 0)
+        return 1;
+    G = H / group;
+    for (r = 0; r < num_rows; ++r) {
+        if (sorted_src[r] < 0) {
+            memset(out + r * H, 0, (size_t)H);
+            memset(out_sf + r * G, 0, sizeof(float) * (size_t)G);
+        }
+    }
+    return oracle_expand_cast_fp8(x, T, H, k, pos, num_rows, group, out, out_sf);
 }
 
 /* ------------------------------------------------------------------------ */
