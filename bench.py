@@ -571,9 +571,69 @@ def extra_workloads(L, dev, stream, sp, chk, args):
                                        "rows_per_s": round(M / (ms_s * 1e-3), 1),
                                        "GB_s": round(gbs_s, 1), "frac_of_peak": round(gbs_s / peak, 4),
                                        "timing": f"{reps} passes back to back, mean"}}
-    del hx, q2, sf2, flush
+    del hx, q2, sf2
+    torch.cuda.empty_cache()
+    res["prefill_64k_padded"] = padded_workload(L, dev, stream, sp, chk, flush, iters, peak)
+    del flush
     torch.cuda.empty_cache()
     return res
+
+
+def padded_workload(L, dev, stream, sp, chk, flush, iters, peak, align=128):
+    """route + expand + cast into the padded layout (each expert's segment
+    rounded up to `align` rows, the rest zero-filled in the expand's launch),
+    on the large-prefill inputs, with the buffers sized for the worst case
+    (T*k + E*(align-1) rows), as a caller without a host sync must."""
+    import torch
+
+    from moe_routing_precision_gb300 import ops, workloads
+    w = workloads.WORKLOADS[WORKLOAD]
+    inp = workloads.make_inputs(w, seed=0, device=dev)
+    s, x = inp["scores"], inp["x"]
+    T, E, k, H, R, G = w.T, w.E, w.k, w.H, w.R, w.G
+    NR = R + E * (align - 1)
+    i32 = dict(dtype=torch.int32, device=dev)
+    idx, wt = torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device=dev)
+    counts, offsets, pos, src = (torch.empty(E, **i32), torch.empty(E + 1, **i32),
+                                 torch.empty(T, k, **i32), torch.empty(NR, **i32))
+    ws = torch.empty(max(1, ops.route_map_workspace_bytes(T, E, k)), dtype=torch.uint8, device=dev)
+    q = torch.empty(NR, H, dtype=torch.uint8, device=dev)
+    sf = torch.empty(NR, G, dtype=torch.float32, device=dev)
+
+    def rec():
+        chk(L.moe_topk_gate(s.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
+        chk(L.moe_route_map_aligned(idx.data_ptr(), T, E, k, align, NR, counts.data_ptr(),
+                                    offsets.data_ptr(), pos.data_ptr(), src.data_ptr(),
+                                    ws.data_ptr(), ws.numel(), sp), "route")
+        chk(L.moe_expand_cast_fp8_padded(x.data_ptr(), T, H, k, pos.data_ptr(), src.data_ptr(),
+                                         NR, q.data_ptr(), sf.data_ptr(), 128, sp), "expand")
+
+    ts = []
+    for i in range(max(3, iters // 2) + 2):
+        flush.fill_(i & 0xFF)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        rec()
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 2:
+            ts.append(e0.elapsed_time(e1))
+    ms = statistics.median(ts)
+    if L.moe_get_device_status(sp, None) != 0:
+        raise RuntimeError("device error in the padded workload")
+    padded_total = int(offsets[E].item())
+    zero_rows = NR - R
+    B = algorithmic_bytes(T, E, k, H)
+    # plus: sorted_src -1 entries, the expand's scan of sorted_src, zeroed rows
+    b = B["route_expand_cast"] + zero_rows * 4 + NR * 4 + zero_rows * (H + 4 * G)
+    gbs = b / (ms * 1e-3) / 1e9
+    del inp, s, x, q, sf
+    return {"op": "topk + route_map_aligned + expand_cast_fp8_padded", "align": align,
+            "rows": NR, "padded_total": padded_total, "zero_filled_rows": zero_rows,
+            "ms": round(ms, 4), "routed_tokens_per_s": round(R / (ms * 1e-3), 1),
+            "algorithmic_bytes": b, "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "timing": "one batch after a 512 MB L2 flush, median"}
 
 
 def cpu_baseline_leg(scores, x, k, E, tokens=16384, total=65536):

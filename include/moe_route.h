@@ -84,6 +84,7 @@ typedef enum moe_out_dtype {
 #define MOE_DEVERR_EXPERT_RANGE 0x1u /* route_map: topk_idx outside [0, E)      */
 #define MOE_DEVERR_POS_RANGE 0x2u    /* expand/combine: pos >= num_rows         */
 #define MOE_DEVERR_DUPLICATE_EXPERT 0x4u /* route_map: a token names an expert twice */
+#define MOE_DEVERR_ROWS_SHORT 0x8u   /* route_map_aligned: num_rows < padded total */
 
 /*
  * moe_topk_gate -- [TK] 2.1 Top-K Gating, plus the "Weight Normalization" that
@@ -144,6 +145,32 @@ moe_status_t moe_route_map(const int32_t *topk_idx, int64_t num_tokens,
                            size_t workspace_bytes, void *stream);
 
 /*
+ * moe_route_map_aligned -- the route map into a padded expert layout, for an
+ * expert GEMM that wants every expert's rows to start on a tile boundary
+ * ([PX] dispatch: "tokens are optionally copied into padded buffers for the
+ * MoE GEMM"; [TK] 2.2: rows no token lands on are zero-filled by the expand).
+ * As moe_route_map, except that each expert's segment is rounded up to a
+ * multiple of `align` rows:
+ *   offsets[e+1]  = offsets[e] + align * ceil(counts[e] / align)
+ *   pos[t,j]      = offsets[e] + rank of the copy among e's copies
+ *   sorted_src[r] = t*k + j for r = pos[t,j]; -1 for every other row of
+ *                   [0, num_rows) (padding rows and the tail)   [num_rows] i32
+ * counts[e] is the unpadded count.  align == 1 gives moe_route_map's results
+ * (with a -1 tail when num_rows > T*k).
+ *   num_rows: rows of the padded buffers; T*k + E*(align-1) always suffices.
+ *   If it is smaller than offsets[E] the kernel sets MOE_DEVERR_ROWS_SHORT and
+ *   drops the copies that would land at or past num_rows (their pos is -1).
+ * Requires 1 <= align <= 4096, T*k + E*(align-1) < 2^31 and num_rows < 2^31;
+ * the workspace is moe_route_map_workspace_bytes(T, E, k).
+ */
+moe_status_t moe_route_map_aligned(const int32_t *topk_idx, int64_t num_tokens,
+                                   int32_t num_experts, int32_t num_topk,
+                                   int32_t align, int64_t num_rows, int32_t *counts,
+                                   int32_t *offsets, int32_t *pos, int32_t *sorted_src,
+                                   void *workspace, size_t workspace_bytes,
+                                   void *stream);
+
+/*
  * moe_route_map_noalloc -- moe_route_map for callers that cannot allocate
  * device memory.  The pages have no counterpart: it exists for callers such
  * as engine plugins or runtimes that hand out every device buffer from their
@@ -196,6 +223,22 @@ moe_status_t moe_expand_cast_fp8(const void *x, int64_t num_tokens,
                                  const int32_t *pos, int64_t num_rows,
                                  uint8_t *out, float *out_sf, int32_t group,
                                  void *stream);
+
+/*
+ * moe_expand_cast_fp8_padded -- moe_expand_cast_fp8 into a padded layout,
+ * zero-filling in the same launch every row r < num_rows with
+ * sorted_src[r] < 0 ([TK] 2.2: the expand kernel's grid covers max(T, rows)
+ * so that the invalid rows are zeroed without another launch).  Those rows get
+ * all-zero codes and all-zero scales; rows named by pos are written as
+ * moe_expand_cast_fp8 writes them.  sorted_src: [num_rows] i32 as
+ * moe_route_map_aligned returns it.  Same requirements and error bits as
+ * moe_expand_cast_fp8.
+ */
+moe_status_t moe_expand_cast_fp8_padded(const void *x, int64_t num_tokens,
+                                        int32_t hidden, int32_t num_topk,
+                                        const int32_t *pos, const int32_t *sorted_src,
+                                        int64_t num_rows, uint8_t *out, float *out_sf,
+                                        int32_t group, void *stream);
 
 /*
  * swiglu_cast_fp8 -- [TK] 3.3, plain form (no clamp, no top-k weight).  For

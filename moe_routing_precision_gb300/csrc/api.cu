@@ -141,6 +141,64 @@ moe_status_t moe_route_map(const int32_t* topk_idx, int64_t num_tokens, int32_t 
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
+moe_status_t moe_route_map_aligned(const int32_t* topk_idx, int64_t num_tokens,
+                                   int32_t num_experts, int32_t num_topk, int32_t align,
+                                   int64_t num_rows, int32_t* counts, int32_t* offsets,
+                                   int32_t* pos, int32_t* sorted_src, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (num_tokens < 0 || !experts_ok(num_experts, num_topk)) return MOE_ERR_INVALID_ARG;
+  if (align < 1 || align > 4096 || num_rows < 0 || num_rows >= ((int64_t)1 << 31))
+    return MOE_ERR_INVALID_ARG;
+  if (num_tokens * (int64_t)num_topk + (int64_t)num_experts * (align - 1) >= ((int64_t)1 << 31))
+    return MOE_ERR_INVALID_ARG;
+  if (num_tokens == 0) {
+    if (num_rows > 0) return MOE_ERR_UNSUPPORTED;  // nothing to route: no padded rows either
+    return moe_route_map(topk_idx, 0, num_experts, num_topk, counts, offsets, pos, sorted_src,
+                         workspace, workspace_bytes, stream);
+  }
+  if (!topk_idx || !counts || !offsets || !pos || !sorted_src || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_idx, 4) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(pos, 4) ||
+      !aligned(sorted_src, 4) || !aligned(workspace, 16))
+    return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < moe_route_map_workspace_bytes(num_tokens, num_experts, num_topk))
+    return MOE_ERR_INVALID_ARG;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  cudaError_t e = launch_route_map_aligned(c, topk_idx, num_tokens, num_experts, num_topk, align,
+                                           num_rows, counts, offsets, pos, sorted_src,
+                                           static_cast<int32_t*>(workspace),
+                                           route_num_chunks(num_tokens));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status_t moe_expand_cast_fp8_padded(const void* x, int64_t num_tokens, int32_t hidden,
+                                        int32_t num_topk, const int32_t* pos,
+                                        const int32_t* sorted_src, int64_t num_rows,
+                                        uint8_t* out, float* out_sf, int32_t group,
+                                        void* stream) {
+  if (group != MOE_CAST_GROUP) return MOE_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || num_rows < 0 || hidden < MOE_CAST_GROUP || hidden % MOE_CAST_GROUP != 0 ||
+      num_topk < 1 || num_topk > MOE_MAX_TOPK)
+    return MOE_ERR_INVALID_ARG;
+  if (num_rows >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
+  if (num_tokens * (hidden / MOE_CAST_GROUP) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (num_tokens == 0 && num_rows == 0) return MOE_OK;
+  if ((num_tokens > 0 && (!x || !pos)) || (num_rows > 0 && (!out || !out_sf || !sorted_src)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(pos, 4) || !aligned(sorted_src, 4) || !aligned(out, 16) ||
+      !aligned(out_sf, 4))
+    return MOE_ERR_INVALID_ARG;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  // with no tokens the kernels still run once over the rows to zero them
+  cudaError_t e = launch_expand_cast(c, x, num_tokens, hidden, num_topk, pos, num_rows, out,
+                                     out_sf, sorted_src);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
 moe_status_t moe_expand_cast_fp8(const void* x, int64_t num_tokens, int32_t hidden,
                                  int32_t num_topk, const int32_t* pos, int64_t num_rows,
                                  uint8_t* out, float* out_sf, int32_t group, void* stream) {

@@ -180,8 +180,13 @@ cudaError_t launch_topk_gate(const LaunchCtx& c, const float* scores, int64_t T,
 cudaError_t launch_route_map(const LaunchCtx& c, const int32_t* idx, int64_t T, int E, int k,
                              int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* sorted_src,
                              int32_t* ws, int64_t num_chunks);
+cudaError_t launch_route_map_aligned(const LaunchCtx& c, const int32_t* idx, int64_t T, int E,
+                                     int k, int align, int64_t num_rows, int32_t* counts,
+                                     int32_t* offsets, int32_t* pos, int32_t* sorted_src,
+                                     int32_t* ws, int64_t num_chunks);
 cudaError_t launch_expand_cast(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
-                               const int32_t* pos, int64_t R, uint8_t* out, float* out_sf);
+                               const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
+                               const int32_t* zero_rows = nullptr);
 cudaError_t launch_swiglu_cast(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
                                float* out_sf);
 cudaError_t launch_combine(const LaunchCtx& c, const void* y, const float* w, const int32_t* pos,

@@ -53,13 +53,40 @@ __device__ __forceinline__ void load_tile(const uint16_t* __restrict__ x,
   }
 }
 
+// Padded layouts (TileKernels article, section 2.2: expand_to_fused zero-fills
+// the rows no token lands on in the same launch).  With zsrc non-null, every
+// row r < num_rows whose zsrc[r] (the route map's sorted_src) is negative gets
+// all-zero codes and scales.  Warp-granular: a warp reads 32 entries with one
+// coalesced load and zeroes each marked row 512 bytes per store instruction.
+// These rows are disjoint from every row a copy is written to.
+__device__ __forceinline__ void zero_fill_rows(const int32_t* __restrict__ zsrc, int64_t num_rows,
+                                               int H, int G, uint8_t* __restrict__ out,
+                                               float* __restrict__ out_sf, int64_t gwarp,
+                                               int64_t nwarps, int lane) {
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (int64_t r0 = gwarp * 32; r0 < num_rows; r0 += nwarps * 32) {
+    const int64_t r = r0 + lane;
+    const bool z = r < num_rows && __ldg(zsrc + r) < 0;
+    unsigned m = __ballot_sync(0xFFFFFFFFu, z);
+    while (m) {
+      const int i = __ffs(m) - 1;
+      m &= m - 1;
+      uint8_t* q = out + (r0 + i) * H;
+      for (int c = lane * 16; c < H; c += 512) st_stream_v4(q + c, zero);
+      float* sfr = out_sf + (r0 + i) * G;
+      for (int g = lane; g < G; g += 32) st_stream_f32(sfr + g, 0.0f);
+    }
+  }
+}
+
 // G4: G % 4 == 0 (and out_sf 16-byte aligned), so a warp's 4 units are 4
 // consecutive groups of one token and their 4 scales form one aligned 16-byte
 // vector per destination row.
 template <bool G4>
 __global__ void __launch_bounds__(kThreads) expand_cast_kernel(
     const uint16_t* __restrict__ x, uint32_t units, int H, int k, const int32_t* __restrict__ pos,
-    int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf, FastDiv fdG, unsigned* err) {
+    int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf, FastDiv fdG,
+    const int32_t* __restrict__ zsrc, unsigned* err) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
   const int sub = lane >> 3;  // unit within the warp's tile
@@ -113,6 +140,12 @@ __global__ void __launch_bounds__(kThreads) expand_cast_kernel(
       }
     }
   }
+  // warps numbered CTA-major, so consecutive 32-row groups (the all-padding
+  // tail is one contiguous run) go to different CTAs instead of a few late ones
+  if (zsrc != nullptr)
+    zero_fill_rows(zsrc, R, H, H >> 7, out, out_sf,
+                   (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x,
+                   ((int64_t)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31);
   if (bad) flag_error(err, MOE_DEVERR_POS_RANGE);
 }
 
@@ -125,7 +158,8 @@ __global__ void __launch_bounds__(kThreads) expand_cast_kernel(
 template <bool G4>
 __global__ void __launch_bounds__(1024) expand_cast_rows_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
-    int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf, int tpc, unsigned* err) {
+    int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf, int tpc,
+    const int32_t* __restrict__ zsrc, unsigned* err) {
   pdl_enter();
   const int P = H >> 4;  // threads per token
   const int G = H >> 7;
@@ -194,6 +228,12 @@ __global__ void __launch_bounds__(1024) expand_cast_rows_kernel(
       }
     }
   }
+  // warps numbered CTA-major, so consecutive 32-row groups (the all-padding
+  // tail is one contiguous run) go to different CTAs instead of a few late ones
+  if (zsrc != nullptr)
+    zero_fill_rows(zsrc, R, H, H >> 7, out, out_sf,
+                   (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x,
+                   ((int64_t)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31);
   if (bad) flag_error(err, MOE_DEVERR_POS_RANGE);
 }
 
@@ -216,7 +256,8 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t byt
 template <int NBUF>
 __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
-    int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf, unsigned* err) {
+    int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf,
+    const int32_t* __restrict__ zsrc, unsigned* err) {
   extern __shared__ __align__(128) uint8_t s_buf[];
   pdl_enter();
   const int P = H >> 4;  // threads per token
@@ -286,6 +327,12 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
   }
   // the copies read shared memory until they complete: wait before exiting
   if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  // warps numbered CTA-major, so consecutive 32-row groups (the all-padding
+  // tail is one contiguous run) go to different CTAs instead of a few late ones
+  if (zsrc != nullptr)
+    zero_fill_rows(zsrc, R, H, H >> 7, out, out_sf,
+                   (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x,
+                   ((int64_t)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31);
   if (bad) flag_error(err, MOE_DEVERR_POS_RANGE);
 }
 
@@ -298,7 +345,7 @@ constexpr int kBulkCtasPerSm = 3;
 template <int NBUF>
 cudaError_t launch_bulk(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                         const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
-                        int ctas_per_sm) {
+                        int ctas_per_sm, const int32_t* zsrc) {
   const int P = H / 16;
   const int threads = (P + 31) / 32 * 32;
   const int G = H / kGroup;
@@ -310,9 +357,9 @@ cudaError_t launch_bulk(const LaunchCtx& c, const void* x, int64_t T, int H, int
     if (st != cudaSuccess) return st;
   }
   const int64_t cap = (int64_t)c.num_sms * ctas_per_sm;
-  const int blocks = (int)(T < cap ? T : cap);
+  const int blocks = (int)(T < cap ? (T > 0 ? T : 1) : cap);  // >= 1: zero-fill with T = 0
   return launch_pdl(expand_cast_bulk_kernel<NBUF>, blocks, threads, smem, c.stream,
-                    static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, c.err);
+                    static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, zsrc, c.err);
 }
 
 // CTAs per SM for the row form, measured on GB300 (prefill-sized expand).
@@ -321,20 +368,22 @@ constexpr int kRowCtasPerSm = 1;
 template <bool G4>
 cudaError_t launch_rows(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                         const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
-                        int ctas_per_sm) {
+                        int ctas_per_sm, const int32_t* zsrc) {
   const int P = H / 16;
   const int tpc = P >= 256 ? 1 : 256 / P;
   const int64_t groups = (T + tpc - 1) / tpc;
   const int64_t cap = (int64_t)c.num_sms * ctas_per_sm;
-  const int blocks = (int)(groups < cap ? groups : cap);
+  const int blocks = (int)(groups < cap ? (groups > 0 ? groups : 1) : cap);  // >= 1: zero-fill
   const int threads = (P * tpc + 31) / 32 * 32;  // whole warps: the shuffles use full masks
   return launch_pdl(expand_cast_rows_kernel<G4>, blocks, threads, 0, c.stream,
-                    static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, tpc, c.err);
+                    static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, tpc, zsrc,
+                    c.err);
 }
 
 template <bool G4>
 cudaError_t launch_g(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
-                     const int32_t* pos, int64_t R, uint8_t* out, float* out_sf) {
+                     const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
+                     const int32_t* zsrc) {
   const int G = H / kGroup;
   const uint32_t units = (uint32_t)(T * G);  // < 2^31, checked by the caller
   const uint32_t tiles = (units + 3) / 4;
@@ -344,26 +393,28 @@ cudaError_t launch_g(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                                                                  kThreads, 0);
   if (st != cudaSuccess) return st;
   const int64_t cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
-  const int blocks = (int)(need < cap ? need : cap);
+  const int blocks = (int)(need < cap ? (need > 0 ? need : 1) : cap);  // >= 1: zero-fill with T = 0
   return launch_pdl(expand_cast_kernel<G4>, blocks, kThreads, 0, c.stream,
                     static_cast<const uint16_t*>(x), units, H, k, pos, R, out, out_sf,
-                    FastDiv((uint32_t)G), c.err);
+                    FastDiv((uint32_t)G), zsrc, c.err);
 }
 
 }  // namespace
 
 cudaError_t launch_expand_cast(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
-                               const int32_t* pos, int64_t R, uint8_t* out, float* out_sf) {
+                               const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
+                               const int32_t* zero_rows) {
   // the 16-byte scale store needs G % 4 == 0 and a 16-byte aligned out_sf
   const bool g4 = (H / kGroup) % 4 == 0 && (reinterpret_cast<uintptr_t>(out_sf) % 16) == 0;
   const bool aligned16 = (reinterpret_cast<uintptr_t>(out) % 16) == 0;
   if (H <= 16384 && g4 && aligned16)
-    return launch_bulk<kBulkBuffers>(c, x, T, H, k, pos, R, out, out_sf, kBulkCtasPerSm);
+    return launch_bulk<kBulkBuffers>(c, x, T, H, k, pos, R, out, out_sf, kBulkCtasPerSm,
+                                     zero_rows);
   if (H <= 16384)
-    return g4 ? launch_rows<true>(c, x, T, H, k, pos, R, out, out_sf, kRowCtasPerSm)
-              : launch_rows<false>(c, x, T, H, k, pos, R, out, out_sf, kRowCtasPerSm);
-  return g4 ? launch_g<true>(c, x, T, H, k, pos, R, out, out_sf)
-            : launch_g<false>(c, x, T, H, k, pos, R, out, out_sf);
+    return g4 ? launch_rows<true>(c, x, T, H, k, pos, R, out, out_sf, kRowCtasPerSm, zero_rows)
+              : launch_rows<false>(c, x, T, H, k, pos, R, out, out_sf, kRowCtasPerSm, zero_rows);
+  return g4 ? launch_g<true>(c, x, T, H, k, pos, R, out, out_sf, zero_rows)
+            : launch_g<false>(c, x, T, H, k, pos, R, out, out_sf, zero_rows);
 }
 
 }  // namespace moe

@@ -71,8 +71,9 @@ __device__ __forceinline__ int32_t warp_incl_scan(int32_t v, int lane) {
 
 __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(
     const int32_t* __restrict__ idx, int64_t T, int E, int k, int chunk_tokens, int num_chunks,
-    const int32_t* __restrict__ hist, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ pos, int32_t* __restrict__ sorted_src, unsigned* err) {
+    int align, int64_t num_rows, const int32_t* __restrict__ hist, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ pos, int32_t* __restrict__ sorted_src,
+    unsigned* err) {
   extern __shared__ int32_t smem[];
   int32_t* s_off = smem;                                     // [E] totals, then offsets
   int32_t* s_base = smem + E;                                // [E] copies in earlier chunks
@@ -84,7 +85,6 @@ __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x;
-  const int64_t R = T * k;
   const int64_t t = (int64_t)b * chunk_tokens + warp * 32 + lane;  // this lane's token
   const bool tok = (warp * 32 < chunk_tokens) && t < T;
 
@@ -171,12 +171,14 @@ __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(
   }
   __syncthreads();
 
-  // ---- offsets: exclusive scan of the totals, kRankThreads at a time
+  // ---- offsets: exclusive scan of the totals rounded up to `align` (1 for
+  // the plain layout), kRankThreads at a time
   if (tid == 0) s_carry = 0;
   __syncthreads();
   for (int base = 0; base < E; base += kRankThreads) {
     const int e = base + tid;
-    const int32_t v = (e < E) ? s_off[e] : 0;
+    const int32_t cnt = (e < E) ? s_off[e] : 0;
+    const int32_t v = (cnt + align - 1) / align * align;
     const int32_t incl = warp_incl_scan(v, lane);
     if (lane == 31) s_warp_tot[warp] = incl;
     __syncthreads();
@@ -188,7 +190,11 @@ __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(
     __syncthreads();
     const int32_t excl = s_carry + s_warp_tot[warp] + incl - v;
     if (e < E) s_off[e] = excl;
-    if (b == 0 && e < E) counts[e] = v;
+    if (b == 0 && e < E) counts[e] = cnt;
+    // this expert's padding rows, written by one CTA
+    if (e < E && e % num_chunks == b)
+      for (int64_t r = (int64_t)excl + cnt; r < (int64_t)excl + v && r < num_rows; ++r)
+        sorted_src[r] = -1;
     __syncthreads();
     if (tid == kRankThreads - 1) s_carry = excl + v;
     __syncthreads();
@@ -196,7 +202,12 @@ __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(
   if (b == 0) {
     for (int e = tid; e < E; e += kRankThreads) offsets[e] = s_off[e];
     if (tid == 0) offsets[E] = s_carry;
+    if (tid == 0 && (int64_t)s_carry > num_rows) flag_error(err, MOE_DEVERR_ROWS_SHORT);
   }
+  // rows past the padded total, up to num_rows, are not any copy's
+  for (int64_t r = (int64_t)s_carry + (int64_t)b * kRankThreads + tid; r < num_rows;
+       r += (int64_t)num_chunks * kRankThreads)
+    sorted_src[r] = -1;
   // ---- start of each word's copies of e: offset + chunk base + earlier words
   for (int e = tid; e < E; e += kRankThreads) {
     int32_t run = s_off[e] + s_base[e];
@@ -224,9 +235,10 @@ __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(
         continue;
       }
       const int32_t slot = s_wpre[warp * E + e] + __popc(s_word[warp * E + e] & below);
-      // slot < R whenever topk_idx is unchanged since the count kernel read
-      // it; a caller who rewrote it in between gets a flag, not a wild write
-      if ((unsigned)slot < (unsigned)R) {
+      // slot < num_rows whenever num_rows covers the padded total and
+      // topk_idx is unchanged since the count kernel read it; otherwise a flag,
+      // not a wild write
+      if ((int64_t)slot < num_rows && slot >= 0) {
         pos[p] = slot;
         sorted_src[slot] = (int32_t)p;
       } else {
@@ -240,9 +252,10 @@ __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(
 
 }  // namespace
 
-cudaError_t launch_route_map(const LaunchCtx& c, const int32_t* idx, int64_t T, int E, int k,
-                             int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* sorted_src,
-                             int32_t* ws, int64_t num_chunks) {
+cudaError_t launch_route_map_aligned(const LaunchCtx& c, const int32_t* idx, int64_t T, int E,
+                                     int k, int align, int64_t num_rows, int32_t* counts,
+                                     int32_t* offsets, int32_t* pos, int32_t* sorted_src,
+                                     int32_t* ws, int64_t num_chunks) {
   const int64_t R = T * k;
   const int chunk_tokens = (int)route_chunk_tokens(T);
   const size_t count_smem = sizeof(int32_t) * E;
@@ -256,8 +269,15 @@ cudaError_t launch_route_map(const LaunchCtx& c, const int32_t* idx, int64_t T, 
     if (st != cudaSuccess) return st;
   }
   return launch_pdl(route_rank_kernel, (unsigned)num_chunks, kRankThreads, rank_smem, c.stream,
-                    idx, T, E, k, chunk_tokens, (int)num_chunks, ws, counts, offsets, pos,
-                    sorted_src, c.err);
+                    idx, T, E, k, chunk_tokens, (int)num_chunks, align, num_rows, ws, counts,
+                    offsets, pos, sorted_src, c.err);
+}
+
+cudaError_t launch_route_map(const LaunchCtx& c, const int32_t* idx, int64_t T, int E, int k,
+                             int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* sorted_src,
+                             int32_t* ws, int64_t num_chunks) {
+  return launch_route_map_aligned(c, idx, T, E, k, 1, T * k, counts, offsets, pos, sorted_src, ws,
+                                  num_chunks);
 }
 
 }  // namespace moe

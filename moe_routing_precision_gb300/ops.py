@@ -21,6 +21,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE =
 MOE_WEIGHTS_NONE, MOE_WEIGHTS_SOFTMAX_TOPK = 0, 1
 MOE_OUT_BF16, MOE_OUT_F32 = 0, 1
 MOE_DEVERR_EXPERT_RANGE, MOE_DEVERR_POS_RANGE, MOE_DEVERR_DUPLICATE_EXPERT = 0x1, 0x2, 0x4
+MOE_DEVERR_ROWS_SHORT = 0x8
 GROUP = 128
 
 # Every symbol declared in include/moe_route.h, with its ctypes signature.
@@ -32,6 +33,10 @@ SIGNATURES = {
     "moe_route_map": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _P, _P, _P, _P, _sz, _P]),
     "moe_route_map_noalloc": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _P, _P, _P, _P]),
     "moe_expand_cast_fp8": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _i64, _P, _P, _i32, _P]),
+    "moe_route_map_aligned": (ctypes.c_int, [_P, _i64, _i32, _i32, _i32, _i64, _P, _P, _P, _P,
+                                             _P, _sz, _P]),
+    "moe_expand_cast_fp8_padded": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _P, _i64, _P, _P,
+                                                  _i32, _P]),
     "swiglu_cast_fp8": (ctypes.c_int, [_P, _i64, _i32, _P, _P, _i32, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _i64, _i32, _i32, _i64, _P, _i32, _P]),
     "moe_peak_copy": (ctypes.c_int, [_P, _P, _sz, _P]),
@@ -165,6 +170,51 @@ def route_map(topk_idx: torch.Tensor, num_experts: int, *, workspace=None, out=N
     return counts, offsets, pos, src
 
 
+def route_map_aligned(topk_idx: torch.Tensor, num_experts: int, align: int,
+                      num_rows: int | None = None, *, workspace=None, stream=None):
+    """Route map into a padded layout: each expert's segment rounded up to a
+    multiple of `align` rows.  num_rows defaults to T*k + E*(align-1), which
+    always suffices.  -> (counts [E], offsets [E+1] padded, pos [T, k],
+    sorted_src [num_rows], -1 on padding rows), all int32."""
+    _dev(topk_idx, "topk_idx", torch.int32)
+    T, k = topk_idx.shape
+    E = int(num_experts)
+    R = T * k + E * (align - 1) if num_rows is None else int(num_rows)
+    counts = _empty((E,), torch.int32, topk_idx)
+    offsets = _empty((E + 1,), torch.int32, topk_idx)
+    pos = _empty((T, k), torch.int32, topk_idx)
+    src = _empty((R,), torch.int32, topk_idx)
+    need = route_map_workspace_bytes(T, E, k)
+    if workspace is None:
+        workspace = _empty((max(need, 1),), torch.uint8, topk_idx)
+    _dev(workspace, "workspace", torch.uint8)
+    rc = lib().moe_route_map_aligned(_ptr(topk_idx), T, E, k, int(align), R, _ptr(counts),
+                                     _ptr(offsets), _ptr(pos), _ptr(src), _ptr(workspace),
+                                     workspace.numel(), _stream(stream))
+    _check(rc, "moe_route_map_aligned")
+    return counts, offsets, pos, src
+
+
+def expand_cast_fp8_padded(x: torch.Tensor, pos: torch.Tensor, sorted_src: torch.Tensor, *,
+                           out=None, out_sf=None, stream=None):
+    """expand_cast_fp8 into a padded layout of len(sorted_src) rows, zeroing
+    (codes and scales) every row whose sorted_src entry is negative."""
+    _dev(x, "x", torch.bfloat16)
+    _dev(pos, "pos", torch.int32)
+    _dev(sorted_src, "sorted_src", torch.int32)
+    T, H = x.shape
+    k = pos.shape[1]
+    R = sorted_src.shape[0]
+    q = out if out is not None else _empty((R, H), torch.uint8, x)
+    sf = out_sf if out_sf is not None else _empty((R, H // GROUP), torch.float32, x)
+    _dev(q, "out", torch.uint8, (R, H))
+    _dev(sf, "out_sf", torch.float32, (R, H // GROUP))
+    rc = lib().moe_expand_cast_fp8_padded(_ptr(x), T, H, k, _ptr(pos), _ptr(sorted_src), R,
+                                          _ptr(q), _ptr(sf), GROUP, _stream(stream))
+    _check(rc, "moe_expand_cast_fp8_padded")
+    return q, sf
+
+
 def expand_cast_fp8(x: torch.Tensor, pos: torch.Tensor, num_rows: int | None = None, *,
                     out=None, out_sf=None, stream=None):
     """Per-token E4M3 cast (one fp32 scale per 128 channels) written to the
@@ -251,5 +301,6 @@ def launch_count() -> int:
 
 
 __all__ = ["lib", "MoeError", "topk_gate", "route_map", "route_map_workspace_bytes",
+           "route_map_aligned", "expand_cast_fp8_padded",
            "expand_cast_fp8", "swiglu_cast_fp8", "combine", "peak_copy", "device_status",
            "launch_count", "SIGNATURES"]

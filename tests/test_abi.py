@@ -141,3 +141,19 @@ def test_binding_refuses_cpu_tensors():
         ops.topk_gate(torch.zeros(4, 16), 2)
     with pytest.raises(ValueError, match="CUDA"):
         ops.swiglu_cast_fp8(torch.zeros(4, 256, dtype=torch.bfloat16))
+
+
+def test_padded_entry_points_reject_bad_arguments(L):
+    f = L.moe_route_map_aligned
+    ws = L.moe_route_map_workspace_bytes(100, 16, 2)
+    args = lambda align, rows: (FAKE, 100, 16, 2, align, rows, FAKE, FAKE, FAKE, FAKE, FAKE, ws, None)
+    assert f(*args(0, 1000)) == INVALID                  # align 0
+    assert f(*args(8192, 1000)) == INVALID               # align > 4096
+    assert f(*args(4, -1)) == INVALID                    # negative rows
+    assert f(*args(4, 1 << 31)) == INVALID               # rows >= 2^31
+    assert f(FAKE, 100, 16, 2, 4, 1000, FAKE, FAKE, FAKE, None, FAKE, ws, None) == INVALID
+    g = L.moe_expand_cast_fp8_padded
+    assert g(FAKE, 4, 256, 2, FAKE, FAKE, 20, FAKE, FAKE, 64, None) == UNSUPPORTED
+    assert g(FAKE, 4, 256, 2, FAKE, None, 20, FAKE, FAKE, 128, None) == INVALID   # no sorted_src
+    assert g(FAKE, 4, 256, 2, FAKE, FAKE + 2, 20, FAKE, FAKE, 128, None) == INVALID
+    assert g(None, 0, 256, 2, None, None, 0, None, None, 128, None) == 0          # nothing to do

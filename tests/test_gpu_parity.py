@@ -351,3 +351,68 @@ def test_swiglu_workload_sampled_rows():
     assert frac <= 1e-3
     del inp, q, sf
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- padded layout
+
+@pytest.mark.parametrize("T,E,k,align", [(1000, 256, 8, 128), (37, 16, 2, 4), (513, 33, 3, 32),
+                                         (300, 1024, 32, 64), (129, 16, 2, 1), (5, 64, 4, 256)])
+def test_route_map_aligned_parity(T, E, k, align):
+    idx = _random_idx(T, E, k, seed=T + E + align)
+    got = ops.route_map_aligned(idx.to(DEV), E, align)
+    ref = oracle.route_map_aligned(idx.numpy(), E, align)
+    for name, a, b in zip(("counts", "offsets", "pos", "sorted_src"), got, ref):
+        assert_equal(np_(a), b, name)
+    assert ops.device_status() == 0
+
+
+def test_route_map_aligned_flags_short_buffer():
+    T, E, k, align = 64, 16, 2, 128
+    idx = _random_idx(T, E, k, seed=3).to(DEV)
+    counts, offsets, pos, src = ops.route_map_aligned(idx, E, align, num_rows=T * k)
+    assert ops.device_status() & ops.MOE_DEVERR_ROWS_SHORT
+    p = np_(pos)
+    assert ((p == -1) | ((p >= 0) & (p < T * k))).all()
+
+
+@pytest.mark.parametrize("T,E,k,H,align", [(200, 64, 8, 7168, 128), (37, 16, 2, 256, 16),
+                                           (64, 8, 4, 512, 128), (33, 32, 3, 384, 8)])
+def test_expand_padded_parity(T, E, k, H, align):
+    inp = workloads.random_small(T, E, k, H, seed=T + H + align, zero_groups=True)
+    x = inp["x"]
+    idx = _random_idx(T, E, k, seed=T + align)
+    _, _, o_pos, o_src = oracle.route_map_aligned(idx.numpy(), E, align)
+    R = o_src.size
+    q = torch.full((R, H), 0xAB, dtype=torch.uint8, device=DEV)
+    sf = torch.full((R, H // 128), float("nan"), device=DEV)
+    _, _, pos, src = ops.route_map_aligned(idx.to(DEV), E, align)
+    ops.expand_cast_fp8_padded(x.to(DEV), pos, src, out=q, out_sf=sf)
+    assert ops.device_status() == 0
+    o_q, o_sf = oracle.expand_cast_fp8_padded(bits(x), o_pos, o_src)
+    assert_equal(np_(q), o_q, "padded q")
+    assert_f32_bits_equal(np_(sf), o_sf, "padded sf")
+
+
+def test_expand_padded_no_tokens_zero_fills():
+    H, R = 512, 100
+    src = torch.full((R,), -1, dtype=torch.int32, device=DEV)
+    q = torch.full((R, H), 0xAB, dtype=torch.uint8, device=DEV)
+    sf = torch.full((R, H // 128), 7.0, device=DEV)
+    ops.expand_cast_fp8_padded(torch.empty(0, H, dtype=torch.bfloat16, device=DEV),
+                               torch.empty(0, 2, dtype=torch.int32, device=DEV), src,
+                               out=q, out_sf=sf)
+    assert int(q.abs().sum()) == 0 and float(sf.abs().sum()) == 0.0
+
+
+def test_padded_chain_feeds_combine():
+    # the padded pos works unchanged for combine (rows are looked up by pos)
+    w = workloads.WORKLOADS["tiny"]
+    inp = workloads.make_inputs(w, seed=0, device=DEV)
+    idx, wt = ops.topk_gate(inp["scores"], w.k)
+    _, offsets, pos, src = ops.route_map_aligned(idx, w.E, 16)
+    R = src.shape[0]
+    g = torch.Generator().manual_seed(0)
+    y = torch.randn(R, w.H, generator=g).to(torch.bfloat16)
+    out = ops.combine(y.to(DEV), wt, pos, torch.float32)
+    o32, _, mag = oracle.combine(bits(y), np_(wt), np_(pos))
+    check_combine_f32(np_(out), o32, mag)
