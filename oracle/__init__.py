@@ -59,6 +59,10 @@ def _load():
                 "oracle_route_map": (ctypes.c_int, [P, i64, i32, i32, P, P, P, P]),
                 "oracle_route_map_aligned": (ctypes.c_int, [P, i64, i32, i32, i32, i64, P, P, P, P]),
                 "oracle_expand_cast_fp8_padded": (ctypes.c_int, [P, i64, i32, i32, P, P, i64, i32, P, P]),
+                "oracle_expand_cast_fp8_ex": (ctypes.c_int, [P, i64, i32, i32, P, P, i64, i32, i32,
+                                                             i64, P, P]),
+                "oracle_swiglu_cast_fp8_ex": (ctypes.c_int, [P, i64, i32, i32, i32, ctypes.c_float, P,
+                                                             i32, i64, P, P, P]),
                 "oracle_per_token_cast": (ctypes.c_int, [P, i64, i32, i32, P, P]),
                 "oracle_expand_cast_fp8": (ctypes.c_int, [P, i64, i32, i32, P, i64, i32, P, P]),
                 "oracle_swiglu_values": (ctypes.c_int, [P, i64, i32, P]),
@@ -217,6 +221,58 @@ def expand_cast_fp8_padded(x_bits, pos, sorted_src, group: int = 128, fill: int 
     return q, sf
 
 
+SF_COLMAJOR, SF_POW2, SF_UE8M0 = 1, 2, 4
+
+
+def sf_buffer(rows: int, G: int, flags: int, ld: int | None = None):
+    """An empty scale buffer of the layout `flags` names (filled with a
+    sentinel: NaN for f32, 0xAB for bytes) and its leading dimension."""
+    ld = rows if ld is None else ld
+    if flags & SF_UE8M0:
+        if flags & SF_COLMAJOR:
+            return np.full((-(-G // 4), ld, 4), 0xAB, np.uint8), ld
+        return np.full((rows, G), 0xAB, np.uint8), ld
+    if flags & SF_COLMAJOR:
+        return np.full((G, ld), np.nan, np.float32), ld
+    return np.full((rows, G), np.nan, np.float32), ld
+
+
+def expand_cast_fp8_ex(x_bits, pos, num_rows: int | None = None, sorted_src=None,
+                       flags: int = 0, ld: int | None = None, group: int = 128, fill: int = 0xAB):
+    """Expand + cast with scale options (SF_COLMAJOR, SF_POW2, SF_UE8M0) and an
+    optional zero-fill of the rows with sorted_src < 0.
+    -> (q [R, H] uint8, scales in the flagged layout)."""
+    x = _as(x_bits, np.uint16)
+    p = _as(pos, np.int32)
+    T, H = x.shape
+    k = p.shape[1]
+    R = (T * k if sorted_src is None else len(sorted_src)) if num_rows is None else int(num_rows)
+    src = None if sorted_src is None else _as(sorted_src, np.int32)
+    q = np.full((R, H), fill, dtype=np.uint8)
+    sf, ld = sf_buffer(R, H // group, flags, ld)
+    _check(_load().oracle_expand_cast_fp8_ex(_ptr(x), T, H, k, _ptr(p), _ptr(src), R, group,
+                                             int(flags), int(ld), _ptr(q), _ptr(sf)),
+           "expand_cast_fp8_ex")
+    return q, sf
+
+
+def swiglu_cast_fp8_ex(x_bits, clamp: float | None = None, weights=None, flags: int = 0,
+                       ld: int | None = None, group: int = 128):
+    """SwiGLU with optional clamp and per-row weight, then the cast with scale
+    options.  -> (q [M, N], scales in the flagged layout, clamp count)."""
+    x = _as(x_bits, np.uint16)
+    M, N2 = x.shape
+    N = N2 // 2
+    w = None if weights is None else _as(np.asarray(weights, np.float32), np.float32)
+    q = np.empty((M, N), dtype=np.uint8)
+    sf, ld = sf_buffer(M, N // group, flags, ld)
+    cnt = np.zeros(1, dtype=np.uint64)
+    _check(_load().oracle_swiglu_cast_fp8_ex(_ptr(x), M, N, group, int(clamp is not None),
+                                             float(clamp or 0.0), _ptr(w), int(flags), int(ld),
+                                             _ptr(q), _ptr(sf), _ptr(cnt)), "swiglu_cast_fp8_ex")
+    return q, sf, int(cnt[0])
+
+
 def per_token_cast(x_bits, group: int = 128):
     """TileKernels page, 3.2 per_token_cast: x [T, H] bf16 bits (uint16) ->
     (q [T, H] uint8 E4M3 codes, sf [T, H/group] float32)."""
@@ -288,7 +344,8 @@ def combine(y_bits, w, pos, num_rows: int | None = None):
 __all__ = [
     "build", "OracleError", "bf16_bits", "e4m3_value", "e4m3_decode", "e4m3_decode_fast",
     "e4m3_encode", "bf16_from_double", "topk_gate", "route_map", "route_map_aligned",
-    "expand_cast_fp8_padded", "per_token_cast",
+    "expand_cast_fp8_padded", "expand_cast_fp8_ex", "swiglu_cast_fp8_ex", "sf_buffer",
+    "SF_COLMAJOR", "SF_POW2", "SF_UE8M0", "per_token_cast",
     "expand_cast_fp8", "swiglu_values", "swiglu_cast_fp8", "combine",
 ]
 

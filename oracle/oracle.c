@@ -364,6 +364,142 @@ static float cast_group(const float *v, int n, uint8_t *q)
     return sf;
 }
 
+/* ---- cast options (TileKernels page, section 3.1: CastOutputConfig's
+ * round_sf and packed UE8M0; section 2.2: the TMA-aligned column-major scale
+ * layout expand_to_fused can write).  Flags:
+ *   ORACLE_SF_COLMAJOR (1): scales stored transposed, [G][ld] (ld >= rows)
+ *   ORACLE_SF_POW2     (2): round_sf: the scale is the smallest power of two
+ *                           >= fl32(max(amax, 1e-4) / 448)
+ *   ORACLE_SF_UE8M0    (4): store the (power-of-two) scale as its biased
+ *                           exponent byte (UE8M0: value 2^(byte - 127));
+ *                           row-major [rows][G] bytes, or with COLMAJOR four
+ *                           consecutive groups of a row packed in one 32-bit
+ *                           word (group 4i + j in byte j), [ceil(G/4)][ld]. */
+#define ORACLE_SF_COLMAJOR 1
+#define ORACLE_SF_POW2 2
+#define ORACLE_SF_UE8M0 4
+
+/* The power of two >= s (s positive, finite), by its definition. */
+static float pow2_at_least(float s)
+{
+    float p = 1.0f;
+    while (p < s)
+        p *= 2.0f;
+    while (p / 2.0f >= s)
+        p /= 2.0f;
+    return p;
+}
+
+/* Cast one group with the options: returns the scale (f32) actually used. */
+static float cast_group_opts(const float *v, int n, int flags, uint8_t *q)
+{
+    float amax = 0.0f;
+    float clamped, sf, sf_inv;
+    int i;
+    for (i = 0; i < n; ++i) {
+        float a = fabsf(v[i]);
+        if (a > amax)
+            amax = a;
+    }
+    clamped = (amax < 1e-4f) ? 1e-4f : amax;
+    sf = clamped / 448.0f;
+    if (flags & (ORACLE_SF_POW2 | ORACLE_SF_UE8M0))
+        sf = pow2_at_least(sf);
+    sf_inv = 1.0f / sf;
+    for (i = 0; i < n; ++i) {
+        float scaled = v[i] * sf_inv;
+        q[i] = oracle_e4m3_encode(scaled);
+    }
+    return sf;
+}
+
+/* Write scale `sf` of (row r, group g) in the layout the flags name. */
+static void store_scale(void *out_sf, int flags, int64_t ld, int32_t G, int64_t r, int32_t g,
+                        float sf)
+{
+    if (flags & ORACLE_SF_UE8M0) {
+        int ex;
+        uint8_t byte;
+        frexp((double)sf, &ex);  /* sf = 0.5 * 2^ex exactly: log2(sf) = ex - 1 */
+        byte = (uint8_t)(ex - 1 + 127);
+        if (flags & ORACLE_SF_COLMAJOR)
+            ((uint8_t *)out_sf)[((int64_t)(g / 4) * ld + r) * 4 + (g % 4)] = byte;
+        else
+            ((uint8_t *)out_sf)[r * G + g] = byte;
+    } else {
+        if (flags & ORACLE_SF_COLMAJOR)
+            ((float *)out_sf)[(int64_t)g * ld + r] = sf;
+        else
+            ((float *)out_sf)[r * G + g] = sf;
+    }
+}
+
+/* Expand + cast with scale options, optionally zero-filling (codes and
+ * scales: 0.0f, or byte 0 for UE8M0) the rows with sorted_src[r] < 0
+ * (sorted_src may be NULL).  Rows no pos names and no zero-fill covers are
+ * left untouched. */
+int oracle_expand_cast_fp8_ex(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                              const int32_t *pos, const int32_t *sorted_src, int64_t num_rows,
+                              int32_t group, int32_t flags, int64_t ld, uint8_t *out,
+                              void *out_sf)
+{
+    int64_t t, r;
+    int32_t j, g, i, G;
+    float *buf, *sfs;
+    uint8_t *qrow;
+
+    if (T < 0 || k < 1 || group < 1 || H < group || H % group != 0 || num_rows < 0)
+        return 1;
+    if ((flags & ORACLE_SF_COLMAJOR) && ld < num_rows)
+        return 1;
+    G = H / group;
+    if (sorted_src) {
+        for (r = 0; r < num_rows; ++r) {
+            if (sorted_src[r] >= 0)
+                continue;
+            memset(out + r * H, 0, (size_t)H);
+            for (g = 0; g < G; ++g) {
+                if (flags & ORACLE_SF_UE8M0) {
+                    if (flags & ORACLE_SF_COLMAJOR)
+                        ((uint8_t *)out_sf)[((int64_t)(g / 4) * ld + r) * 4 + (g % 4)] = 0;
+                    else
+                        ((uint8_t *)out_sf)[r * G + g] = 0;
+                } else {
+                    store_scale(out_sf, flags, ld, G, r, g, 0.0f);
+                }
+            }
+        }
+    }
+    buf = (float *)malloc(sizeof(float) * (size_t)group);
+    sfs = (float *)malloc(sizeof(float) * (size_t)G);
+    qrow = (uint8_t *)malloc((size_t)H);
+    if (!buf || !sfs || !qrow) {
+        free(buf); free(sfs); free(qrow);
+        return 1;
+    }
+    for (t = 0; t < T; ++t) {
+        for (g = 0; g < G; ++g) {
+            for (i = 0; i < group; ++i)
+                buf[i] = bf16_bits_to_float(x[t * H + (int64_t)g * group + i]);
+            sfs[g] = cast_group_opts(buf, group, flags, qrow + (int64_t)g * group);
+        }
+        for (j = 0; j < k; ++j) {
+            int32_t rr = pos[t * k + j];
+            if (rr < 0)
+                continue;
+            if (rr >= num_rows) {
+                free(buf); free(sfs); free(qrow);
+                return 2;
+            }
+            memcpy(out + (int64_t)rr * H, qrow, (size_t)H);
+            for (g = 0; g < G; ++g)
+                store_scale(out_sf, flags, ld, G, rr, g, sfs[g]);
+        }
+    }
+    free(buf); free(sfs); free(qrow);
+    return 0;
+}
+
 /* per_token_cast: x [T, H] bf16 bits -> q [T, H] E4M3 bytes and
  * sf [T, H/group] fp32, row-major. */
 int oracle_per_token_cast(const uint16_t *x, int64_t T, int32_t H,
@@ -512,6 +648,69 @@ int oracle_swiglu_cast_fp8(const uint16_t *x, int64_t M, int32_t N,
                                        q + r * N + (int64_t)g * group);
     }
     free(v);
+    return 0;
+}
+
+/* SwiGLU variants (TileKernels page, section 3.3): optional clamp (the gate
+ * clamped from above, val_l = min(val_l, c); the up value clamped to [-c, c])
+ * and optional per-row top-k weight (v = g / (1 + exp(-g)) * u * w[r]), then
+ * the per-group cast with the scale options above.  clamp_count (nullable)
+ * receives the number of inputs the clamp changed (gate values > c plus up
+ * values with |u| > c), added to its current value.  has_clamp = 0: no clamp. */
+int oracle_swiglu_cast_fp8_ex(const uint16_t *x, int64_t M, int32_t N, int32_t group,
+                              int32_t has_clamp, float clamp, const float *weights,
+                              int32_t flags, int64_t ld, uint8_t *q, void *out_sf,
+                              uint64_t *clamp_count)
+{
+    int64_t r;
+    int32_t c, g, G;
+    float *v;
+    uint64_t count = 0;
+
+    if (M < 0 || group < 1 || N < group || N % group != 0)
+        return 1;
+    if ((flags & ORACLE_SF_COLMAJOR) && ld < M)
+        return 1;
+    G = N / group;
+    v = (float *)malloc(sizeof(float) * (size_t)N);
+    if (!v)
+        return 1;
+    for (r = 0; r < M; ++r) {
+        const uint16_t *row = x + r * 2 * (int64_t)N;
+        for (c = 0; c < N; ++c) {
+            float gt = bf16_bits_to_float(row[c]);
+            float u = bf16_bits_to_float(row[N + c]);
+            float e, den, silu, val;
+            if (has_clamp) {
+                if (gt > clamp) {
+                    gt = clamp;
+                    count += 1;
+                }
+                if (u > clamp) {
+                    u = clamp;
+                    count += 1;
+                } else if (u < -clamp) {
+                    u = -clamp;
+                    count += 1;
+                }
+            }
+            e = expf(-gt);
+            den = 1.0f + e;
+            silu = gt / den;
+            val = silu * u;
+            if (weights)
+                val = val * weights[r];
+            v[c] = val;
+        }
+        for (g = 0; g < G; ++g) {
+            float sf = cast_group_opts(v + (int64_t)g * group, group, flags,
+                                       q + r * N + (int64_t)g * group);
+            store_scale(out_sf, flags, ld, G, r, g, sf);
+        }
+    }
+    free(v);
+    if (clamp_count)
+        *clamp_count += count;
     return 0;
 }
 
