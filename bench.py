@@ -574,6 +574,8 @@ def extra_workloads(L, dev, stream, sp, chk, args):
     del hx, q2, sf2
     torch.cuda.empty_cache()
     res["prefill_64k_padded"] = padded_workload(L, dev, stream, sp, chk, flush, iters, peak)
+    torch.cuda.empty_cache()
+    res.update(cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak))
     del flush
     torch.cuda.empty_cache()
     return res
@@ -634,6 +636,93 @@ def padded_workload(L, dev, stream, sp, chk, flush, iters, peak, align=128):
             "ms": round(ms, 4), "routed_tokens_per_s": round(R / (ms * 1e-3), 1),
             "algorithmic_bytes": b, "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
             "timing": "one batch after a 512 MB L2 flush, median"}
+
+
+def cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak):
+    """The cast variants on the large-prefill and SwiGLU workloads: scales as
+    packed UE8M0 exponents in the TMA-aligned column-major layout (flags
+    COLMAJOR | POW2 | UE8M0); the SwiGLU with clamp 7.0, per-row weights and
+    the clamp counter as well.  One batch after an L2 flush, median."""
+    import torch
+
+    from moe_routing_precision_gb300 import ops, workloads
+    flags = ops.SF_COLMAJOR | ops.SF_POW2 | ops.SF_UE8M0
+
+    def timed(fn, n):
+        ts = []
+        for i in range(n + 2):
+            flush.fill_(i & 0xFF)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 2:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    res = {}
+    w = workloads.WORKLOADS[WORKLOAD]
+    inp = workloads.make_inputs(w, seed=0, device=dev)
+    s, x = inp["scores"], inp["x"]
+    T, E, k, H, R, G = w.T, w.E, w.k, w.H, w.R, w.G
+    ld = (R + 3) // 4 * 4
+    i32 = dict(dtype=torch.int32, device=dev)
+    idx, wt = torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device=dev)
+    counts, offsets, pos, src = (torch.empty(E, **i32), torch.empty(E + 1, **i32),
+                                 torch.empty(T, k, **i32), torch.empty(R, **i32))
+    ws = torch.empty(max(1, ops.route_map_workspace_bytes(T, E, k)), dtype=torch.uint8, device=dev)
+    q = torch.empty(R, H, dtype=torch.uint8, device=dev)
+    sfb = torch.empty((G + 3) // 4, ld, 4, dtype=torch.uint8, device=dev)
+    ws2 = torch.empty(ops.expand_cast_fp8_ex_workspace_bytes(T, H, flags), dtype=torch.uint8,
+                      device=dev)
+
+    def rec():
+        chk(L.moe_topk_gate(s.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
+        chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
+                            pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
+        chk(L.moe_expand_cast_fp8_ex(x.data_ptr(), T, H, k, pos.data_ptr(), src.data_ptr(), R,
+                                     q.data_ptr(), sfb.data_ptr(), flags, ld, ws2.data_ptr(),
+                                     ws2.numel(), 128, sp), "expand_ex")
+
+    ms = timed(rec, max(3, iters // 2))
+    B = algorithmic_bytes(T, E, k, H)
+    b = B["route_expand_cast"] - R * G * 4 + R * G      # one scale byte per group
+    gbs = b / (ms * 1e-3) / 1e9
+    res["prefill_64k_ue8m0_colmajor"] = {
+        "op": "topk + route_map + expand_cast_fp8_ex (packed UE8M0, column-major)",
+        "ms": round(ms, 4), "routed_tokens_per_s": round(R / (ms * 1e-3), 1),
+        "algorithmic_bytes": b, "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+        "timing": "one batch after a 512 MB L2 flush, median"}
+    del inp, s, x, q, sfb
+    torch.cuda.empty_cache()
+
+    w = workloads.WORKLOADS["swiglu_64k"]
+    hx = workloads.make_inputs(w, seed=0, device=dev)["swiglu_x"]
+    M, N = w.M, w.N
+    G2, ld2 = N // 128, (M + 3) // 4 * 4
+    q2 = torch.empty(M, N, dtype=torch.uint8, device=dev)
+    sf2 = torch.empty((G2 + 3) // 4, ld2, 4, dtype=torch.uint8, device=dev)
+    wr = torch.rand(M, generator=torch.Generator(device=dev).manual_seed(1), device=dev)
+    cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def sw():
+        chk(L.swiglu_cast_fp8_ex(hx.data_ptr(), M, N, q2.data_ptr(), sf2.data_ptr(), flags, ld2,
+                                 1, 7.0, wr.data_ptr(), cnt.data_ptr(), 128, sp), "swiglu_ex")
+
+    ms = timed(sw, iters)
+    b = M * 2 * N * 2 + M * 4 + M * N + M * G2
+    gbs = b / (ms * 1e-3) / 1e9
+    res["swiglu_64k_clamp_weight_ue8m0"] = {
+        "op": "swiglu_cast_fp8_ex (clamp 7, per-row weight, clamp count, packed UE8M0 col-major)",
+        "ms": round(ms, 4), "rows_per_s": round(M / (ms * 1e-3), 1), "algorithmic_bytes": b,
+        "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+        "clamped_inputs_per_pass": int(cnt.item()) // (iters + 2),
+        "timing": "after a 512 MB L2 flush, median"}
+    if L.moe_get_device_status(sp, None) != 0:
+        raise RuntimeError("device error in the cast-option workloads")
+    return res
 
 
 def cpu_baseline_leg(scores, x, k, E, tokens=16384, total=65536):

@@ -80,6 +80,15 @@ typedef enum moe_out_dtype {
     MOE_OUT_F32 = 1
 } moe_out_dtype_t;
 
+/* Scale options of the *_ex cast calls (bit flags). */
+#define MOE_SF_COLMAJOR 0x1u /* scales transposed: [G][sf_ld] (TMA-aligned column-major) */
+#define MOE_SF_POW2 0x2u     /* round_sf: smallest power of two >= the plain scale      */
+#define MOE_SF_UE8M0 0x4u    /* store the power-of-two scale as its biased exponent
+                                byte; requires MOE_SF_POW2.  Row-major: [rows][G] u8;
+                                with MOE_SF_COLMAJOR: [ceil(G/4)][sf_ld] u32, four
+                                consecutive groups of a row per word (group 4i+j in
+                                byte j)                                                 */
+
 /* Bits of the device error word (moe_get_device_status). */
 #define MOE_DEVERR_EXPERT_RANGE 0x1u /* route_map: topk_idx outside [0, E)      */
 #define MOE_DEVERR_POS_RANGE 0x2u    /* expand/combine: pos >= num_rows         */
@@ -241,6 +250,52 @@ moe_status_t moe_expand_cast_fp8_padded(const void *x, int64_t num_tokens,
                                         int32_t group, void *stream);
 
 /*
+ * moe_expand_cast_fp8_ex -- moe_expand_cast_fp8 with the scale options of
+ * [TK] 3.1 (round_sf, packed UE8M0) and [TK] 2.2 (TMA-aligned column-major
+ * scales), and optionally the zero-fill of moe_expand_cast_fp8_padded.
+ *   sf_flags: 0 or a combination of MOE_SF_COLMAJOR, MOE_SF_POW2,
+ *             MOE_SF_UE8M0 (which requires MOE_SF_POW2):
+ *     0                      out_sf [num_rows][G] f32 (moe_expand_cast_fp8's)
+ *     COLMAJOR               out_sf [G][sf_ld] f32
+ *     POW2 (| COLMAJOR)      as above, scale = smallest power of two >=
+ *                            max(amax, 1e-4)/448 (codes use its exact inverse)
+ *     UE8M0|POW2             out_sf [num_rows][G] u8: biased exponent (value
+ *                            2^(byte-127)) of the power-of-two scale
+ *     UE8M0|POW2|COLMAJOR    out_sf [ceil(G/4)][sf_ld] u32, group 4i+j of row r
+ *                            in byte j of word [i][r]
+ *   sf_ld: column-major leading dimension, >= num_rows and a multiple of 4
+ *          (16-byte aligned columns for TMA); ignored without COLMAJOR.
+ *   sorted_src: NULL, or [num_rows] i32 to zero-fill the rows with a negative
+ *          entry (codes 0, scales 0.0 or byte 0) in the same launch.
+ *   workspace, workspace_bytes: NULL / 0, or device memory (16-byte aligned)
+ *          of at least moe_expand_cast_fp8_ex_workspace_bytes(num_tokens,
+ *          hidden, sf_flags) bytes.  With a column-major layout, sorted_src
+ *          and a workspace, each token's scales are staged there once and a
+ *          second kernel writes the column-major buffer row by row from
+ *          sorted_src, in whole 128-byte lines; sorted_src must then be pos's
+ *          inverse (as moe_route_map / moe_route_map_aligned return it), and
+ *          a sorted_src entry >= num_tokens * num_topk sets
+ *          MOE_DEVERR_POS_RANGE and gives that row zero scales.  Otherwise each copy's scales are
+ *          stored directly (the same values; every store then writes part of
+ *          an L2 sector, which at large num_rows is much slower).  Unused for
+ *          row-major layouts.
+ * Requirements and error bits as moe_expand_cast_fp8; out_sf 4-byte aligned
+ * (1-byte for row-major UE8M0).
+ */
+moe_status_t moe_expand_cast_fp8_ex(const void *x, int64_t num_tokens, int32_t hidden,
+                                    int32_t num_topk, const int32_t *pos,
+                                    const int32_t *sorted_src, int64_t num_rows,
+                                    uint8_t *out, void *out_sf, uint32_t sf_flags,
+                                    int64_t sf_ld, void *workspace, size_t workspace_bytes,
+                                    int32_t group, void *stream);
+
+/* Workspace bytes moe_expand_cast_fp8_ex stages column-major scales in:
+ * num_tokens * G * 4 (f32) or num_tokens * ceil(G/4) * 4 (packed UE8M0),
+ * G = hidden / 128, rounded up to 256; 0 for row-major layouts. */
+size_t moe_expand_cast_fp8_ex_workspace_bytes(int64_t num_tokens, int32_t hidden,
+                                              uint32_t sf_flags);
+
+/*
  * swiglu_cast_fp8 -- [TK] 3.3, plain form (no clamp, no top-k weight).  For
  * each row r and channel c < N, in f32:
  *   g = x[r, c] (left half, the gate), u = x[r, N + c] (right half, up)
@@ -257,6 +312,23 @@ moe_status_t moe_expand_cast_fp8_padded(const void *x, int64_t num_tokens,
 moe_status_t swiglu_cast_fp8(const void *x, int64_t num_rows, int32_t n,
                              uint8_t *out, float *out_sf, int32_t group,
                              void *stream);
+
+/*
+ * swiglu_cast_fp8_ex -- swiglu_cast_fp8 with the variants of [TK] 3.3 and the
+ * scale options of moe_expand_cast_fp8_ex:
+ *   has_clamp, clamp: if has_clamp, g = min(g, clamp) and u = min(max(u,
+ *              -clamp), clamp) before the activation (clamp >= 0, finite);
+ *   weights:   NULL, or [M] f32: v = g / (1 + exp(-g)) * u * weights[r] (the
+ *              routed copy's top-k weight, in expert-sorted row order);
+ *   clamp_count: NULL, or one u64 in device memory to which the number of
+ *              inputs the clamp changed is ADDED (zero it to count one call);
+ *   sf_flags, sf_ld: as moe_expand_cast_fp8_ex, over M rows.
+ * Requirements as swiglu_cast_fp8.
+ */
+moe_status_t swiglu_cast_fp8_ex(const void *x, int64_t num_rows, int32_t n, uint8_t *out,
+                                void *out_sf, uint32_t sf_flags, int64_t sf_ld,
+                                int32_t has_clamp, float clamp, const float *weights,
+                                uint64_t *clamp_count, int32_t group, void *stream);
 
 /*
  * moe_combine -- [PX] combine: "accumulate in registers using the token

@@ -220,6 +220,96 @@ moe_status_t moe_expand_cast_fp8(const void* x, int64_t num_tokens, int32_t hidd
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
+}  // extern "C"
+
+namespace moe {
+namespace {
+// Valid scale-option sets: UE8M0 needs POW2; column-major needs a leading
+// dimension >= rows that keeps columns 16-byte aligned.
+bool sf_opts_ok(uint32_t flags, int64_t ld, int64_t rows, const void* out_sf) {
+  const uint32_t all = MOE_SF_COLMAJOR | MOE_SF_POW2 | MOE_SF_UE8M0;
+  if (flags & ~all) return false;
+  if ((flags & MOE_SF_UE8M0) && !(flags & MOE_SF_POW2)) return false;
+  if (flags & MOE_SF_COLMAJOR) {
+    if (ld < rows || ld % 4 != 0 || ld >= ((int64_t)1 << 31)) return false;
+  }
+  const bool bytes = (flags & MOE_SF_UE8M0) && !(flags & MOE_SF_COLMAJOR);
+  return bytes || aligned(out_sf, 4);
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+size_t moe_expand_cast_fp8_ex_workspace_bytes(int64_t num_tokens, int32_t hidden,
+                                              uint32_t sf_flags) {
+  if (num_tokens <= 0 || hidden < MOE_CAST_GROUP || !(sf_flags & MOE_SF_COLMAJOR)) return 0;
+  const int64_t G = hidden / MOE_CAST_GROUP;
+  const int64_t row = (sf_flags & MOE_SF_UE8M0) ? (G + 3) / 4 * 4 : G * 4;
+  return (size_t)((num_tokens * row + 255) / 256 * 256);
+}
+
+moe_status_t moe_expand_cast_fp8_ex(const void* x, int64_t num_tokens, int32_t hidden,
+                                    int32_t num_topk, const int32_t* pos,
+                                    const int32_t* sorted_src, int64_t num_rows, uint8_t* out,
+                                    void* out_sf, uint32_t sf_flags, int64_t sf_ld,
+                                    void* workspace, size_t workspace_bytes, int32_t group,
+                                    void* stream) {
+  if (group != MOE_CAST_GROUP) return MOE_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || num_rows < 0 || hidden < MOE_CAST_GROUP || hidden % MOE_CAST_GROUP != 0 ||
+      num_topk < 1 || num_topk > MOE_MAX_TOPK)
+    return MOE_ERR_INVALID_ARG;
+  if (num_rows >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
+  if (num_tokens * (hidden / MOE_CAST_GROUP) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!sf_opts_ok(sf_flags, sf_ld, num_rows, out_sf)) return MOE_ERR_INVALID_ARG;
+  if (num_tokens == 0 && (num_rows == 0 || sorted_src == nullptr)) return MOE_OK;
+  if ((num_tokens > 0 && (!x || !pos)) || (num_rows > 0 && (!out || !out_sf)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(pos, 4) || !aligned(sorted_src, 4) || !aligned(out, 16))
+    return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_expand_cast_fp8_ex_workspace_bytes(num_tokens, hidden, sf_flags);
+  if (workspace != nullptr && (!aligned(workspace, 16) || workspace_bytes < need))
+    return MOE_ERR_INVALID_ARG;
+  const bool stage = need > 0 && workspace != nullptr && sorted_src != nullptr;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  SfOut sfo;
+  sfo.flags = (int)sf_flags;
+  sfo.ld = sf_ld;
+  if (stage) sfo.stage = static_cast<uint8_t*>(workspace);
+  cudaError_t e = launch_expand_cast(c, x, num_tokens, hidden, num_topk, pos, num_rows, out,
+                                     static_cast<float*>(out_sf), sorted_src, sfo);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+moe_status_t swiglu_cast_fp8_ex(const void* x, int64_t num_rows, int32_t n, uint8_t* out,
+                                void* out_sf, uint32_t sf_flags, int64_t sf_ld, int32_t has_clamp,
+                                float clamp, const float* weights, uint64_t* clamp_count,
+                                int32_t group, void* stream) {
+  if (group != MOE_CAST_GROUP) return MOE_ERR_UNSUPPORTED;
+  if (num_rows < 0 || n < MOE_CAST_GROUP || n % MOE_CAST_GROUP != 0) return MOE_ERR_INVALID_ARG;
+  if (num_rows * (n / MOE_CAST_GROUP) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (has_clamp && !(clamp >= 0.0f && clamp <= 3.0e38f)) return MOE_ERR_INVALID_ARG;
+  if (!sf_opts_ok(sf_flags, sf_ld, num_rows, out_sf)) return MOE_ERR_INVALID_ARG;
+  if (num_rows == 0) return MOE_OK;
+  if (!x || !out || !out_sf) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(weights, 4) || !aligned(clamp_count, 8))
+    return MOE_ERR_INVALID_ARG;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  SwigluExt ext;
+  ext.has_clamp = has_clamp ? 1 : 0;
+  ext.clamp = clamp;
+  ext.weights = weights;
+  ext.clamp_count = reinterpret_cast<unsigned long long*>(clamp_count);
+  ext.sf.flags = (int)sf_flags;
+  ext.sf.ld = sf_ld;
+  cudaError_t e = launch_swiglu_cast_ex(c, x, num_rows, n, out, out_sf, ext);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
 moe_status_t swiglu_cast_fp8(const void* x, int64_t num_rows, int32_t n, uint8_t* out,
                              float* out_sf, int32_t group, void* stream) {
   if (group != MOE_CAST_GROUP) return MOE_ERR_UNSUPPORTED;

@@ -39,6 +39,15 @@ __device__ __forceinline__ uint4 ld_v4(const void* p) {
 }
 
 // 16-byte store of data nobody re-reads in this kernel (evict-first).
+// The same load with an L2 eviction policy (a createpolicy result).
+__device__ __forceinline__ uint4 ld_stream_v4_hint(const void* p, uint64_t policy) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p), "l"(policy));
+  return v;
+}
+
 __device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
                "r"(v.y), "r"(v.z), "r"(v.w)
@@ -65,6 +74,51 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
 // Scale of one group from its absolute maximum (f32, IEEE rounding).
 __device__ __forceinline__ float group_scale(float amax) {
   return __fdiv_rn(fmaxf(amax, kScaleFloor), kE4M3Max);
+}
+
+// Scale options (MOE_SF_* in moe_route.h; TileKernels article, 3.1 round_sf /
+// packed UE8M0 and 2.2 TMA-aligned column-major scales).  With POW2 (or
+// UE8M0) the scale is the smallest power of two >= the plain scale: a
+// positive normal f32 with a non-zero mantissa moves to the next exponent.
+__device__ __forceinline__ float group_scale_opts(float amax, int flags) {
+  float s = group_scale(amax);
+  if (flags & (MOE_SF_POW2 | MOE_SF_UE8M0)) {
+    uint32_t b = __float_as_uint(s);
+    if (b & 0x007FFFFFu) b = (b & 0xFF800000u) + 0x00800000u;
+    s = __uint_as_float(b);
+  }
+  return s;
+}
+
+// Store scale `sf` of (row r, group g) in the flagged layout; UE8M0 stores
+// the biased exponent byte of the (power-of-two) scale, packed four groups of
+// a row per 32-bit word when column-major.  `zero` stores 0.0 / byte 0.
+__device__ __forceinline__ void store_sf_opts(void* out_sf, int flags, int64_t ld, int G,
+                                              int64_t r, int g, float sf, bool zero = false) {
+  if (flags & MOE_SF_UE8M0) {
+    const uint8_t byte = zero ? 0 : (uint8_t)((__float_as_uint(sf) >> 23) & 0xFFu);
+    uint8_t* b = static_cast<uint8_t*>(out_sf);
+    if (flags & MOE_SF_COLMAJOR)
+      b[((int64_t)(g >> 2) * ld + r) * 4 + (g & 3)] = byte;
+    else
+      b[r * G + g] = byte;
+  } else {
+    float* f = static_cast<float*>(out_sf);
+    const float v = zero ? 0.0f : sf;
+    if (flags & MOE_SF_COLMAJOR)
+      f[(int64_t)g * ld + r] = v;
+    else
+      f[r * G + g] = v;
+  }
+}
+
+// Store token t's scale of group g into the row-major staging buffer.
+__device__ __forceinline__ void store_stage(uint8_t* stage, int flags, int G, int64_t t, int g,
+                                            float sf) {
+  if (flags & MOE_SF_UE8M0)
+    stage[t * (((G + 3) >> 2) << 2) + g] = (uint8_t)((__float_as_uint(sf) >> 23) & 0xFFu);
+  else
+    reinterpret_cast<float*>(stage)[t * G + g] = sf;
 }
 
 // Quantise 16 f32 values with multiplier `inv`, pack the 16 codes.
@@ -184,11 +238,33 @@ cudaError_t launch_route_map_aligned(const LaunchCtx& c, const int32_t* idx, int
                                      int k, int align, int64_t num_rows, int32_t* counts,
                                      int32_t* offsets, int32_t* pos, int32_t* sorted_src,
                                      int32_t* ws, int64_t num_chunks);
+// Scale output description for the cast kernels: flags 0 is the plain
+// row-major f32 layout.
+struct SfOut {
+  int flags = 0;
+  int64_t ld = 0;
+  // Column-major layouts only: when non-null, the expand kernels write each
+  // token's scales once, row-major, here ([T][G] f32, or [T][ceil(G/4)] packed
+  // UE8M0 words), and launch_sf_gather then writes the column-major buffer
+  // row by row from sorted_src with whole-line stores.
+  uint8_t* stage = nullptr;
+};
 cudaError_t launch_expand_cast(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                                const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
-                               const int32_t* zero_rows = nullptr);
+                               const int32_t* zero_rows = nullptr, SfOut sfo = SfOut());
 cudaError_t launch_swiglu_cast(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
                                float* out_sf);
+// SwiGLU variants: clamp (has_clamp), per-row weight (nullable), clamp count
+// (nullable, added to), scale options.
+struct SwigluExt {
+  int has_clamp = 0;
+  float clamp = 0.0f;
+  const float* weights = nullptr;
+  unsigned long long* clamp_count = nullptr;
+  SfOut sf;
+};
+cudaError_t launch_swiglu_cast_ex(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
+                                  void* out_sf, const SwigluExt& ext);
 cudaError_t launch_combine(const LaunchCtx& c, const void* y, const float* w, const int32_t* pos,
                            int64_t T, int H, int k, int64_t R, void* out, bool out_f32);
 cudaError_t launch_peak_copy(const LaunchCtx& c, const void* src, void* dst, size_t bytes);

@@ -62,7 +62,7 @@ __device__ __forceinline__ void load_tile(const uint16_t* __restrict__ x,
 __device__ __forceinline__ void zero_fill_rows(const int32_t* __restrict__ zsrc, int64_t num_rows,
                                                int H, int G, uint8_t* __restrict__ out,
                                                float* __restrict__ out_sf, int64_t gwarp,
-                                               int64_t nwarps, int lane) {
+                                               int64_t nwarps, int lane, SfOut sfo) {
   const uint4 zero = make_uint4(0, 0, 0, 0);
   for (int64_t r0 = gwarp * 32; r0 < num_rows; r0 += nwarps * 32) {
     const int64_t r = r0 + lane;
@@ -73,8 +73,15 @@ __device__ __forceinline__ void zero_fill_rows(const int32_t* __restrict__ zsrc,
       m &= m - 1;
       uint8_t* q = out + (r0 + i) * H;
       for (int c = lane * 16; c < H; c += 512) st_stream_v4(q + c, zero);
-      float* sfr = out_sf + (r0 + i) * G;
-      for (int g = lane; g < G; g += 32) st_stream_f32(sfr + g, 0.0f);
+      if (sfo.stage != nullptr) {
+        // staged column-major scales: the gather writes these rows' zeros
+      } else if (sfo.flags == 0) {
+        float* sfr = out_sf + (r0 + i) * G;
+        for (int g = lane; g < G; g += 32) st_stream_f32(sfr + g, 0.0f);
+      } else {
+        for (int g = lane; g < G; g += 32)
+          store_sf_opts(out_sf, sfo.flags, sfo.ld, G, r0 + i, g, 0.0f, true);
+      }
     }
   }
 }
@@ -86,7 +93,7 @@ template <bool G4>
 __global__ void __launch_bounds__(kThreads) expand_cast_kernel(
     const uint16_t* __restrict__ x, uint32_t units, int H, int k, const int32_t* __restrict__ pos,
     int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf, FastDiv fdG,
-    const int32_t* __restrict__ zsrc, unsigned* err) {
+    const int32_t* __restrict__ zsrc, SfOut sfo, unsigned* err) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
   const int sub = lane >> 3;  // unit within the warp's tile
@@ -108,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) expand_cast_kernel(
     // rows are written
     if (tile + warps < tiles) load_tile(x, pos, tile + warps, sub, l8, units, fdG, G, H, k, cur);
     const float amax = max8(absmax16_bf16(a, b));
-    const float sf = group_scale(amax);
+    const float sf = group_scale_opts(amax, sfo.flags);
     const float inv = __fdiv_rn(1.0f, sf);
     const uint4 q = quant16_bf16(a, b, inv);
     float4 sf4;
@@ -120,6 +127,7 @@ __global__ void __launch_bounds__(kThreads) expand_cast_kernel(
     }
     uint8_t* qdst = out + g * kGroup + l8 * 16;
     float* sdst = out_sf + g;
+    if (sfo.stage != nullptr && active && l8 == 0) store_stage(sfo.stage, sfo.flags, G, t, g, sf);
     for (int j0 = 0; j0 < k; j0 += 8) {
       if (j0 > 0)  // slots past the first 8 (k > 8)
         mine = (active && j0 + l8 < k) ? __ldg(pos + (int64_t)t * k + j0 + l8) : -1;
@@ -132,7 +140,9 @@ __global__ void __launch_bounds__(kThreads) expand_cast_kernel(
           continue;
         }
         st_stream_v4(qdst + (int64_t)r * H, q);
-        if (G4) {
+        if (sfo.flags != 0) {  // scale options: one lane per group stores its scale
+          if (l8 == 0 && sfo.stage == nullptr) store_sf_opts(out_sf, sfo.flags, sfo.ld, G, r, g, sf);
+        } else if (G4) {
           if (lane == 0) st_stream_v4(sdst + (int64_t)r * G, *reinterpret_cast<uint4*>(&sf4));
         } else if (l8 == 0) {
           st_stream_f32(sdst + (int64_t)r * G, sf);
@@ -145,7 +155,7 @@ __global__ void __launch_bounds__(kThreads) expand_cast_kernel(
   if (zsrc != nullptr)
     zero_fill_rows(zsrc, R, H, H >> 7, out, out_sf,
                    (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x,
-                   ((int64_t)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31);
+                   ((int64_t)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31, sfo);
   if (bad) flag_error(err, MOE_DEVERR_POS_RANGE);
 }
 
@@ -159,7 +169,7 @@ template <bool G4>
 __global__ void __launch_bounds__(1024) expand_cast_rows_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
     int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf, int tpc,
-    const int32_t* __restrict__ zsrc, unsigned* err) {
+    const int32_t* __restrict__ zsrc, SfOut sfo, unsigned* err) {
   pdl_enter();
   const int P = H >> 4;  // threads per token
   const int G = H >> 7;
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(1024) expand_cast_rows_kernel(
       pos0 = (l8 < k) ? __ldg(pos + tn * k + l8) : -1;
     }
     const float amax = max8(absmax16_bf16(ca, cb));
-    const float sf = group_scale(amax);
+    const float sf = group_scale_opts(amax, sfo.flags);
     const float inv = __fdiv_rn(1.0f, sf);
     const uint4 q = quant16_bf16(ca, cb, inv);
     float4 sf4;
@@ -209,6 +219,7 @@ __global__ void __launch_bounds__(1024) expand_cast_rows_kernel(
     }
     uint8_t* qdst = out + c * 16;
     float* sdst = out_sf + g;
+    if (sfo.stage != nullptr && active && l8 == 0) store_stage(sfo.stage, sfo.flags, G, t, g, sf);
     for (int j0 = 0; j0 < k; j0 += 8) {
       if (j0 > 0) mine = (active && j0 + l8 < k) ? __ldg(pos + t * k + j0 + l8) : -1;
 #pragma unroll
@@ -220,7 +231,9 @@ __global__ void __launch_bounds__(1024) expand_cast_rows_kernel(
           continue;
         }
         st_stream_v4(qdst + (int64_t)r * H, q);
-        if (G4) {
+        if (sfo.flags != 0) {  // scale options: one lane per group stores its scale
+          if (l8 == 0 && sfo.stage == nullptr) store_sf_opts(out_sf, sfo.flags, sfo.ld, G, r, g, sf);
+        } else if (G4) {
           if (lane == 0) st_stream_v4(sdst + (int64_t)r * G, *reinterpret_cast<uint4*>(&sf4));
         } else if (l8 == 0) {
           st_stream_f32(sdst + (int64_t)r * G, sf);
@@ -233,7 +246,7 @@ __global__ void __launch_bounds__(1024) expand_cast_rows_kernel(
   if (zsrc != nullptr)
     zero_fill_rows(zsrc, R, H, H >> 7, out, out_sf,
                    (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x,
-                   ((int64_t)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31);
+                   ((int64_t)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31, sfo);
   if (bad) flag_error(err, MOE_DEVERR_POS_RANGE);
 }
 
@@ -253,11 +266,30 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t byt
                : "memory");
 }
 
+// The same copy with an L2 eviction policy.  With column-major or byte scale
+// layouts, every scale store writes part of a 32-byte sector, and the sector
+// is completed by other tokens' stores later; the token rows read and the code
+// rows written are marked evict-first, so that the partly written scale lines
+// stay in L2 until complete instead of going to HBM (and coming back) in
+// pieces.
+__device__ __forceinline__ void bulk_s2g_hint(void* gdst, uint32_t ssrc, uint32_t bytes,
+                                              uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+               ::"l"(gdst), "r"(ssrc), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 template <int NBUF>
 __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
     int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf,
-    const int32_t* __restrict__ zsrc, unsigned* err) {
+    const int32_t* __restrict__ zsrc, SfOut sfo, unsigned* err) {
   extern __shared__ __align__(128) uint8_t s_buf[];
   pdl_enter();
   const int P = H >> 4;  // threads per token
@@ -270,6 +302,9 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
   const uint32_t stride = (uint32_t)((H + 4 * G + 127) / 128 * 128);  // bytes per buffer
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(s_buf);
   bool bad = false;
+  // only the column-major and byte scale layouts store partial lines
+  const bool hint = (sfo.flags & (MOE_SF_COLMAJOR | MOE_SF_UE8M0)) != 0 && sfo.stage == nullptr;
+  const uint64_t policy = l2_evict_first_policy();
   int64_t t = blockIdx.x;
   uint4 a = make_uint4(0, 0, 0, 0), b = a;
   int32_t pnext = -1;  // warp 0: lane j holds pos[t, j] (j < k <= 32)
@@ -289,13 +324,18 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
     if (tn < T) {  // the next token's loads stay in flight during this one
       if (act) {
         const uint16_t* src = x + tn * H + tid * 16;
-        a = ld_stream_v4(src);
-        b = ld_stream_v4(src + 8);
+        if (hint) {
+          a = ld_stream_v4_hint(src, policy);
+          b = ld_stream_v4_hint(src + 8, policy);
+        } else {
+          a = ld_stream_v4(src);
+          b = ld_stream_v4(src + 8);
+        }
       }
       if (tid < 32) pnext = (lane < k) ? __ldg(pos + tn * k + lane) : -1;
     }
     const float amax = max8(absmax16_bf16(ca, cb));
-    const float sf = group_scale(amax);
+    const float sf = group_scale_opts(amax, sfo.flags);
     const float inv = __fdiv_rn(1.0f, sf);
     const uint4 q = quant16_bf16(ca, cb, inv);
     const int buf = it % NBUF;
@@ -304,12 +344,24 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
       __syncthreads();
     }
     uint8_t* sq = s_buf + (size_t)buf * stride;
+    int32_t* spos = reinterpret_cast<int32_t*>(s_buf + (size_t)NBUF * stride) + buf * 32;
     if (act) {
       *reinterpret_cast<uint4*>(sq + tid * 16) = q;
-      if (l8 == 0) *reinterpret_cast<float*>(sq + H + 4 * g) = sf;
+      if (l8 == 0 && sfo.flags == 0) *reinterpret_cast<float*>(sq + H + 4 * g) = sf;
     }
+    if (sfo.flags != 0 && tid < 32) spos[tid] = pcur;  // destinations, for every warp
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the copies
     __syncthreads();
+    if (sfo.flags != 0 && act && l8 == 0) {  // scale options: per-group scale stores
+      if (sfo.stage != nullptr) {
+        store_stage(sfo.stage, sfo.flags, G, t, g, sf);
+      } else {
+        for (int j = 0; j < k; ++j) {
+          const int32_t r = spos[j];
+          if (r >= 0 && r < R) store_sf_opts(out_sf, sfo.flags, sfo.ld, G, r, g, sf);
+        }
+      }
+    }
     if (tid < 32) {
       for (int j = 0; j < k; ++j) {
         const int32_t r = __shfl_sync(0xFFFFFFFFu, pcur, j);
@@ -317,8 +369,12 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
           if (r >= R) {
             bad = true;
           } else {
-            bulk_s2g(out + (int64_t)r * H, sbase + buf * stride, (uint32_t)H);
-            bulk_s2g(out_sf + (int64_t)r * G, sbase + buf * stride + H, (uint32_t)(4 * G));
+            if (hint)
+              bulk_s2g_hint(out + (int64_t)r * H, sbase + buf * stride, (uint32_t)H, policy);
+            else
+              bulk_s2g(out + (int64_t)r * H, sbase + buf * stride, (uint32_t)H);
+            if (sfo.flags == 0)
+              bulk_s2g(out_sf + (int64_t)r * G, sbase + buf * stride + H, (uint32_t)(4 * G));
           }
         }
       }
@@ -332,7 +388,7 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
   if (zsrc != nullptr)
     zero_fill_rows(zsrc, R, H, H >> 7, out, out_sf,
                    (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x,
-                   ((int64_t)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31);
+                   ((int64_t)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31, sfo);
   if (bad) flag_error(err, MOE_DEVERR_POS_RANGE);
 }
 
@@ -345,12 +401,12 @@ constexpr int kBulkCtasPerSm = 3;
 template <int NBUF>
 cudaError_t launch_bulk(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                         const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
-                        int ctas_per_sm, const int32_t* zsrc) {
+                        int ctas_per_sm, const int32_t* zsrc, SfOut sfo) {
   const int P = H / 16;
   const int threads = (P + 31) / 32 * 32;
   const int G = H / kGroup;
   const size_t stride = (size_t)(H + 4 * G + 127) / 128 * 128;
-  const size_t smem = stride * NBUF;
+  const size_t smem = stride * NBUF + sizeof(int32_t) * 32 * NBUF;  // + per-buffer destinations
   if (smem > 48 * 1024) {
     cudaError_t st = cudaFuncSetAttribute(expand_cast_bulk_kernel<NBUF>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -359,7 +415,8 @@ cudaError_t launch_bulk(const LaunchCtx& c, const void* x, int64_t T, int H, int
   const int64_t cap = (int64_t)c.num_sms * ctas_per_sm;
   const int blocks = (int)(T < cap ? (T > 0 ? T : 1) : cap);  // >= 1: zero-fill with T = 0
   return launch_pdl(expand_cast_bulk_kernel<NBUF>, blocks, threads, smem, c.stream,
-                    static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, zsrc, c.err);
+                    static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, zsrc, sfo,
+                    c.err);
 }
 
 // CTAs per SM for the row form, measured on GB300 (prefill-sized expand).
@@ -368,7 +425,7 @@ constexpr int kRowCtasPerSm = 1;
 template <bool G4>
 cudaError_t launch_rows(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                         const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
-                        int ctas_per_sm, const int32_t* zsrc) {
+                        int ctas_per_sm, const int32_t* zsrc, SfOut sfo) {
   const int P = H / 16;
   const int tpc = P >= 256 ? 1 : 256 / P;
   const int64_t groups = (T + tpc - 1) / tpc;
@@ -376,14 +433,14 @@ cudaError_t launch_rows(const LaunchCtx& c, const void* x, int64_t T, int H, int
   const int blocks = (int)(groups < cap ? (groups > 0 ? groups : 1) : cap);  // >= 1: zero-fill
   const int threads = (P * tpc + 31) / 32 * 32;  // whole warps: the shuffles use full masks
   return launch_pdl(expand_cast_rows_kernel<G4>, blocks, threads, 0, c.stream,
-                    static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, tpc, zsrc,
+                    static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, tpc, zsrc, sfo,
                     c.err);
 }
 
 template <bool G4>
 cudaError_t launch_g(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                      const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
-                     const int32_t* zsrc) {
+                     const int32_t* zsrc, SfOut sfo) {
   const int G = H / kGroup;
   const uint32_t units = (uint32_t)(T * G);  // < 2^31, checked by the caller
   const uint32_t tiles = (units + 3) / 4;
@@ -396,25 +453,94 @@ cudaError_t launch_g(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
   const int blocks = (int)(need < cap ? (need > 0 ? need : 1) : cap);  // >= 1: zero-fill with T = 0
   return launch_pdl(expand_cast_kernel<G4>, blocks, kThreads, 0, c.stream,
                     static_cast<const uint16_t*>(x), units, H, k, pos, R, out, out_sf,
-                    FastDiv((uint32_t)G), zsrc, c.err);
+                    FastDiv((uint32_t)G), zsrc, sfo, c.err);
+}
+
+// Column-major scales from the staged per-token rows: thread r writes row r
+// of every column (f32 [G][ld], or packed UE8M0 words [ceil(G/4)][ld]) from
+// the staged row of token sorted_src[r] / k (sorted_src holds copy indices
+// t*k + j), or zeros where sorted_src[r] < 0 (padding rows, as the zero-fill
+// writes them).  Consecutive threads write consecutive
+// rows of a column, so each warp store is one whole 128-byte line; the staged
+// rows are read back from L2 (T * G * 4 bytes at most, just written).
+__global__ void __launch_bounds__(256) sf_gather_kernel(const uint8_t* __restrict__ stage,
+                                                        const int32_t* __restrict__ src, int64_t R,
+                                                        int64_t T, int k, int G, SfOut sfo,
+                                                        void* __restrict__ out_sf, unsigned* err) {
+  pdl_enter();
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= R) return;
+  const int32_t s = __ldg(src + r);
+  int64_t t = s < 0 ? -1 : s / k;
+  if (t >= T) {
+    flag_error(err, MOE_DEVERR_POS_RANGE);
+    t = -1;  // unknown copy: zeros, never a read outside the staged rows
+  }
+  const int64_t tr = t >= 0 ? t : 0;  // row read only when t >= 0
+  const int64_t ld = sfo.ld;
+  if (sfo.flags & MOE_SF_UE8M0) {
+    const int W = (G + 3) >> 2;
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(stage) + tr * W;
+    uint32_t* o = static_cast<uint32_t*>(out_sf) + r;
+    const int full = G >> 2;  // words with 4 groups; a last partial word keeps its unused bytes
+    for (int w = 0; w < full; ++w) o[w * ld] = t >= 0 ? row[w] : 0u;
+    if (full < W) {
+      const uint32_t v = t >= 0 ? row[full] : 0u;
+      uint8_t* ob = reinterpret_cast<uint8_t*>(o + full * ld);
+      for (int b = 0; b < (G & 3); ++b) ob[b] = (uint8_t)(v >> (8 * b));
+    }
+  } else {
+    const float* row = reinterpret_cast<const float*>(stage) + tr * G;
+    float* o = static_cast<float*>(out_sf) + r;
+    int g = 0;
+    if ((G & 3) == 0) {
+      for (; g < G; g += 4) {
+        const float4 v = t >= 0 ? *reinterpret_cast<const float4*>(row + g)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        o[(g + 0) * ld] = v.x;
+        o[(g + 1) * ld] = v.y;
+        o[(g + 2) * ld] = v.z;
+        o[(g + 3) * ld] = v.w;
+      }
+    }
+    for (; g < G; ++g) o[g * ld] = t >= 0 ? row[g] : 0.0f;
+  }
+}
+
+cudaError_t launch_sf_gather(const LaunchCtx& c, const int32_t* src, int64_t R, int64_t T, int k,
+                             int G, SfOut sfo, void* out_sf) {
+  if (R == 0) return cudaSuccess;
+  const int64_t blocks = (R + 255) / 256;
+  return launch_pdl(sf_gather_kernel, (int)blocks, 256, 0, c.stream,
+                    static_cast<const uint8_t*>(sfo.stage), src, R, T, k, G, sfo, out_sf, c.err);
+}
+
+cudaError_t launch_expand_cast_kernel(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
+                                      const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
+                                      const int32_t* zero_rows, SfOut sfo) {
+  // the 16-byte scale store needs G % 4 == 0 and a 16-byte aligned out_sf
+  const bool g4 = (H / kGroup) % 4 == 0 && (reinterpret_cast<uintptr_t>(out_sf) % 16) == 0;
+  const bool aligned16 = (reinterpret_cast<uintptr_t>(out) % 16) == 0;
+  const bool bulk_ok = sfo.flags != 0 || g4;  // scale options don't use the bulk scale copy
+  if (H <= 16384 && bulk_ok && (H / kGroup) % 4 == 0 && aligned16)
+    return launch_bulk<kBulkBuffers>(c, x, T, H, k, pos, R, out, out_sf, kBulkCtasPerSm,
+                                     zero_rows, sfo);
+  if (H <= 16384)
+    return g4 ? launch_rows<true>(c, x, T, H, k, pos, R, out, out_sf, kRowCtasPerSm, zero_rows, sfo)
+              : launch_rows<false>(c, x, T, H, k, pos, R, out, out_sf, kRowCtasPerSm, zero_rows,
+                                   sfo);
+  return g4 ? launch_g<true>(c, x, T, H, k, pos, R, out, out_sf, zero_rows, sfo)
+            : launch_g<false>(c, x, T, H, k, pos, R, out, out_sf, zero_rows, sfo);
 }
 
 }  // namespace
 
 cudaError_t launch_expand_cast(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                                const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
-                               const int32_t* zero_rows) {
-  // the 16-byte scale store needs G % 4 == 0 and a 16-byte aligned out_sf
-  const bool g4 = (H / kGroup) % 4 == 0 && (reinterpret_cast<uintptr_t>(out_sf) % 16) == 0;
-  const bool aligned16 = (reinterpret_cast<uintptr_t>(out) % 16) == 0;
-  if (H <= 16384 && g4 && aligned16)
-    return launch_bulk<kBulkBuffers>(c, x, T, H, k, pos, R, out, out_sf, kBulkCtasPerSm,
-                                     zero_rows);
-  if (H <= 16384)
-    return g4 ? launch_rows<true>(c, x, T, H, k, pos, R, out, out_sf, kRowCtasPerSm, zero_rows)
-              : launch_rows<false>(c, x, T, H, k, pos, R, out, out_sf, kRowCtasPerSm, zero_rows);
-  return g4 ? launch_g<true>(c, x, T, H, k, pos, R, out, out_sf, zero_rows)
-            : launch_g<false>(c, x, T, H, k, pos, R, out, out_sf, zero_rows);
+                               const int32_t* zero_rows, SfOut sfo) {
+  cudaError_t e = launch_expand_cast_kernel(c, x, T, H, k, pos, R, out, out_sf, zero_rows, sfo);
+  if (e != cudaSuccess || sfo.stage == nullptr) return e;
+  return launch_sf_gather(c, zero_rows, R, T, k, H / kGroup, sfo, out_sf);
 }
 
 }  // namespace moe

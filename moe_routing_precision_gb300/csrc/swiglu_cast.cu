@@ -28,11 +28,30 @@ __device__ __forceinline__ float swiglu(float g, float u) {
   return __fdividef(g, 1.0f + e) * u;
 }
 
-__global__ void __launch_bounds__(kThreads) swiglu_cast_kernel(const uint16_t* __restrict__ x,
-                                                               uint32_t units, int N,
-                                                               uint8_t* __restrict__ out,
-                                                               float* __restrict__ out_sf,
-                                                               FastDiv fdG) {
+// min / max that return NaN when either operand is NaN (PTX min.NaN / max.NaN).
+__device__ __forceinline__ float min_nan(float a, float b) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// EXT: the variants of the TileKernels article, section 3.3 (clamp: gate
+// min(g, c), up clamped to [-c, c]; per-row top-k weight multiplied after
+// silu(g) * u; clamp counting) and the scale options.  The plain instance
+// (EXT = false) compiles none of it.  The clamp count is kept per thread over
+// the whole grid-stride loop and added with one atomic per warp.  The register
+// caps keep 5 (EXT) or 6 CTAs of 256 threads resident per SM without spills:
+// each warp's loop is latency-bound, so resident warps set the bandwidth.
+template <bool EXT>
+__global__ void __launch_bounds__(kThreads, EXT ? 5 : 6)
+    swiglu_cast_kernel(const uint16_t* __restrict__ x, uint32_t units, int N,
+                       uint8_t* __restrict__ out, float* __restrict__ out_sf, FastDiv fdG,
+                       SwigluExt ext) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
   const int sub = lane >> 3;
@@ -40,6 +59,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_cast_kernel(const uint16_t* _
   const int G = N >> 7;
   const uint32_t tiles = (units + 3) >> 2;
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
+  unsigned clamped = 0;
   for (uint32_t tile = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; tile < tiles; tile += warps) {
     const uint32_t u = tile * 4 + sub;
     const bool active = u < units;
@@ -48,44 +68,92 @@ __global__ void __launch_bounds__(kThreads) swiglu_cast_kernel(const uint16_t* _
     const uint16_t* gate = x + (int64_t)r * 2 * N + g * kGroup + l8 * 16;
     const uint16_t* up = gate + N;
     uint4 ga = make_uint4(0, 0, 0, 0), gb = ga, ua = ga, ub = ga;
+    float wr = 0.0f;
     if (active) {
       ga = ld_stream_v4(gate);
       gb = ld_stream_v4(gate + 8);
       ua = ld_stream_v4(up);
       ub = ld_stream_v4(up + 8);
+      // issued with the row loads so that its latency overlaps theirs
+      if (EXT && ext.weights != nullptr) wr = __ldg(ext.weights + r);
     }
     float gv[16], uv[16], v[16];
     unpack16(ga, gb, gv);
     unpack16(ua, ub, uv);
+    if (EXT && ext.has_clamp) {
+      // Fast path: the clamp changes nothing unless some gate value or |up|
+      // value of the warp exceeds c (max over 16 values: two min/max per
+      // element, against seven for clamping and counting them all).
+      const float c = ext.clamp;
+      float mg = gv[0], mu = fabsf(uv[0]);
+#pragma unroll
+      for (int i = 1; i < 16; ++i) {
+        mg = fmaxf(mg, gv[i]);
+        mu = fmaxf(mu, fabsf(uv[i]));
+      }
+      if (__any_sync(0xFFFFFFFFu, active && (mg > c || mu > c))) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (active) clamped += (gv[i] > c) + (fabsf(uv[i]) > c);
+          gv[i] = min_nan(gv[i], c);  // NaN stays NaN, as min written as a compare
+          uv[i] = max_nan(min_nan(uv[i], c), -c);
+        }
+      }
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = swiglu(gv[i], uv[i]);
+    if (EXT && ext.weights != nullptr) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], wr);
+    }
     const float amax = max8(absmax16(v));
-    const float sf = group_scale(amax);
+    const float sf = EXT ? group_scale_opts(amax, ext.sf.flags) : group_scale(amax);
     const float inv = __fdiv_rn(1.0f, sf);
     const uint4 q = quant16(v, inv);
     if (active) {
       st_stream_v4(out + (int64_t)r * N + g * kGroup + l8 * 16, q);
-      if (l8 == 0) st_stream_f32(out_sf + (int64_t)r * G + g, sf);
+      if (l8 == 0) {
+        if (EXT && ext.sf.flags != 0)
+          store_sf_opts(out_sf, ext.sf.flags, ext.sf.ld, G, r, g, sf);
+        else
+          st_stream_f32(out_sf + (int64_t)r * G + g, sf);
+      }
     }
   }
+  if (EXT && ext.clamp_count != nullptr) {
+    const unsigned total = __reduce_add_sync(0xFFFFFFFFu, clamped);
+    if (lane == 0 && total) atomicAdd(ext.clamp_count, (unsigned long long)total);
+  }
+}
+
+template <bool EXT>
+cudaError_t launch_t(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
+                     float* out_sf, const SwigluExt& ext) {
+  const int G = N / kGroup;
+  const uint32_t units = (uint32_t)(M * G);  // < 2^31, checked by the caller
+  const uint32_t tiles = (units + 3) / 4;
+  const int64_t need = ((int64_t)tiles + (kThreads / 32) - 1) / (kThreads / 32);
+  int per_sm = 0;
+  cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, swiglu_cast_kernel<EXT>,
+                                                                 kThreads, 0);
+  if (st != cudaSuccess) return st;
+  const int64_t cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
+  const int blocks = (int)(need < cap ? need : cap);
+  return launch_pdl(swiglu_cast_kernel<EXT>, blocks, kThreads, 0, c.stream,
+                    static_cast<const uint16_t*>(x), units, N, out, out_sf, FastDiv((uint32_t)G),
+                    ext);
 }
 
 }  // namespace
 
 cudaError_t launch_swiglu_cast(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
                                float* out_sf) {
-  const int G = N / kGroup;
-  const uint32_t units = (uint32_t)(M * G);  // < 2^31, checked by the caller
-  const uint32_t tiles = (units + 3) / 4;
-  const int64_t need = ((int64_t)tiles + (kThreads / 32) - 1) / (kThreads / 32);
-  int per_sm = 0;
-  cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, swiglu_cast_kernel,
-                                                                 kThreads, 0);
-  if (st != cudaSuccess) return st;
-  const int64_t cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
-  const int blocks = (int)(need < cap ? need : cap);
-  return launch_pdl(swiglu_cast_kernel, blocks, kThreads, 0, c.stream,
-                    static_cast<const uint16_t*>(x), units, N, out, out_sf, FastDiv((uint32_t)G));
+  return launch_t<false>(c, x, M, N, out, out_sf, SwigluExt());
+}
+
+cudaError_t launch_swiglu_cast_ex(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
+                                  void* out_sf, const SwigluExt& ext) {
+  return launch_t<true>(c, x, M, N, out, static_cast<float*>(out_sf), ext);
 }
 
 }  // namespace moe

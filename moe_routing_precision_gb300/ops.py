@@ -23,6 +23,7 @@ MOE_OUT_BF16, MOE_OUT_F32 = 0, 1
 MOE_DEVERR_EXPERT_RANGE, MOE_DEVERR_POS_RANGE, MOE_DEVERR_DUPLICATE_EXPERT = 0x1, 0x2, 0x4
 MOE_DEVERR_ROWS_SHORT = 0x8
 GROUP = 128
+SF_COLMAJOR, SF_POW2, SF_UE8M0 = 0x1, 0x2, 0x4
 
 # Every symbol declared in include/moe_route.h, with its ctypes signature.
 _P = ctypes.c_void_p
@@ -38,6 +39,12 @@ SIGNATURES = {
     "moe_expand_cast_fp8_padded": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _P, _i64, _P, _P,
                                                   _i32, _P]),
     "swiglu_cast_fp8": (ctypes.c_int, [_P, _i64, _i32, _P, _P, _i32, _P]),
+    "moe_expand_cast_fp8_ex": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _P, _i64, _P, _P,
+                                              ctypes.c_uint32, _i64, _P, ctypes.c_size_t, _i32,
+                                              _P]),
+    "moe_expand_cast_fp8_ex_workspace_bytes": (ctypes.c_size_t, [_i64, _i32, ctypes.c_uint32]),
+    "swiglu_cast_fp8_ex": (ctypes.c_int, [_P, _i64, _i32, _P, _P, ctypes.c_uint32, _i64, _i32,
+                                          ctypes.c_float, _P, _P, _i32, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _i64, _i32, _i32, _i64, _P, _i32, _P]),
     "moe_peak_copy": (ctypes.c_int, [_P, _P, _sz, _P]),
     "moe_get_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -215,6 +222,82 @@ def expand_cast_fp8_padded(x: torch.Tensor, pos: torch.Tensor, sorted_src: torch
     return q, sf
 
 
+def sf_empty(rows: int, G: int, flags: int, ld: int | None, like: torch.Tensor):
+    """Scale buffer of the layout `flags` names: f32 [rows, G] or [G, ld];
+    uint8 [rows, G]; or packed words as uint8 [ceil(G/4), ld, 4]."""
+    ld = rows if ld is None else ld
+    if flags & SF_UE8M0:
+        if flags & SF_COLMAJOR:
+            return _empty(((G + 3) // 4, ld, 4), torch.uint8, like), ld
+        return _empty((rows, G), torch.uint8, like), ld
+    if flags & SF_COLMAJOR:
+        return _empty((G, ld), torch.float32, like), ld
+    return _empty((rows, G), torch.float32, like), ld
+
+
+def expand_cast_fp8_ex_workspace_bytes(T: int, H: int, sf_flags: int) -> int:
+    return int(lib().moe_expand_cast_fp8_ex_workspace_bytes(T, H, sf_flags))
+
+
+def expand_cast_fp8_ex(x: torch.Tensor, pos: torch.Tensor, num_rows: int | None = None, *,
+                       sorted_src=None, sf_flags: int = 0, sf_ld: int | None = None, out=None,
+                       out_sf=None, workspace=None, stream=None):
+    """expand_cast_fp8 with scale options (SF_COLMAJOR, SF_POW2, SF_UE8M0) and
+    an optional zero-fill of the rows whose sorted_src entry is negative.
+    workspace: None (direct scale stores), True (allocate one), or a uint8
+    CUDA tensor; used with a column-major layout and sorted_src to write the
+    scales in whole lines (sorted_src must be pos's inverse)."""
+    _dev(x, "x", torch.bfloat16)
+    _dev(pos, "pos", torch.int32)
+    T, H = x.shape
+    k = pos.shape[1]
+    if sorted_src is not None:
+        _dev(sorted_src, "sorted_src", torch.int32)
+    R = (T * k if sorted_src is None else sorted_src.shape[0]) if num_rows is None else int(num_rows)
+    if sf_ld is None and (sf_flags & SF_COLMAJOR):
+        sf_ld = (R + 3) // 4 * 4
+    q = out if out is not None else _empty((R, H), torch.uint8, x)
+    _dev(q, "out", torch.uint8, (R, H))
+    if out_sf is None:
+        out_sf, sf_ld = sf_empty(R, H // GROUP, sf_flags, sf_ld, x)
+    if out_sf.device.type != "cuda" or not out_sf.is_contiguous():
+        raise ValueError("out_sf must be a contiguous CUDA tensor")
+    if workspace is True:
+        n = expand_cast_fp8_ex_workspace_bytes(T, H, sf_flags)
+        workspace = _empty((n,), torch.uint8, x) if n > 0 else None
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    rc = lib().moe_expand_cast_fp8_ex(_ptr(x), T, H, k, _ptr(pos), _ptr(sorted_src), R, _ptr(q),
+                                      _ptr(out_sf), sf_flags, int(sf_ld or R), _ptr(workspace),
+                                      ws_bytes, GROUP, _stream(stream))
+    _check(rc, "moe_expand_cast_fp8_ex")
+    return q, out_sf
+
+
+def swiglu_cast_fp8_ex(x: torch.Tensor, *, clamp: float | None = None, weights=None,
+                       clamp_count=None, sf_flags: int = 0, sf_ld: int | None = None, out=None,
+                       out_sf=None, stream=None):
+    """SwiGLU with optional clamp, per-row weight and clamp counter (an int64
+    CUDA tensor of one element, added to), then the cast with scale options."""
+    _dev(x, "x", torch.bfloat16)
+    M, N2 = x.shape
+    N = N2 // 2
+    if weights is not None:
+        _dev(weights, "weights", torch.float32, (M,))
+    if clamp_count is not None:
+        _dev(clamp_count, "clamp_count", torch.int64, (1,))
+    if sf_ld is None and (sf_flags & SF_COLMAJOR):
+        sf_ld = (M + 3) // 4 * 4
+    q = out if out is not None else _empty((M, N), torch.uint8, x)
+    _dev(q, "out", torch.uint8, (M, N))
+    if out_sf is None:
+        out_sf, sf_ld = sf_empty(M, N // GROUP, sf_flags, sf_ld, x)
+    rc = lib().swiglu_cast_fp8_ex(_ptr(x), M, N, _ptr(q), _ptr(out_sf), sf_flags, int(sf_ld or M),
+                                  int(clamp is not None), float(clamp or 0.0), _ptr(weights),
+                                  _ptr(clamp_count), GROUP, _stream(stream))
+    _check(rc, "swiglu_cast_fp8_ex")
+    return q, out_sf
+
+
 def expand_cast_fp8(x: torch.Tensor, pos: torch.Tensor, num_rows: int | None = None, *,
                     out=None, out_sf=None, stream=None):
     """Per-token E4M3 cast (one fp32 scale per 128 channels) written to the
@@ -301,6 +384,7 @@ def launch_count() -> int:
 
 
 __all__ = ["lib", "MoeError", "topk_gate", "route_map", "route_map_workspace_bytes",
-           "route_map_aligned", "expand_cast_fp8_padded",
+           "route_map_aligned", "expand_cast_fp8_padded", "expand_cast_fp8_ex",
+           "expand_cast_fp8_ex_workspace_bytes", "swiglu_cast_fp8_ex", "sf_empty",
            "expand_cast_fp8", "swiglu_cast_fp8", "combine", "peak_copy", "device_status",
            "launch_count", "SIGNATURES"]

@@ -121,3 +121,50 @@ def check_combine_bf16(gpu_bits, ref_bits, ref_f32, mag):
         raise AssertionError(f"combine bf16: gpu {gpu_bits[i]:#06x} oracle {ref_bits[i]:#06x} "
                              f"(exact {ref_f32[i]!r}, tol {tol[i]:.3g}) at {i}")
     return int((~same).sum())
+
+
+SF_COLMAJOR, SF_POW2, SF_UE8M0 = 0x1, 0x2, 0x4
+
+
+def sf_rows(sf, flags: int, rows: int, G: int) -> np.ndarray:
+    """Scales of a flagged layout as f32 [rows, G] (UE8M0 bytes decoded to
+    2^(byte - 127))."""
+    sf = np.asarray(sf)
+    if flags & SF_UE8M0:
+        if flags & SF_COLMAJOR:
+            words, ld, _ = sf.shape
+            b = sf.transpose(1, 0, 2).reshape(ld, 4 * words)[:rows, :G]
+        else:
+            b = sf.reshape(rows, G)
+        return np.ldexp(1.0, b.astype(np.int64) - 127).astype(np.float32)
+    if flags & SF_COLMAJOR:
+        return np.ascontiguousarray(sf[:, :rows].T, np.float32)
+    return np.asarray(sf, np.float32).reshape(rows, G)
+
+
+def check_swiglu_opts(gpu_q, gpu_sf, ref_q, ref_sf, ref_sf_plain, flags: int, rows: int):
+    """SwiGLU with scale options.  Without POW2, check_swiglu on the decoded
+    scales.  With POW2 the scale is a step function of the group amax: where a
+    few-ulp difference in amax straddles a power of two the two sides pick
+    scales a factor 2 apart.  Such groups must be rare (<= 0.1%), exactly a
+    factor 2 apart, and the oracle's unrounded scale (ref_sf_plain, [rows, G])
+    must sit within 2^-20 of the smaller one; every other group obeys the
+    1-step / 0.1% code rule with identical scales."""
+    G = ref_sf_plain.shape[1]
+    gs = sf_rows(gpu_sf, flags, rows, G).astype(np.float64)
+    rs = sf_rows(ref_sf, flags, rows, G).astype(np.float64)
+    if not flags & SF_POW2:
+        return check_swiglu(gpu_q, gs.astype(np.float32), ref_q, rs)
+    diff = gs != rs
+    if diff.any():
+        assert diff.mean() <= SWIGLU_MISMATCH_FRAC, f"{diff.mean():.4%} of pow2 scales differ"
+        lo = np.minimum(gs, rs)[diff]
+        assert (np.maximum(gs, rs)[diff] == 2 * lo).all(), "pow2 scales differ by more than 2x"
+        plain = ref_sf_plain.astype(np.float64)[diff]
+        assert (np.abs(plain - lo) <= 2.0 ** -20 * plain).all(), "pow2 scale off a boundary"
+    keep = np.repeat(~diff, gpu_q.shape[1] // G, axis=1)
+    d = np.abs(fp8_ordinal(gpu_q) - fp8_ordinal(ref_q))[keep]
+    assert d.max(initial=0) <= 1, f"swiglu pow2: a code is {d.max()} steps off"
+    frac = float((d != 0).mean()) if d.size else 0.0
+    assert frac <= SWIGLU_MISMATCH_FRAC, f"swiglu pow2: {frac:.4%} of codes differ"
+    return frac

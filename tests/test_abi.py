@@ -157,3 +157,38 @@ def test_padded_entry_points_reject_bad_arguments(L):
     assert g(FAKE, 4, 256, 2, FAKE, None, 20, FAKE, FAKE, 128, None) == INVALID   # no sorted_src
     assert g(FAKE, 4, 256, 2, FAKE, FAKE + 2, 20, FAKE, FAKE, 128, None) == INVALID
     assert g(None, 0, 256, 2, None, None, 0, None, None, 128, None) == 0          # nothing to do
+
+
+def test_cast_option_entry_points_reject_bad_arguments(L):
+    f = L.moe_expand_cast_fp8_ex
+    args = lambda flags, ld, sf=FAKE, R=20, ws=None, wsb=0: (
+        FAKE, 4, 512, 2, FAKE, FAKE, R, FAKE, sf, flags, ld, ws, wsb, 128, None)
+    assert f(*args(4, 0)) == INVALID                     # UE8M0 without POW2
+    assert f(*args(8, 0)) == INVALID                     # unknown flag
+    assert f(*args(1, 18)) == INVALID                    # ld < rows
+    assert f(*args(1, 22)) == INVALID                    # ld not a multiple of 4
+    assert f(*args(3, 1 << 31)) == INVALID               # ld >= 2^31
+    assert f(*args(2, 0, sf=FAKE + 2)) == INVALID        # f32 scales 4-byte aligned
+    assert f(*args(7, 20, sf=FAKE + 2)) == INVALID       # packed words 4-byte aligned
+    need = L.moe_expand_cast_fp8_ex_workspace_bytes(4, 512, 7)
+    assert need == 256                                   # 4 tokens x 1 word, rounded to 256
+    assert L.moe_expand_cast_fp8_ex_workspace_bytes(4, 512, 3) == 256
+    assert L.moe_expand_cast_fp8_ex_workspace_bytes(1000, 7168, 1) == (1000 * 56 * 4 + 255) // 256 * 256
+    assert L.moe_expand_cast_fp8_ex_workspace_bytes(1000, 7168, 7) == (1000 * 56 + 255) // 256 * 256
+    assert L.moe_expand_cast_fp8_ex_workspace_bytes(1000, 7168, 6) == 0   # row-major: none
+    assert f(*args(7, 20, ws=FAKE, wsb=need - 1)) == INVALID        # workspace too small
+    assert f(*args(7, 20, ws=FAKE + 8, wsb=need)) == INVALID        # workspace 16-byte aligned
+    assert f(FAKE, 4, 512, 2, FAKE, None, 20, FAKE, FAKE, 0, 0, None, 0, 64, None) == UNSUPPORTED
+    assert f(None, 0, 512, 2, None, None, 0, None, None, 7, 0, None, 0, 128, None) == 0
+    g = L.swiglu_cast_fp8_ex
+    sargs = lambda flags=0, ld=0, has_clamp=0, clamp=0.0, w=None, cnt=None: (
+        FAKE, 4, 512, FAKE, FAKE, flags, ld, has_clamp, clamp, w, cnt, 128, None)
+    assert g(*sargs(flags=4)) == INVALID
+    assert g(*sargs(flags=1, ld=2)) == INVALID
+    assert g(*sargs(has_clamp=1, clamp=-1.0)) == INVALID
+    assert g(*sargs(has_clamp=1, clamp=float("nan"))) == INVALID
+    assert g(*sargs(has_clamp=1, clamp=float("inf"))) == INVALID
+    assert g(*sargs(w=FAKE + 2)) == INVALID              # weights 4-byte aligned
+    assert g(*sargs(cnt=FAKE + 4)) == INVALID            # counter 8-byte aligned
+    assert g(None, 0, 512, None, None, 7, 0, 1, 1.0, None, None, 128, None) == 0
+    assert L.moe_kernel_launch_count() == 0
