@@ -576,6 +576,8 @@ def extra_workloads(L, dev, stream, sp, chk, args):
     res["prefill_64k_padded"] = padded_workload(L, dev, stream, sp, chk, flush, iters, peak)
     torch.cuda.empty_cache()
     res.update(cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak))
+    torch.cuda.empty_cache()
+    res["decode_1k"] = decode_workload(L, dev, stream, sp, chk, flush, iters, peak)
     del flush
     torch.cuda.empty_cache()
     return res
@@ -722,6 +724,72 @@ def cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak):
         "timing": "after a 512 MB L2 flush, median"}
     if L.moe_get_device_status(sp, None) != 0:
         raise RuntimeError("device error in the cast-option workloads")
+    return res
+
+
+def decode_workload(L, dev, stream, sp, chk, flush, iters, peak):
+    """route + expand + cast of the T=1024 decode batch (E=256, k=8, H=4096)
+    through moe_route_expand_cast_fp8: the four separate launches (chained by
+    programmatic dependent launch), the same four captured in a CUDA graph, and
+    the fused single cooperative launch.  Each timed after a 512 MB L2 flush
+    that also keeps the GPU busy while the host enqueues (device time only)."""
+    import torch
+
+    from moe_routing_precision_gb300 import ops, workloads
+    w = workloads.WORKLOADS["decode_1k"]
+    inp = workloads.make_inputs(w, seed=0, device=dev)
+    s, x = inp["scores"], inp["x"]
+    T, E, k, H, R, G = w.T, w.E, w.k, w.H, w.R, w.G
+    i32 = dict(dtype=torch.int32, device=dev)
+    idx, wt = torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device=dev)
+    counts, offsets, pos, src = (torch.empty(E, **i32), torch.empty(E + 1, **i32),
+                                 torch.empty(T, k, **i32), torch.empty(R, **i32))
+    q = torch.empty(R, H, dtype=torch.uint8, device=dev)
+    sf = torch.empty(R, G, dtype=torch.float32, device=dev)
+    ws = ops.route_expand_cast_workspace(T, E, k, x)
+
+    def call(mode, st=sp):
+        chk(L.moe_route_expand_cast_fp8(s.data_ptr(), T, E, k, x.data_ptr(), H, idx.data_ptr(),
+                                        wt.data_ptr(), counts.data_ptr(), offsets.data_ptr(),
+                                        pos.data_ptr(), src.data_ptr(), q.data_ptr(),
+                                        sf.data_ptr(), ws.data_ptr(), ws.numel(), mode, 128, st),
+            "route_expand_cast")
+
+    def timed(fn):
+        ts = []
+        for i in range(iters + 3):
+            flush.fill_(i & 0xFF)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    res = {"op": "topk + route_map + expand_cast_fp8 (T=1024, E=256, k=8, H=4096)"}
+    B = algorithmic_bytes(T, E, k, H)["route_expand_cast"]
+    sep = timed(lambda: call(ops.PATH_SEPARATE))
+    fused = timed(lambda: call(ops.PATH_FUSED))
+    call(ops.PATH_SEPARATE)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream(device=dev)
+    with torch.cuda.graph(g, stream=cs):
+        call(ops.PATH_SEPARATE, cs.cuda_stream)
+    graph = timed(lambda: g.replay())
+    if L.moe_get_device_status(sp, None) != 0:
+        raise RuntimeError("device error in the decode workload")
+    for name, us in (("separate_launches", sep), ("separate_in_cuda_graph", graph),
+                     ("fused_single_launch", fused)):
+        gbs = B / (us * 1e-6) / 1e9
+        res[name] = {"us": round(us, 2), "routed_tokens_per_s": round(R / (us * 1e-6), 1),
+                     "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+    res["algorithmic_bytes"] = B
+    res["timing"] = "one call after a 512 MB L2 flush, median; device time"
+    del g
     return res
 
 

@@ -94,6 +94,12 @@ typedef enum moe_out_dtype {
 #define MOE_DEVERR_POS_RANGE 0x2u    /* expand/combine: pos >= num_rows         */
 #define MOE_DEVERR_DUPLICATE_EXPERT 0x4u /* route_map: a token names an expert twice */
 #define MOE_DEVERR_ROWS_SHORT 0x8u   /* route_map_aligned: num_rows < padded total */
+#define MOE_DEVERR_TIMEOUT 0x10u     /* fused decode path: a bounded wait ran out */
+
+/* Paths of moe_route_expand_cast_fp8. */
+#define MOE_PATH_AUTO 0     /* the library's choice: SEPARATE (measured fastest on GB300)  */
+#define MOE_PATH_FUSED 1    /* one cooperative launch (decode shapes only)               */
+#define MOE_PATH_SEPARATE 2 /* moe_topk_gate + moe_route_map + moe_expand_cast_fp8      */
 
 /*
  * moe_topk_gate -- [TK] 2.1 Top-K Gating, plus the "Weight Normalization" that
@@ -347,6 +353,58 @@ moe_status_t moe_combine(const void *y, const float *topk_weights,
                          const int32_t *pos, int64_t num_tokens, int32_t hidden,
                          int32_t num_topk, int64_t num_rows, void *out,
                          int32_t out_dtype, void *stream);
+
+/*
+ * moe_route_expand_cast_fp8 -- steps 1-3 of the path in one call: top-k gate +
+ * softmax weights, route map, expand + per-token E4M3 cast, with exactly the
+ * results of moe_topk_gate (MOE_WEIGHTS_SOFTMAX_TOPK), moe_route_map and
+ * moe_expand_cast_fp8 (num_rows = T*k).
+ *
+ * The FUSED path is the decode specialisation of "CuTeDSL at Perplexity"
+ * (prefill/decode kernels; MoE dispatch): one cooperative launch of one block
+ * per SM.  Every warp selects its tokens' experts and every block casts its
+ * tokens into shared memory; block 0 then builds the route map once all
+ * blocks have arrived on a counter, and signals the others, which write their
+ * rows.  Each wait is bounded (1 s); one that runs out sets
+ * MOE_DEVERR_TIMEOUT.  It applies to T <= 2048, 32 < E <= 256, k <= 32,
+ * T*k <= 16384, H <= 16384 (shared-memory staging permitting).  The SEPARATE path is the
+ * four launches of the individual calls.
+ *   scores [T,E] f32; x [T,H] bf16; topk_idx [T,k] i32; topk_weights [T,k]
+ *   f32; counts [E], offsets [E+1], pos [T,k], sorted_src [T*k] i32;
+ *   out [T*k,H] u8; out_sf [T*k,H/128] f32.
+ *   workspace: at least moe_route_expand_cast_fp8_workspace_bytes(T,E,k)
+ *   bytes, 16-byte aligned.  Its first 256 bytes hold the fused path's
+ *   control words: ZERO them once before the first call (each call leaves
+ *   them zero; after a MOE_DEVERR_TIMEOUT, zero them again).  One workspace
+ *   must not be used by two calls in flight at once.
+ *   mode: MOE_PATH_AUTO, MOE_PATH_FUSED (MOE_ERR_UNSUPPORTED where it does not
+ *   apply) or MOE_PATH_SEPARATE.  On GB300 the separate launches, chained by
+ *   programmatic dependent launch, were measured as fast as the fused launch
+ *   for T <= 64 and faster above (the single routing block and the
+ *   cooperative launch cost more than the launch gaps they remove), so AUTO
+ *   takes the separate path.
+ * Requirements as the individual calls; group == 128.
+ */
+moe_status_t moe_route_expand_cast_fp8(const float *scores, int64_t num_tokens,
+                                       int32_t num_experts, int32_t num_topk, const void *x,
+                                       int32_t hidden, int32_t *topk_idx, float *topk_weights,
+                                       int32_t *counts, int32_t *offsets, int32_t *pos,
+                                       int32_t *sorted_src, uint8_t *out, float *out_sf,
+                                       void *workspace, size_t workspace_bytes, int32_t mode,
+                                       int32_t group, void *stream);
+
+/* 256 + moe_route_map_workspace_bytes(T, E, k). */
+size_t moe_route_expand_cast_fp8_workspace_bytes(int64_t num_tokens, int32_t num_experts,
+                                                 int32_t num_topk);
+
+/* Test hooks of the fused path, process-wide, read at each launch:
+ *   MOE_DEBUG_WAIT_TIMEOUT_NS: the bound of every wait (default 1e9 ns);
+ *   MOE_DEBUG_SKIP_ROUTE_SIGNAL: nonzero = block 0 never signals "routed", so
+ *   the copy blocks' waits run out (the failure path, without a fault).
+ * Returns MOE_ERR_INVALID_ARG for an unknown key or a value out of range. */
+#define MOE_DEBUG_WAIT_TIMEOUT_NS 1
+#define MOE_DEBUG_SKIP_ROUTE_SIGNAL 2
+moe_status_t moe_debug_set(int32_t key, int64_t value);
 
 /*
  * moe_peak_copy -- a plain 16-byte vectorised device-to-device copy of

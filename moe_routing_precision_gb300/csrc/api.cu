@@ -81,7 +81,7 @@ const char* moe_status_string(moe_status_t s) {
     case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: bad pointer, size, alignment or range";
     case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: valid request not implemented";
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or launch failed";
-    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE: a kernel flagged out-of-range data";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE: a kernel flagged out-of-range data or a timeout";
   }
   return "unknown moe_status_t";
 }
@@ -343,6 +343,75 @@ moe_status_t moe_combine(const void* y, const float* topk_weights, const int32_t
   cudaError_t e = launch_combine(c, y, topk_weights, pos, num_tokens, hidden, num_topk, num_rows,
                                  out, out_dtype == MOE_OUT_F32);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
+size_t moe_route_expand_cast_fp8_workspace_bytes(int64_t num_tokens, int32_t num_experts,
+                                                 int32_t num_topk) {
+  return 256 + moe_route_map_workspace_bytes(num_tokens, num_experts, num_topk);
+}
+
+moe_status_t moe_route_expand_cast_fp8(const float* scores, int64_t num_tokens,
+                                       int32_t num_experts, int32_t num_topk, const void* x,
+                                       int32_t hidden, int32_t* topk_idx, float* topk_weights,
+                                       int32_t* counts, int32_t* offsets, int32_t* pos,
+                                       int32_t* sorted_src, uint8_t* out, float* out_sf,
+                                       void* workspace, size_t workspace_bytes, int32_t mode,
+                                       int32_t group, void* stream) {
+  if (group != MOE_CAST_GROUP) return MOE_ERR_UNSUPPORTED;
+  if (mode != MOE_PATH_AUTO && mode != MOE_PATH_FUSED && mode != MOE_PATH_SEPARATE)
+    return MOE_ERR_INVALID_ARG;
+  if (num_tokens < 0 || !experts_ok(num_experts, num_topk)) return MOE_ERR_INVALID_ARG;
+  if (hidden < MOE_CAST_GROUP || hidden % MOE_CAST_GROUP != 0) return MOE_ERR_INVALID_ARG;
+  if (num_tokens * (int64_t)num_topk >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
+  if (num_tokens * (hidden / MOE_CAST_GROUP) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !aligned(counts, 4) || !aligned(offsets, 4)) return MOE_ERR_INVALID_ARG;
+  if (num_tokens > 0) {
+    if (!scores || !x || !topk_idx || !topk_weights || !pos || !sorted_src || !out || !out_sf ||
+        !workspace)
+      return MOE_ERR_INVALID_ARG;
+    if (!aligned(scores, 4) || !aligned(x, 16) || !aligned(topk_idx, 4) ||
+        !aligned(topk_weights, 4) || !aligned(pos, 4) || !aligned(sorted_src, 4) ||
+        !aligned(out, 16) || !aligned(out_sf, 4) || !aligned(workspace, 16))
+      return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes <
+        moe_route_expand_cast_fp8_workspace_bytes(num_tokens, num_experts, num_topk))
+      return MOE_ERR_INVALID_ARG;
+  }
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  const bool fused_ok =
+      num_tokens > 0 &&
+      decode_fused_smem(num_tokens, num_experts, num_topk, hidden, c.num_sms, nullptr, nullptr) > 0;
+  if (mode == MOE_PATH_FUSED && !fused_ok && num_tokens > 0) return MOE_ERR_UNSUPPORTED;
+  if (mode == MOE_PATH_FUSED && fused_ok) {
+    cudaError_t e = launch_decode_fused(c, scores, num_tokens, num_experts, num_topk, x, hidden,
+                                        topk_idx, topk_weights, counts, offsets, pos, sorted_src,
+                                        out, out_sf, static_cast<unsigned*>(workspace));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+  }
+  moe_status_t r = moe_topk_gate(scores, num_tokens, num_experts, num_topk, topk_idx,
+                                 topk_weights, MOE_WEIGHTS_SOFTMAX_TOPK, stream);
+  if (r != MOE_OK) return r;
+  void* route_ws = num_tokens > 0 ? static_cast<uint8_t*>(workspace) + 256 : nullptr;
+  r = moe_route_map(topk_idx, num_tokens, num_experts, num_topk, counts, offsets, pos, sorted_src,
+                    route_ws, num_tokens > 0 ? workspace_bytes - 256 : 0, stream);
+  if (r != MOE_OK) return r;
+  return moe_expand_cast_fp8(x, num_tokens, hidden, num_topk, pos, num_tokens * num_topk, out,
+                             out_sf, group, stream);
+}
+
+moe_status_t moe_debug_set(int32_t key, int64_t value) {
+  if (key == MOE_DEBUG_WAIT_TIMEOUT_NS) {
+    if (value < 1000 || value > (int64_t)60 * 1000000000) return MOE_ERR_INVALID_ARG;
+    g_decode_timeout_ns.store(value);
+    return MOE_OK;
+  }
+  if (key == MOE_DEBUG_SKIP_ROUTE_SIGNAL) {
+    g_decode_skip_signal.store(value != 0 ? 1 : 0);
+    return MOE_OK;
+  }
+  return MOE_ERR_INVALID_ARG;
 }
 
 moe_status_t moe_peak_copy(const void* src, void* dst, size_t bytes, void* stream) {

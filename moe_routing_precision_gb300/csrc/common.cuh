@@ -6,6 +6,8 @@
 #include <cuda_fp8.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "moe_route.h"
 
 namespace moe {
@@ -228,6 +230,15 @@ struct LaunchCtx {
   int num_sms;
   unsigned* err;  // device error word
 };
+
+// Fused decode path (decode_fused.cu) and its test hooks.
+extern std::atomic<int64_t> g_decode_timeout_ns;
+extern std::atomic<int> g_decode_skip_signal;
+size_t decode_fused_smem(int64_t T, int E, int k, int H, int num_sms, int* blocks, int* tpb);
+cudaError_t launch_decode_fused(const LaunchCtx& c, const float* scores, int64_t T, int E, int k,
+                                const void* x, int H, int32_t* idx, float* w, int32_t* counts,
+                                int32_t* offsets, int32_t* pos, int32_t* src, uint8_t* out,
+                                float* out_sf, unsigned* ctl);
 
 cudaError_t launch_topk_gate(const LaunchCtx& c, const float* scores, int64_t T, int E, int k,
                              int32_t* idx, float* w);

@@ -43,6 +43,11 @@ SIGNATURES = {
                                               ctypes.c_uint32, _i64, _P, ctypes.c_size_t, _i32,
                                               _P]),
     "moe_expand_cast_fp8_ex_workspace_bytes": (ctypes.c_size_t, [_i64, _i32, ctypes.c_uint32]),
+    "moe_route_expand_cast_fp8": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _i32, _P, _P, _P, _P,
+                                                 _P, _P, _P, _P, _P, ctypes.c_size_t, _i32, _i32,
+                                                 _P]),
+    "moe_route_expand_cast_fp8_workspace_bytes": (ctypes.c_size_t, [_i64, _i32, _i32]),
+    "moe_debug_set": (ctypes.c_int, [_i32, _i64]),
     "swiglu_cast_fp8_ex": (ctypes.c_int, [_P, _i64, _i32, _P, _P, ctypes.c_uint32, _i64, _i32,
                                           ctypes.c_float, _P, _P, _i32, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _i64, _i32, _i32, _i64, _P, _i32, _P]),
@@ -235,6 +240,47 @@ def sf_empty(rows: int, G: int, flags: int, ld: int | None, like: torch.Tensor):
     return _empty((rows, G), torch.float32, like), ld
 
 
+PATH_AUTO, PATH_FUSED, PATH_SEPARATE = 0, 1, 2
+MOE_DEVERR_TIMEOUT = 0x10
+DEBUG_WAIT_TIMEOUT_NS, DEBUG_SKIP_ROUTE_SIGNAL = 1, 2
+
+
+def route_expand_cast_workspace(T: int, E: int, k: int, like: torch.Tensor) -> torch.Tensor:
+    """A zero-filled workspace for route_expand_cast_fp8 (its first 256 bytes
+    are the fused path's control words, which must start at zero)."""
+    n = int(lib().moe_route_expand_cast_fp8_workspace_bytes(T, E, k))
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=like.device)
+
+
+def route_expand_cast_fp8(scores: torch.Tensor, x: torch.Tensor, k: int, *, mode: int = PATH_AUTO,
+                          workspace=None, out=None, stream=None):
+    """topk_gate + route_map + expand_cast_fp8 in one call (the fused decode
+    path: one cooperative launch).  -> (topk_idx, topk_w, counts, offsets, pos,
+    sorted_src, q, sf)."""
+    _dev(scores, "scores", torch.float32)
+    _dev(x, "x", torch.bfloat16)
+    T, E = scores.shape
+    H = x.shape[1]
+    R = T * k
+    idx, w = _empty((T, k), torch.int32, x), _empty((T, k), torch.float32, x)
+    counts, offsets = _empty((E,), torch.int32, x), _empty((E + 1,), torch.int32, x)
+    pos, src = _empty((T, k), torch.int32, x), _empty((R,), torch.int32, x)
+    q, sf = (out if out is not None else
+             (_empty((R, H), torch.uint8, x), _empty((R, H // GROUP), torch.float32, x)))
+    if workspace is None:
+        workspace = route_expand_cast_workspace(T, E, k, x)
+    rc = lib().moe_route_expand_cast_fp8(_ptr(scores), T, E, k, _ptr(x), H, _ptr(idx), _ptr(w),
+                                         _ptr(counts), _ptr(offsets), _ptr(pos), _ptr(src),
+                                         _ptr(q), _ptr(sf), _ptr(workspace), workspace.numel(),
+                                         mode, GROUP, _stream(stream))
+    _check(rc, "moe_route_expand_cast_fp8")
+    return idx, w, counts, offsets, pos, src, q, sf
+
+
+def debug_set(key: int, value: int) -> None:
+    _check(lib().moe_debug_set(key, int(value)), "moe_debug_set")
+
+
 def expand_cast_fp8_ex_workspace_bytes(T: int, H: int, sf_flags: int) -> int:
     return int(lib().moe_expand_cast_fp8_ex_workspace_bytes(T, H, sf_flags))
 
@@ -386,5 +432,6 @@ def launch_count() -> int:
 __all__ = ["lib", "MoeError", "topk_gate", "route_map", "route_map_workspace_bytes",
            "route_map_aligned", "expand_cast_fp8_padded", "expand_cast_fp8_ex",
            "expand_cast_fp8_ex_workspace_bytes", "swiglu_cast_fp8_ex", "sf_empty",
+           "route_expand_cast_fp8", "route_expand_cast_workspace", "debug_set",
            "expand_cast_fp8", "swiglu_cast_fp8", "combine", "peak_copy", "device_status",
            "launch_count", "SIGNATURES"]

@@ -192,3 +192,27 @@ def test_cast_option_entry_points_reject_bad_arguments(L):
     assert g(*sargs(cnt=FAKE + 4)) == INVALID            # counter 8-byte aligned
     assert g(None, 0, 512, None, None, 7, 0, 1, 1.0, None, None, 128, None) == 0
     assert L.moe_kernel_launch_count() == 0
+
+
+def test_route_expand_cast_rejects_bad_arguments(L):
+    f = L.moe_route_expand_cast_fp8
+    T, E, k, H = 8, 256, 8, 512
+    need = L.moe_route_expand_cast_fp8_workspace_bytes(T, E, k)
+    assert need == 256 + L.moe_route_map_workspace_bytes(T, E, k)
+    def args(mode=0, H=H, x=FAKE, ws=FAKE, wsb=need, group=128):
+        return (FAKE, T, E, k, x, H, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, wsb,
+                mode, group, None)
+    assert f(*args(mode=3)) == INVALID
+    assert f(*args(mode=-1)) == INVALID
+    assert f(*args(group=64)) == UNSUPPORTED
+    assert f(*args(H=200)) == INVALID
+    assert f(*args(wsb=need - 1)) == INVALID
+    assert f(*args(ws=FAKE + 8)) == INVALID         # workspace 16-byte aligned
+    assert f(*args(x=FAKE + 4)) == INVALID          # x 16-byte aligned
+    assert f(*args(ws=None)) == INVALID
+    assert L.moe_debug_set(99, 0) == INVALID
+    assert L.moe_debug_set(1, 10) == INVALID        # timeout below 1 us
+    assert L.moe_debug_set(1, 61 * 10**9) == INVALID
+    assert L.moe_debug_set(1, 10**9) == 0
+    assert L.moe_debug_set(2, 0) == 0
+    assert L.moe_kernel_launch_count() == 0

@@ -1,0 +1,144 @@
+"""GPU parity of the fused decode path (top-k gate, route map and expand +
+E4M3 cast in one cooperative launch) against the oracle, its agreement with
+the separate launches, path selection, and the bounded-wait failure path
+(a signal that is never sent; no fault, no hang)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_routing_precision_gb300 import ops, workloads
+from tests.parity_util import assert_equal, assert_f32_bits_equal, assert_weights_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from moe_routing_precision_gb300 import _build
+    _build.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+    assert ops.device_status() == 0
+    yield
+    ops.debug_set(ops.DEBUG_SKIP_ROUTE_SIGNAL, 0)
+    ops.debug_set(ops.DEBUG_WAIT_TIMEOUT_NS, 1_000_000_000)
+    assert ops.device_status() == 0
+
+
+def np_(t):
+    return t.detach().cpu().numpy()
+
+
+def _inputs(T, E, k, H, seed, ties=False):
+    inp = workloads.random_small(T, E, k, H, seed=seed, ties=ties, zero_groups=True)
+    return inp["scores"], inp["x"]
+
+
+def _check_against_oracle(scores, x, k, res):
+    idx, w, counts, offsets, pos, src, q, sf = res
+    E = scores.shape[1]
+    o_idx, o_w = oracle.topk_gate(scores.numpy(), k)
+    o_counts, o_off, o_pos, o_src = oracle.route_map(o_idx, E)
+    o_q, o_sf = oracle.expand_cast_fp8(oracle.bf16_bits(x), o_pos)
+    assert_equal(np_(idx), o_idx, "topk_idx")
+    assert_weights_close(np_(w), o_w)
+    assert_equal(np_(counts), o_counts, "counts")
+    assert_equal(np_(offsets), o_off, "offsets")
+    assert_equal(np_(pos), o_pos, "pos")
+    assert_equal(np_(src), o_src, "sorted_src")
+    assert_equal(np_(q), o_q, "q")
+    assert_f32_bits_equal(np_(sf), o_sf, "sf")
+
+
+CASES = [(1, 64, 2, 128), (7, 256, 8, 4096), (100, 256, 8, 7168), (1024, 256, 8, 4096),
+         (33, 128, 4, 384), (300, 64, 6, 1024), (2048, 256, 8, 512), (50, 256, 16, 256),
+         (151, 96, 3, 640), (153, 256, 8, 16384)]
+
+
+@pytest.mark.parametrize("T,E,k,H", CASES)
+@pytest.mark.parametrize("ties", [False, True])
+def test_fused_matches_oracle(T, E, k, H, ties):
+    scores, x = _inputs(T, E, k, H, seed=T + E + H, ties=ties)
+    ws = ops.route_expand_cast_workspace(T, E, k, x.to(DEV))
+    res = ops.route_expand_cast_fp8(scores.to(DEV), x.to(DEV), k, mode=ops.PATH_FUSED,
+                                    workspace=ws)
+    assert ops.device_status() == 0
+    _check_against_oracle(scores, x, k, res)
+    assert int(ws[:8].abs().sum()) == 0            # control words left zero
+
+
+@pytest.mark.parametrize("T,E,k,H", [(64, 256, 8, 4096), (1000, 128, 4, 1024)])
+def test_fused_equals_separate_launches(T, E, k, H):
+    scores, x = _inputs(T, E, k, H, seed=5)
+    s, xd = scores.to(DEV), x.to(DEV)
+    a = ops.route_expand_cast_fp8(s, xd, k, mode=ops.PATH_FUSED)
+    b = ops.route_expand_cast_fp8(s, xd, k, mode=ops.PATH_SEPARATE)
+    assert ops.device_status() == 0
+    for u, v in zip(a, b):
+        assert torch.equal(u.view(torch.uint8) if u.dtype == torch.float32 else u,
+                           v.view(torch.uint8) if v.dtype == torch.float32 else v)
+
+
+def test_back_to_back_calls_share_a_workspace():
+    T, E, k, H = 256, 256, 8, 2048
+    ws = ops.route_expand_cast_workspace(T, E, k, torch.empty(1, device=DEV))
+    outs = []
+    for seed in range(4):                           # no synchronisation between the calls
+        scores, x = _inputs(T, E, k, H, seed=seed)
+        outs.append((scores, x, ops.route_expand_cast_fp8(scores.to(DEV), x.to(DEV), k,
+                                                          mode=ops.PATH_FUSED, workspace=ws)))
+    assert ops.device_status() == 0
+    for scores, x, res in outs:
+        _check_against_oracle(scores, x, k, res)
+
+
+def test_fused_is_one_launch_and_auto_takes_the_separate_path():
+    E, k, H = 256, 8, 512
+    for T, mode, launches in [(512, ops.PATH_FUSED, 1), (512, ops.PATH_AUTO, 4),
+                              (4096, ops.PATH_AUTO, 4)]:
+        scores, x = _inputs(T, E, k, H, seed=T)
+        s, xd = scores.to(DEV), x.to(DEV)
+        ws = ops.route_expand_cast_workspace(T, E, k, xd)
+        torch.cuda.synchronize()
+        n0 = ops.launch_count()
+        res = ops.route_expand_cast_fp8(s, xd, k, mode=mode, workspace=ws)
+        assert ops.launch_count() - n0 == launches
+        assert ops.device_status() == 0
+        if T == 512:
+            _check_against_oracle(scores, x, k, res)
+
+
+@pytest.mark.parametrize("E,k", [(16, 2), (512, 8)])
+def test_fused_refuses_shapes_it_does_not_handle(E, k):
+    scores, x = _inputs(8, E, k, 256, seed=1)
+    with pytest.raises(ops.MoeError) as ei:
+        ops.route_expand_cast_fp8(scores.to(DEV), x.to(DEV), k, mode=ops.PATH_FUSED)
+    assert ei.value.rc == ops.MOE_ERR_UNSUPPORTED
+    res = ops.route_expand_cast_fp8(scores.to(DEV), x.to(DEV), k, mode=ops.PATH_AUTO)
+    assert ops.device_status() == 0
+    _check_against_oracle(scores, x, k, res)
+
+
+def test_wait_that_runs_out_reports_timeout_and_leaves_a_usable_context():
+    """Block 0 routes but never signals: every block's bounded wait runs out
+    after 20 ms, the kernel sets MOE_DEVERR_TIMEOUT and finishes, and the
+    control words are reset by the last block."""
+    T, E, k, H = 200, 256, 8, 1024
+    scores, x = _inputs(T, E, k, H, seed=3)
+    s, xd = scores.to(DEV), x.to(DEV)
+    ws = ops.route_expand_cast_workspace(T, E, k, xd)
+    ops.debug_set(ops.DEBUG_WAIT_TIMEOUT_NS, 20_000_000)
+    ops.debug_set(ops.DEBUG_SKIP_ROUTE_SIGNAL, 1)
+    try:
+        ops.route_expand_cast_fp8(s, xd, k, mode=ops.PATH_FUSED, workspace=ws)
+        bits = ops.device_status()
+    finally:
+        ops.debug_set(ops.DEBUG_SKIP_ROUTE_SIGNAL, 0)
+        ops.debug_set(ops.DEBUG_WAIT_TIMEOUT_NS, 1_000_000_000)
+    assert bits == ops.MOE_DEVERR_TIMEOUT
+    assert int(ws[:8].abs().sum()) == 0
+    res = ops.route_expand_cast_fp8(s, xd, k, mode=ops.PATH_FUSED, workspace=ws)
+    assert ops.device_status() == 0
+    _check_against_oracle(scores, x, k, res)
