@@ -54,6 +54,11 @@ def _load():
                 "oracle_e4m3_decode": (ctypes.c_double, [ctypes.c_uint8]),
                 "oracle_e4m3_encode": (ctypes.c_uint8, [ctypes.c_float]),
                 "oracle_e4m3_encode_array": (None, [P, i64, P]),
+                "oracle_e2m1_value": (ctypes.c_double, [ctypes.c_int]),
+                "oracle_e2m1_encode": (ctypes.c_uint8, [ctypes.c_float]),
+                "oracle_e2m1_encode_array": (None, [P, i64, P]),
+                "oracle_expand_cast_fp4": (ctypes.c_int, [P, i64, i32, i32, P, P, i64, i32, i32,
+                                                          i64, P, P]),
                 "oracle_bf16_from_double": (ctypes.c_uint16, [ctypes.c_double]),
                 "oracle_topk_gate": (ctypes.c_int, [P, i64, i32, i32, P, P]),
                 "oracle_route_map": (ctypes.c_int, [P, i64, i32, i32, P, P, P, P]),
@@ -147,6 +152,30 @@ def e4m3_encode(v) -> np.ndarray:
     v = _as(np.asarray(v, dtype=np.float32), np.float32)
     out = np.empty(v.shape, dtype=np.uint8)
     _load().oracle_e4m3_encode_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def e2m1_value(code: int) -> float:
+    """Value of a 4-bit E2M1 code (OCP Microscaling FP4 element type)."""
+    return _load().oracle_e2m1_value(int(code))
+
+
+def e2m1_encode(v) -> np.ndarray:
+    """Round to nearest E2M1, ties to even code, saturating at 6; one code
+    (0..15) per value."""
+    shape = np.shape(v)
+    v = _as(np.asarray(v, dtype=np.float32), np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_e2m1_encode_array(_ptr(v), v.size, _ptr(out))
+    return out.reshape(shape)
+
+
+def e2m1_unpack(packed) -> np.ndarray:
+    """[..., n/2] packed bytes -> [..., n] codes (element 2i = low nibble)."""
+    b = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(b.shape[:-1] + (b.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = b & 0xF
+    out[..., 1::2] = b >> 4
     return out
 
 
@@ -271,6 +300,25 @@ def swiglu_cast_fp8_ex(x_bits, clamp: float | None = None, weights=None, flags: 
                                              float(clamp or 0.0), _ptr(w), int(flags), int(ld),
                                              _ptr(q), _ptr(sf), _ptr(cnt)), "swiglu_cast_fp8_ex")
     return q, sf, int(cnt[0])
+
+
+def expand_cast_fp4(x_bits, pos, num_rows: int | None = None, sorted_src=None, group: int = 32,
+                    flags: int = 0, ld: int | None = None, fill: int = 0xAB):
+    """TileKernels page, 3.1 + 3.2 + 2.2 with the FP4 output type: per-group
+    E2M1 cast (max 6, clamp_min 6 * 2^-126) of each token, copied to its pos
+    rows.  -> (q [R, H/2] packed uint8, scales in the flagged layout)."""
+    x = _as(x_bits, np.uint16)
+    p = _as(pos, np.int32)
+    T, H = x.shape
+    k = p.shape[1]
+    R = (T * k if sorted_src is None else len(sorted_src)) if num_rows is None else int(num_rows)
+    src = None if sorted_src is None else _as(sorted_src, np.int32)
+    q = np.full((R, H // 2), fill, dtype=np.uint8)
+    sf, ld = sf_buffer(R, H // group, flags, ld)
+    _check(_load().oracle_expand_cast_fp4(_ptr(x), T, H, k, _ptr(p), _ptr(src), R, group,
+                                          int(flags), int(ld), _ptr(q), _ptr(sf)),
+           "expand_cast_fp4")
+    return q, sf
 
 
 def per_token_cast(x_bits, group: int = 128):

@@ -715,6 +715,166 @@ int oracle_swiglu_cast_fp8_ex(const uint16_t *x, int64_t M, int32_t N, int32_t g
 }
 
 /* ------------------------------------------------------------------------ */
+/* FP4 E2M1 cast (TileKernels page, section 3.1: CastOutputConfig's           */
+/* clamp_min_value for float4_e2m1fn is max_value * 2^-126; section 3.2:      */
+/* per-group absmax -> scale -> multiply by the inverse scale, at a group size */
+/* the config chooses, num_per_channels)                                      */
+/* ------------------------------------------------------------------------ */
+
+/* E2M1 (the FP4 element type of the OCP Microscaling Formats specification):
+ * sign bit 3, exponent bits 2..1 with bias 1, mantissa bit 0; no infinity or
+ * NaN.  Exponent field 0: subnormal m * 0.5.  Otherwise (1 + m/2) * 2^(e-1).
+ * Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double oracle_e2m1_value(int code)
+{
+    int mag = code & 7;
+    int e = mag >> 1, m = mag & 1;
+    double v = (e == 0) ? 0.5 * m : (1.0 + 0.5 * m) * ldexp(1.0, e - 1);
+    return (code & 8) ? -v : v;
+}
+
+/* Round to nearest, ties to the even code (mantissa bit 0), saturating at
+ * +-6; the sign is kept, also for a result of zero.  NaN -> 0xFF (no E2M1
+ * encoding; an error marker).  The nearest code is found by comparing the
+ * magnitude with every code value in double, which is exact for fp32 inputs. */
+uint8_t oracle_e2m1_encode(float v)
+{
+    double a;
+    int c, best = 0;
+    uint8_t sign;
+
+    if (v != v)
+        return 0xFF;
+    sign = signbit(v) ? 8 : 0;
+    a = fabs((double)v);
+    if (a >= 6.0)
+        return (uint8_t)(sign | 7);
+    for (c = 1; c < 8; ++c) {
+        double dc = fabs(a - oracle_e2m1_value(c));
+        double db = fabs(a - oracle_e2m1_value(best));
+        if (dc < db || (dc == db && (c & 1) == 0))
+            best = c;
+    }
+    return (uint8_t)(sign | best);
+}
+
+void oracle_e2m1_encode_array(const float *v, int64_t n, uint8_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        out[i] = oracle_e2m1_encode(v[i]);
+}
+
+/* Cast one group of n fp32 values to E2M1: amax = max |v|;
+ * sf = fl32(max(amax, 6 * 2^-126) / 6) (6 = the largest E2M1 value, the
+ * floor its clamp_min_value), rounded up to a power of two under the POW2 /
+ * UE8M0 options; sf_inv = fl32(1 / sf); code_i = E2M1(fl32(v_i * sf_inv)).
+ * Returns sf. */
+static float cast_group_fp4(const float *v, int n, int flags, uint8_t *codes)
+{
+    const float floor_v = ldexpf(6.0f, -126);
+    float amax = 0.0f;
+    float clamped, sf, sf_inv;
+    int i;
+
+    for (i = 0; i < n; ++i) {
+        float a = fabsf(v[i]);
+        if (a > amax)
+            amax = a;
+    }
+    clamped = (amax < floor_v) ? floor_v : amax;
+    sf = clamped / 6.0f;
+    if (flags & (ORACLE_SF_POW2 | ORACLE_SF_UE8M0))
+        sf = pow2_at_least(sf);
+    sf_inv = 1.0f / sf;
+    for (i = 0; i < n; ++i) {
+        float scaled = v[i] * sf_inv;
+        codes[i] = oracle_e2m1_encode(scaled);
+    }
+    return sf;
+}
+
+/* Two E2M1 codes per byte: element 2i in the low nibble, 2i + 1 in the high
+ * nibble (the order of the element pairs in memory). */
+static void pack_e2m1(const uint8_t *codes, int n, uint8_t *out)
+{
+    int i;
+    for (i = 0; i < n; i += 2)
+        out[i / 2] = (uint8_t)((codes[i] & 0xF) | ((codes[i + 1] & 0xF) << 4));
+}
+
+/* Expand + FP4 cast: each token's row x[t] cast per group of `group`
+ * channels (scales in the layout `flags` names, as the FP8 options), and
+ * its packed codes [H/2] and scales copied to the rows pos[t, j] >= 0 of
+ * out [num_rows][H/2] and out_sf.  Rows with sorted_src[r] < 0 (sorted_src
+ * may be NULL) get zero codes and zero scales (byte 0 for UE8M0); other rows
+ * no pos names are left untouched.  group: a divisor of H, even. */
+int oracle_expand_cast_fp4(const uint16_t *x, int64_t T, int32_t H, int32_t k,
+                           const int32_t *pos, const int32_t *sorted_src, int64_t num_rows,
+                           int32_t group, int32_t flags, int64_t ld, uint8_t *out,
+                           void *out_sf)
+{
+    int64_t t, r;
+    int32_t j, g, i, G;
+    float *buf, *sfs;
+    uint8_t *codes, *qrow;
+
+    if (T < 0 || k < 1 || group < 2 || group % 2 != 0 || H < group || H % group != 0 ||
+        num_rows < 0)
+        return 1;
+    if ((flags & ORACLE_SF_COLMAJOR) && ld < num_rows)
+        return 1;
+    G = H / group;
+    if (sorted_src) {
+        for (r = 0; r < num_rows; ++r) {
+            if (sorted_src[r] >= 0)
+                continue;
+            memset(out + r * (H / 2), 0, (size_t)(H / 2));
+            for (g = 0; g < G; ++g) {
+                if (flags & ORACLE_SF_UE8M0) {
+                    if (flags & ORACLE_SF_COLMAJOR)
+                        ((uint8_t *)out_sf)[((int64_t)(g / 4) * ld + r) * 4 + (g % 4)] = 0;
+                    else
+                        ((uint8_t *)out_sf)[r * G + g] = 0;
+                } else {
+                    store_scale(out_sf, flags, ld, G, r, g, 0.0f);
+                }
+            }
+        }
+    }
+    buf = (float *)malloc(sizeof(float) * (size_t)group);
+    sfs = (float *)malloc(sizeof(float) * (size_t)G);
+    codes = (uint8_t *)malloc((size_t)H);
+    qrow = (uint8_t *)malloc((size_t)(H / 2));
+    if (!buf || !sfs || !codes || !qrow) {
+        free(buf); free(sfs); free(codes); free(qrow);
+        return 1;
+    }
+    for (t = 0; t < T; ++t) {
+        for (g = 0; g < G; ++g) {
+            for (i = 0; i < group; ++i)
+                buf[i] = bf16_bits_to_float(x[t * H + (int64_t)g * group + i]);
+            sfs[g] = cast_group_fp4(buf, group, flags, codes + (int64_t)g * group);
+        }
+        pack_e2m1(codes, H, qrow);
+        for (j = 0; j < k; ++j) {
+            int32_t rr = pos[t * k + j];
+            if (rr < 0)
+                continue;
+            if (rr >= num_rows) {
+                free(buf); free(sfs); free(codes); free(qrow);
+                return 2;
+            }
+            memcpy(out + (int64_t)rr * (H / 2), qrow, (size_t)(H / 2));
+            for (g = 0; g < G; ++g)
+                store_scale(out_sf, flags, ld, G, rr, g, sfs[g]);
+        }
+    }
+    free(buf); free(sfs); free(codes); free(qrow);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Step 5: weighted combine ("CuTeDSL at Perplexity", combine kernel)         */
 /* ------------------------------------------------------------------------ */
 
