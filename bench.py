@@ -692,6 +692,26 @@ def cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak):
     B = algorithmic_bytes(T, E, k, H)
     b = B["route_expand_cast"] - R * G * 4 + R * G      # one scale byte per group
     gbs = b / (ms * 1e-3) / 1e9
+    # FP4 E2M1, 32-channel groups, f32 scales (same routing, same inputs)
+    q4 = torch.empty(R, H // 2, dtype=torch.uint8, device=dev)
+    sf4 = torch.empty(R, H // 32, dtype=torch.float32, device=dev)
+
+    def rec4():
+        chk(L.moe_topk_gate(s.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
+        chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
+                            pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
+        chk(L.moe_expand_cast_fp4(x.data_ptr(), T, H, k, pos.data_ptr(), None, R, q4.data_ptr(),
+                                  sf4.data_ptr(), 0, 0, None, 0, 32, sp), "expand_fp4")
+
+    ms4 = timed(rec4, max(3, iters // 2))
+    b4 = B["topk_gate"] + B["route_map"] + T * H * 2 + R * 4 + R * (H // 2) + R * (H // 32) * 4
+    gbs4 = b4 / (ms4 * 1e-3) / 1e9
+    res["prefill_64k_fp4_group32"] = {
+        "op": "topk + route_map + expand_cast_fp4 (E2M1, 32-channel groups, f32 scales)",
+        "ms": round(ms4, 4), "routed_tokens_per_s": round(R / (ms4 * 1e-3), 1),
+        "algorithmic_bytes": b4, "GB_s": round(gbs4, 1), "frac_of_peak": round(gbs4 / peak, 4),
+        "timing": "one batch after a 512 MB L2 flush, median"}
+    del q4, sf4
     res["prefill_64k_ue8m0_colmajor"] = {
         "op": "topk + route_map + expand_cast_fp8_ex (packed UE8M0, column-major)",
         "ms": round(ms, 4), "routed_tokens_per_s": round(R / (ms * 1e-3), 1),

@@ -302,6 +302,36 @@ size_t moe_expand_cast_fp8_ex_workspace_bytes(int64_t num_tokens, int32_t hidden
                                               uint32_t sf_flags);
 
 /*
+ * moe_expand_cast_fp4 -- expand + per-group FP4 E2M1 cast: [TK] 3.1
+ * (CastOutputConfig with the float4_e2m1fn output type, clamp_min_value =
+ * max_value * 2^-126 = 6 * 2^-126), 3.2 (per-group absmax -> scale ->
+ * multiply by the scale's inverse, num_per_channels channels per group) and
+ * 2.2 (copy to the rows pos names).
+ *   scale of a group: fl32(max(amax, 6 * 2^-126) / 6), or the smallest power
+ *   of two >= it under MOE_SF_POW2; code = E2M1(fl32(x * fl32(1 / scale))),
+ *   round to nearest, ties to the even code, saturating at +-6, the sign kept
+ *   (also for zero).  E2M1 (OCP MX FP4): sign bit 3, exponent bits 2..1 with
+ *   bias 1, mantissa bit 0; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+ *   out: [num_rows][H/2] u8, two codes per byte, element 2i in the low nibble.
+ *   out_sf, sf_flags, sf_ld, sorted_src, workspace: as moe_expand_cast_fp8_ex,
+ *   with G = H / group scales per row.
+ *   group: 16, 32, 64 or 128 channels per scale.
+ * Requires H % 32 == 0, H % group == 0, H <= 16384, 1 <= k <= MOE_MAX_TOPK,
+ * num_rows < 2^31, x and out 16-byte aligned.  Error bits as
+ * moe_expand_cast_fp8.
+ */
+moe_status_t moe_expand_cast_fp4(const void *x, int64_t num_tokens, int32_t hidden,
+                                 int32_t num_topk, const int32_t *pos, const int32_t *sorted_src,
+                                 int64_t num_rows, uint8_t *out, void *out_sf, uint32_t sf_flags,
+                                 int64_t sf_ld, void *workspace, size_t workspace_bytes,
+                                 int32_t group, void *stream);
+
+/* Workspace bytes moe_expand_cast_fp4 stages column-major scales in: as
+ * moe_expand_cast_fp8_ex_workspace_bytes with G = hidden / group. */
+size_t moe_expand_cast_fp4_workspace_bytes(int64_t num_tokens, int32_t hidden, int32_t group,
+                                           uint32_t sf_flags);
+
+/*
  * swiglu_cast_fp8 -- [TK] 3.3, plain form (no clamp, no top-k weight).  For
  * each row r and channel c < N, in f32:
  *   g = x[r, c] (left half, the gate), u = x[r, N + c] (right half, up)

@@ -283,6 +283,47 @@ moe_status_t moe_expand_cast_fp8_ex(const void* x, int64_t num_tokens, int32_t h
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
+size_t moe_expand_cast_fp4_workspace_bytes(int64_t num_tokens, int32_t hidden, int32_t group,
+                                           uint32_t sf_flags) {
+  if (num_tokens <= 0 || group <= 0 || hidden < group || !(sf_flags & MOE_SF_COLMAJOR)) return 0;
+  const int64_t G = hidden / group;
+  const int64_t row = (sf_flags & MOE_SF_UE8M0) ? (G + 3) / 4 * 4 : G * 4;
+  return (size_t)((num_tokens * row + 255) / 256 * 256);
+}
+
+moe_status_t moe_expand_cast_fp4(const void* x, int64_t num_tokens, int32_t hidden,
+                                 int32_t num_topk, const int32_t* pos, const int32_t* sorted_src,
+                                 int64_t num_rows, uint8_t* out, void* out_sf, uint32_t sf_flags,
+                                 int64_t sf_ld, void* workspace, size_t workspace_bytes,
+                                 int32_t group, void* stream) {
+  if (group != 16 && group != 32 && group != 64 && group != 128) return MOE_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || num_rows < 0 || hidden < 32 || hidden % 32 != 0 || hidden % group != 0 ||
+      num_topk < 1 || num_topk > MOE_MAX_TOPK)
+    return MOE_ERR_INVALID_ARG;
+  if (hidden > 16384) return MOE_ERR_UNSUPPORTED;
+  if (num_rows >= ((int64_t)1 << 31)) return MOE_ERR_INVALID_ARG;
+  if (!sf_opts_ok(sf_flags, sf_ld, num_rows, out_sf)) return MOE_ERR_INVALID_ARG;
+  if (num_tokens == 0 && (num_rows == 0 || sorted_src == nullptr)) return MOE_OK;
+  if ((num_tokens > 0 && (!x || !pos)) || (num_rows > 0 && (!out || !out_sf)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(pos, 4) || !aligned(sorted_src, 4) || !aligned(out, 16))
+    return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_expand_cast_fp4_workspace_bytes(num_tokens, hidden, group, sf_flags);
+  if (workspace != nullptr && (!aligned(workspace, 16) || workspace_bytes < need))
+    return MOE_ERR_INVALID_ARG;
+  const bool stage = need > 0 && workspace != nullptr && sorted_src != nullptr;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  SfOut sfo;
+  sfo.flags = (int)sf_flags;
+  sfo.ld = sf_ld;
+  if (stage) sfo.stage = static_cast<uint8_t*>(workspace);
+  cudaError_t e = launch_expand_cast_fp4(c, x, num_tokens, hidden, num_topk, pos, num_rows, out,
+                                         out_sf, sorted_src, sfo, group);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
 moe_status_t swiglu_cast_fp8_ex(const void* x, int64_t num_rows, int32_t n, uint8_t* out,
                                 void* out_sf, uint32_t sf_flags, int64_t sf_ld, int32_t has_clamp,
                                 float clamp, const float* weights, uint64_t* clamp_count,

@@ -82,14 +82,15 @@ __device__ __forceinline__ float group_scale(float amax) {
 // packed UE8M0 and 2.2 TMA-aligned column-major scales).  With POW2 (or
 // UE8M0) the scale is the smallest power of two >= the plain scale: a
 // positive normal f32 with a non-zero mantissa moves to the next exponent.
+__device__ __forceinline__ float round_pow2_up(float s) {
+  uint32_t b = __float_as_uint(s);
+  if (b & 0x007FFFFFu) b = (b & 0xFF800000u) + 0x00800000u;
+  return __uint_as_float(b);
+}
+
 __device__ __forceinline__ float group_scale_opts(float amax, int flags) {
-  float s = group_scale(amax);
-  if (flags & (MOE_SF_POW2 | MOE_SF_UE8M0)) {
-    uint32_t b = __float_as_uint(s);
-    if (b & 0x007FFFFFu) b = (b & 0xFF800000u) + 0x00800000u;
-    s = __uint_as_float(b);
-  }
-  return s;
+  const float s = group_scale(amax);
+  return (flags & (MOE_SF_POW2 | MOE_SF_UE8M0)) ? round_pow2_up(s) : s;
 }
 
 // Store scale `sf` of (row r, group g) in the flagged layout; UE8M0 stores
@@ -260,6 +261,50 @@ struct SfOut {
   // row by row from sorted_src with whole-line stores.
   uint8_t* stage = nullptr;
 };
+
+// Padded layouts (TileKernels article, section 2.2: expand_to_fused zero-fills
+// the rows no token lands on in the same launch).  With zsrc non-null, every
+// row r < num_rows whose zsrc[r] (the route map's sorted_src) is negative gets
+// all-zero codes and scales.  Warp-granular: a warp reads 32 entries with one
+// coalesced load and zeroes each marked row 512 bytes per store instruction.
+// These rows are disjoint from every row a copy is written to.
+__device__ __forceinline__ void zero_fill_rows(const int32_t* __restrict__ zsrc, int64_t num_rows,
+                                               int row_bytes, int G, uint8_t* __restrict__ out,
+                                               float* __restrict__ out_sf, int64_t gwarp,
+                                               int64_t nwarps, int lane, SfOut sfo) {
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (int64_t r0 = gwarp * 32; r0 < num_rows; r0 += nwarps * 32) {
+    const int64_t r = r0 + lane;
+    const bool z = r < num_rows && __ldg(zsrc + r) < 0;
+    unsigned m = __ballot_sync(0xFFFFFFFFu, z);
+    while (m) {
+      const int i = __ffs(m) - 1;
+      m &= m - 1;
+      uint8_t* q = out + (r0 + i) * row_bytes;  // row_bytes: a multiple of 16
+      for (int c = lane * 16; c < row_bytes; c += 512) st_stream_v4(q + c, zero);
+      if (sfo.stage != nullptr) {
+        // staged column-major scales: the gather writes these rows' zeros
+      } else if (sfo.flags == 0) {
+        float* sfr = out_sf + (r0 + i) * G;
+        for (int g = lane; g < G; g += 32) st_stream_f32(sfr + g, 0.0f);
+      } else {
+        for (int g = lane; g < G; g += 32)
+          store_sf_opts(out_sf, sfo.flags, sfo.ld, G, r0 + i, g, 0.0f, true);
+      }
+    }
+  }
+}
+
+// Expand + FP4 E2M1 cast (expand_cast_fp4.cu): group 16, 32, 64 or 128.
+cudaError_t launch_expand_cast_fp4(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
+                                   const int32_t* pos, int64_t R, uint8_t* out, void* out_sf,
+                                   const int32_t* zero_rows, SfOut sfo, int group);
+
+// Column-major scales from staged per-token rows (SfOut::stage), row by row
+// from sorted_src; in expand_cast.cu.
+cudaError_t launch_sf_gather(const LaunchCtx& c, const int32_t* src, int64_t R, int64_t T, int k,
+                             int G, SfOut sfo, void* out_sf);
+
 cudaError_t launch_expand_cast(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                                const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
                                const int32_t* zero_rows = nullptr, SfOut sfo = SfOut());

@@ -53,39 +53,6 @@ __device__ __forceinline__ void load_tile(const uint16_t* __restrict__ x,
   }
 }
 
-// Padded layouts (TileKernels article, section 2.2: expand_to_fused zero-fills
-// the rows no token lands on in the same launch).  With zsrc non-null, every
-// row r < num_rows whose zsrc[r] (the route map's sorted_src) is negative gets
-// all-zero codes and scales.  Warp-granular: a warp reads 32 entries with one
-// coalesced load and zeroes each marked row 512 bytes per store instruction.
-// These rows are disjoint from every row a copy is written to.
-__device__ __forceinline__ void zero_fill_rows(const int32_t* __restrict__ zsrc, int64_t num_rows,
-                                               int H, int G, uint8_t* __restrict__ out,
-                                               float* __restrict__ out_sf, int64_t gwarp,
-                                               int64_t nwarps, int lane, SfOut sfo) {
-  const uint4 zero = make_uint4(0, 0, 0, 0);
-  for (int64_t r0 = gwarp * 32; r0 < num_rows; r0 += nwarps * 32) {
-    const int64_t r = r0 + lane;
-    const bool z = r < num_rows && __ldg(zsrc + r) < 0;
-    unsigned m = __ballot_sync(0xFFFFFFFFu, z);
-    while (m) {
-      const int i = __ffs(m) - 1;
-      m &= m - 1;
-      uint8_t* q = out + (r0 + i) * H;
-      for (int c = lane * 16; c < H; c += 512) st_stream_v4(q + c, zero);
-      if (sfo.stage != nullptr) {
-        // staged column-major scales: the gather writes these rows' zeros
-      } else if (sfo.flags == 0) {
-        float* sfr = out_sf + (r0 + i) * G;
-        for (int g = lane; g < G; g += 32) st_stream_f32(sfr + g, 0.0f);
-      } else {
-        for (int g = lane; g < G; g += 32)
-          store_sf_opts(out_sf, sfo.flags, sfo.ld, G, r0 + i, g, 0.0f, true);
-      }
-    }
-  }
-}
-
 // G4: G % 4 == 0 (and out_sf 16-byte aligned), so a warp's 4 units are 4
 // consecutive groups of one token and their 4 scales form one aligned 16-byte
 // vector per destination row.
@@ -507,13 +474,6 @@ __global__ void __launch_bounds__(256) sf_gather_kernel(const uint8_t* __restric
   }
 }
 
-cudaError_t launch_sf_gather(const LaunchCtx& c, const int32_t* src, int64_t R, int64_t T, int k,
-                             int G, SfOut sfo, void* out_sf) {
-  if (R == 0) return cudaSuccess;
-  const int64_t blocks = (R + 255) / 256;
-  return launch_pdl(sf_gather_kernel, (int)blocks, 256, 0, c.stream,
-                    static_cast<const uint8_t*>(sfo.stage), src, R, T, k, G, sfo, out_sf, c.err);
-}
 
 cudaError_t launch_expand_cast_kernel(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                                       const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
@@ -534,6 +494,14 @@ cudaError_t launch_expand_cast_kernel(const LaunchCtx& c, const void* x, int64_t
 }
 
 }  // namespace
+
+cudaError_t launch_sf_gather(const LaunchCtx& c, const int32_t* src, int64_t R, int64_t T, int k,
+                             int G, SfOut sfo, void* out_sf) {
+  if (R == 0) return cudaSuccess;
+  const int64_t blocks = (R + 255) / 256;
+  return launch_pdl(sf_gather_kernel, (int)blocks, 256, 0, c.stream,
+                    static_cast<const uint8_t*>(sfo.stage), src, R, T, k, G, sfo, out_sf, c.err);
+}
 
 cudaError_t launch_expand_cast(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                                const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,

@@ -1,0 +1,212 @@
+// expand_cast_fp4.cu -- expand + per-group FP4 E2M1 cast.
+//
+// TileKernels article (itsolotime.com): section 3.1's CastOutputConfig names
+// float4_e2m1fn as an output type with clamp_min_value = max_value * 2^-126
+// (max_value = 6, so the scale stays a normal f32 and its inverse finite);
+// section 3.2's per_token_cast takes the group absmax over num_per_channels
+// channels, scale = max(amax, clamp_min) / max_value, and multiplies by the
+// scale's inverse; section 2.2's expand_to_fused copies each token's codes and
+// scales to the rows pos names.  Two codes per byte, element 2i in the low
+// nibble.  Group sizes 16, 32, 64 and 128 (1, 2, 4 or 8 lanes of 16 channels).
+//
+// Same structure as the E4M3 bulk-store kernel: one CTA per token slice,
+// thread c owning channels 16c..16c+15; the token's packed codes (H/2 bytes)
+// and, for plain row-major f32 scales with G % 4 == 0, its scales are staged
+// in shared memory and leave with TMA bulk copies (cp.async.bulk) issued by one
+// thread; other scale layouts are stored per group by one lane, or staged per
+// token for the column-major gather.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kFp4Buffers = 4;
+constexpr int kFp4CtasPerSm = 3;
+
+// clamp_min_value of float4_e2m1fn: 6 * 2^-126 = 1.5 * 2^-124.
+__device__ __forceinline__ float fp4_floor() { return __uint_as_float(0x01C00000u); }
+
+__device__ __forceinline__ float fp4_scale(float amax, int flags) {
+  const float s = __fdiv_rn(fmaxf(amax, fp4_floor()), 6.0f);
+  return (flags & (MOE_SF_POW2 | MOE_SF_UE8M0)) ? round_pow2_up(s) : s;
+}
+
+// Two f32 values -> one byte of two E2M1 codes (round to nearest even,
+// saturate to +-6), `lo` in the low nibble: the hardware conversion
+// cvt.rn.satfinite.e2m1x2.f32, whose first source goes to the high nibble.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;\n}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 16 bf16 values times `inv` -> 8 bytes of packed E2M1 codes.
+__device__ __forceinline__ uint2 quant16_bf16_e2m1(const uint4& a, const uint4& b, float inv) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t c[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t byte = e2m1x2(__fmul_rn(bf16_lo(w[i]), inv), __fmul_rn(bf16_hi(w[i]), inv));
+    c[i >> 2] |= byte << (8 * (i & 3));
+  }
+  return make_uint2(c[0], c[1]);
+}
+
+// Max over the L lanes of an aligned L-lane subgroup.
+template <int L>
+__device__ __forceinline__ float maxL(float m) {
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  return m;
+}
+
+__device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
+               "r"(bytes)
+               : "memory");
+}
+
+// L = lanes per group (group = 16 L channels).  sf_bulk: plain row-major f32
+// scales whose rows (4G bytes) are 16-byte multiples go out with the codes.
+template <int L, int NBUF>
+__global__ void __launch_bounds__(1024) expand_cast_fp4_kernel(
+    const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
+    int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf,
+    const int32_t* __restrict__ zsrc, SfOut sfo, int sf_bulk, unsigned* err) {
+  extern __shared__ __align__(128) uint8_t s_buf[];
+  pdl_enter();
+  const int P = H >> 4;  // threads per token
+  const int G = P / L;   // groups per token
+  const int HB = H >> 1; // code bytes per row
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const bool act = tid < P;
+  const int g = tid / L;
+  const bool lead = (tid % L) == 0;
+  const uint32_t stride = (uint32_t)((HB + 4 * G + 127) / 128 * 128);  // bytes per buffer
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(s_buf);
+  bool bad = false;
+  int64_t t = blockIdx.x;
+  uint4 a = make_uint4(0, 0, 0, 0), b = a;
+  int32_t pnext = -1;  // warp 0: lane j holds pos[t, j] (j < k <= 32)
+  if (t < T) {
+    if (act) {
+      const uint16_t* src = x + t * H + tid * 16;
+      a = ld_stream_v4(src);
+      b = ld_stream_v4(src + 8);
+    }
+    if (tid < 32 && lane < k) pnext = __ldg(pos + t * k + lane);
+  }
+  int it = 0;
+  for (; t < T; t += gridDim.x, ++it) {
+    const uint4 ca = a, cb = b;
+    const int32_t pcur = pnext;
+    const int64_t tn = t + gridDim.x;
+    if (tn < T) {  // the next token's loads stay in flight during this one
+      if (act) {
+        const uint16_t* src = x + tn * H + tid * 16;
+        a = ld_stream_v4(src);
+        b = ld_stream_v4(src + 8);
+      }
+      if (tid < 32) pnext = (lane < k) ? __ldg(pos + tn * k + lane) : -1;
+    }
+    const float amax = maxL<L>(absmax16_bf16(ca, cb));
+    const float sf = fp4_scale(amax, sfo.flags);
+    const float inv = __fdiv_rn(1.0f, sf);
+    const uint2 q = quant16_bf16_e2m1(ca, cb, inv);
+    const int buf = it % NBUF;
+    if (it >= NBUF) {  // this buffer's copies from NBUF tokens ago must have read it
+      if (tid == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(NBUF - 1) : "memory");
+      __syncthreads();
+    }
+    uint8_t* sq = s_buf + (size_t)buf * stride;
+    int32_t* spos = reinterpret_cast<int32_t*>(s_buf + (size_t)NBUF * stride) + buf * 32;
+    if (act) {
+      *reinterpret_cast<uint2*>(sq + tid * 8) = q;
+      if (lead && sf_bulk) *reinterpret_cast<float*>(sq + HB + 4 * g) = sf;
+    }
+    if (!sf_bulk && tid < 32) spos[tid] = pcur;  // destinations, for every warp
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the copies
+    __syncthreads();
+    if (!sf_bulk && act && lead) {  // one lane per group stores its scale
+      if (sfo.stage != nullptr) {
+        store_stage(sfo.stage, sfo.flags, G, t, g, sf);
+      } else {
+        for (int j = 0; j < k; ++j) {
+          const int32_t r = spos[j];
+          if (r >= 0 && r < R) store_sf_opts(out_sf, sfo.flags, sfo.ld, G, r, g, sf);
+        }
+      }
+    }
+    if (tid < 32) {
+      for (int j = 0; j < k; ++j) {
+        const int32_t r = __shfl_sync(0xFFFFFFFFu, pcur, j);
+        if (tid == 0 && r >= 0) {
+          if (r >= R) {
+            bad = true;
+          } else {
+            bulk_s2g(out + (int64_t)r * HB, sbase + buf * stride, (uint32_t)HB);
+            if (sf_bulk)
+              bulk_s2g(out_sf + (int64_t)r * G, sbase + buf * stride + HB, (uint32_t)(4 * G));
+          }
+        }
+      }
+      if (tid == 0) asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+  }
+  // the copies read shared memory until they complete: wait before exiting
+  if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  if (zsrc != nullptr)
+    zero_fill_rows(zsrc, R, HB, G, out, out_sf,
+                   (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x,
+                   ((int64_t)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31, sfo);
+  if (bad) flag_error(err, MOE_DEVERR_POS_RANGE);
+}
+
+template <int L>
+cudaError_t launch_l(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
+                     const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
+                     const int32_t* zsrc, SfOut sfo) {
+  constexpr int NBUF = kFp4Buffers;
+  const int P = H / 16;
+  const int threads = (P + 31) / 32 * 32;
+  const int G = P / L;
+  const size_t stride = (size_t)(H / 2 + 4 * G + 127) / 128 * 128;
+  const size_t smem = stride * NBUF + sizeof(int32_t) * 32 * NBUF;
+  if (smem > 48 * 1024) {
+    cudaError_t st = cudaFuncSetAttribute(expand_cast_fp4_kernel<L, NBUF>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (st != cudaSuccess) return st;
+  }
+  const int sf_bulk = (sfo.flags == 0 && sfo.stage == nullptr && G % 4 == 0 &&
+                       reinterpret_cast<uintptr_t>(out_sf) % 16 == 0)
+                          ? 1
+                          : 0;
+  const int64_t cap = (int64_t)c.num_sms * kFp4CtasPerSm;
+  const int blocks = (int)(T < cap ? (T > 0 ? T : 1) : cap);  // >= 1: zero-fill with T = 0
+  return launch_pdl(expand_cast_fp4_kernel<L, NBUF>, blocks, threads, smem, c.stream,
+                    static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, zsrc, sfo,
+                    sf_bulk, c.err);
+}
+
+}  // namespace
+
+cudaError_t launch_expand_cast_fp4(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
+                                   const int32_t* pos, int64_t R, uint8_t* out, void* out_sf,
+                                   const int32_t* zero_rows, SfOut sfo, int group) {
+  float* sf = static_cast<float*>(out_sf);
+  cudaError_t e;
+  switch (group) {
+    case 16: e = launch_l<1>(c, x, T, H, k, pos, R, out, sf, zero_rows, sfo); break;
+    case 32: e = launch_l<2>(c, x, T, H, k, pos, R, out, sf, zero_rows, sfo); break;
+    case 64: e = launch_l<4>(c, x, T, H, k, pos, R, out, sf, zero_rows, sfo); break;
+    case 128: e = launch_l<8>(c, x, T, H, k, pos, R, out, sf, zero_rows, sfo); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess || sfo.stage == nullptr) return e;
+  return launch_sf_gather(c, zero_rows, R, T, k, H / group, sfo, out_sf);
+}
+
+}  // namespace moe

@@ -43,6 +43,10 @@ SIGNATURES = {
                                               ctypes.c_uint32, _i64, _P, ctypes.c_size_t, _i32,
                                               _P]),
     "moe_expand_cast_fp8_ex_workspace_bytes": (ctypes.c_size_t, [_i64, _i32, ctypes.c_uint32]),
+    "moe_expand_cast_fp4": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _P, _i64, _P, _P,
+                                           ctypes.c_uint32, _i64, _P, ctypes.c_size_t, _i32, _P]),
+    "moe_expand_cast_fp4_workspace_bytes": (ctypes.c_size_t, [_i64, _i32, _i32,
+                                                              ctypes.c_uint32]),
     "moe_route_expand_cast_fp8": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _i32, _P, _P, _P, _P,
                                                  _P, _P, _P, _P, _P, ctypes.c_size_t, _i32, _i32,
                                                  _P]),
@@ -319,6 +323,36 @@ def expand_cast_fp8_ex(x: torch.Tensor, pos: torch.Tensor, num_rows: int | None 
     return q, out_sf
 
 
+def expand_cast_fp4(x: torch.Tensor, pos: torch.Tensor, num_rows: int | None = None, *,
+                    group: int = 32, sorted_src=None, sf_flags: int = 0, sf_ld: int | None = None,
+                    out=None, out_sf=None, workspace=None, stream=None):
+    """Expand + per-group FP4 E2M1 cast -> (q [R, H/2] packed uint8, scales in
+    the flagged layout).  workspace: None, True (allocate) or a uint8 CUDA
+    tensor, for column-major scales written from sorted_src."""
+    _dev(x, "x", torch.bfloat16)
+    _dev(pos, "pos", torch.int32)
+    T, H = x.shape
+    k = pos.shape[1]
+    if sorted_src is not None:
+        _dev(sorted_src, "sorted_src", torch.int32)
+    R = (T * k if sorted_src is None else sorted_src.shape[0]) if num_rows is None else int(num_rows)
+    if sf_ld is None and (sf_flags & SF_COLMAJOR):
+        sf_ld = (R + 3) // 4 * 4
+    q = out if out is not None else _empty((R, H // 2), torch.uint8, x)
+    _dev(q, "out", torch.uint8, (R, H // 2))
+    if out_sf is None:
+        out_sf, sf_ld = sf_empty(R, H // group, sf_flags, sf_ld, x)
+    if workspace is True:
+        n = int(lib().moe_expand_cast_fp4_workspace_bytes(T, H, group, sf_flags))
+        workspace = _empty((n,), torch.uint8, x) if n > 0 else None
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    rc = lib().moe_expand_cast_fp4(_ptr(x), T, H, k, _ptr(pos), _ptr(sorted_src), R, _ptr(q),
+                                   _ptr(out_sf), sf_flags, int(sf_ld or R), _ptr(workspace),
+                                   ws_bytes, group, _stream(stream))
+    _check(rc, "moe_expand_cast_fp4")
+    return q, out_sf
+
+
 def swiglu_cast_fp8_ex(x: torch.Tensor, *, clamp: float | None = None, weights=None,
                        clamp_count=None, sf_flags: int = 0, sf_ld: int | None = None, out=None,
                        out_sf=None, stream=None):
@@ -432,6 +466,6 @@ def launch_count() -> int:
 __all__ = ["lib", "MoeError", "topk_gate", "route_map", "route_map_workspace_bytes",
            "route_map_aligned", "expand_cast_fp8_padded", "expand_cast_fp8_ex",
            "expand_cast_fp8_ex_workspace_bytes", "swiglu_cast_fp8_ex", "sf_empty",
-           "route_expand_cast_fp8", "route_expand_cast_workspace", "debug_set",
+           "route_expand_cast_fp8", "route_expand_cast_workspace", "debug_set", "expand_cast_fp4",
            "expand_cast_fp8", "swiglu_cast_fp8", "combine", "peak_copy", "device_status",
            "launch_count", "SIGNATURES"]

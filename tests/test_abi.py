@@ -216,3 +216,24 @@ def test_route_expand_cast_rejects_bad_arguments(L):
     assert L.moe_debug_set(1, 10**9) == 0
     assert L.moe_debug_set(2, 0) == 0
     assert L.moe_kernel_launch_count() == 0
+
+
+def test_fp4_entry_point_rejects_bad_arguments(L):
+    f = L.moe_expand_cast_fp4
+    def args(H=512, group=32, flags=0, ld=0, x=FAKE, out=FAKE, ws=None, wsb=0):
+        return (x, 4, H, 2, FAKE, FAKE, 8, out, FAKE, flags, ld, ws, wsb, group, None)
+    assert f(*args(group=48)) == UNSUPPORTED
+    assert f(*args(group=256)) == UNSUPPORTED
+    assert f(*args(H=496)) == INVALID               # H % 32
+    assert f(*args(H=384, group=256)) == UNSUPPORTED
+    assert f(*args(H=288, group=128)) == INVALID     # H % group
+    assert f(*args(H=32768)) == UNSUPPORTED
+    assert f(*args(flags=4)) == INVALID              # UE8M0 without POW2
+    assert f(*args(flags=1, ld=6)) == INVALID        # ld < rows
+    assert f(*args(x=FAKE + 8)) == INVALID
+    assert f(*args(out=FAKE + 8)) == INVALID
+    need = L.moe_expand_cast_fp4_workspace_bytes(4, 512, 32, 1)
+    assert need == 256 and L.moe_expand_cast_fp4_workspace_bytes(4, 512, 32, 2) == 0
+    assert L.moe_expand_cast_fp4_workspace_bytes(1000, 7168, 32, 1) == (1000 * 224 * 4 + 255) // 256 * 256
+    assert f(*args(flags=1, ld=8, ws=FAKE, wsb=need - 1)) == INVALID
+    assert L.moe_kernel_launch_count() == 0

@@ -1,0 +1,147 @@
+"""GPU parity of the FP4 E2M1 expand + cast (TileKernels article, sections
+3.1, 3.2 and 2.2 with the float4_e2m1fn output type) against the oracle:
+packed codes and every scale-buffer byte bit-exact, for every group size,
+scale layout, padded rows and the values at the edges of the format."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_routing_precision_gb300 import ops, workloads
+from tests.parity_util import assert_equal
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from moe_routing_precision_gb300 import _build
+    _build.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+    assert ops.device_status() == 0
+    yield
+    assert ops.device_status() == 0
+
+
+def np_(t):
+    return t.detach().cpu().numpy()
+
+
+def _raw_equal(gpu_sf, ref_sf, what):
+    assert_equal(np.ascontiguousarray(np_(gpu_sf)).view(np.uint8),
+                 np.ascontiguousarray(ref_sf).view(np.uint8), what)
+
+
+def _sentinel_sf(rows, G, flags, ld):
+    ref, ld = oracle.sf_buffer(rows, G, flags, ld)
+    return torch.from_numpy(ref.copy()).to(DEV), ld
+
+
+SHAPES = [(9, 256, 2), (13, 384, 3), (40, 512, 4), (21, 7168, 8), (5, 4096, 2), (3, 16384, 2)]
+
+
+@pytest.mark.parametrize("group", [16, 32, 64, 128])
+@pytest.mark.parametrize("flags", [0, 2, 6])
+@pytest.mark.parametrize("T,H,k", SHAPES)
+def test_expand_fp4_parity(group, flags, T, H, k):
+    if H % group:
+        pytest.skip("H not a multiple of the group")
+    x = workloads.random_small(T, 16, k, H, seed=T * H + group + flags, zero_groups=True)["x"]
+    R = T * k + 5                                   # rows no pos names stay untouched
+    g = torch.Generator().manual_seed(group + H)
+    pos = torch.randperm(R, generator=g)[:T * k].to(torch.int32).view(T, k)
+    pos[::4, 0] = -1                                # dropped copies
+    q = torch.full((R, H // 2), 0xAB, dtype=torch.uint8, device=DEV)
+    sf, ld = _sentinel_sf(R, H // group, flags, None)
+    ops.expand_cast_fp4(x.to(DEV), pos.to(DEV), R, group=group, sf_flags=flags, out=q, out_sf=sf)
+    assert ops.device_status() == 0
+    o_q, o_sf = oracle.expand_cast_fp4(oracle.bf16_bits(x), pos.numpy(), num_rows=R, group=group,
+                                       flags=flags)
+    assert_equal(np_(q), o_q, f"fp4 q group={group} flags={flags}")
+    _raw_equal(sf, o_sf, f"fp4 sf group={group} flags={flags}")
+
+
+@pytest.mark.parametrize("group", [16, 32, 128])
+@pytest.mark.parametrize("flags,staged", [(1, False), (1, True), (3, True), (7, False), (7, True)])
+def test_expand_fp4_colmajor_and_padded(group, flags, staged):
+    T, E, k, H, align = 60, 16, 4, 1024, 32
+    x = workloads.random_small(T, E, k, H, seed=group + flags, zero_groups=True)["x"]
+    g = torch.Generator().manual_seed(7)
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    _, _, o_pos, o_src = oracle.route_map_aligned(idx.numpy(), E, align)
+    R = o_src.size
+    ld = (R + 3) // 4 * 4 + 4
+    q = torch.full((R, H // 2), 0xAB, dtype=torch.uint8, device=DEV)
+    sf, ld = _sentinel_sf(R, H // group, flags, ld)
+    ops.expand_cast_fp4(x.to(DEV), torch.from_numpy(o_pos).to(DEV), group=group,
+                        sorted_src=torch.from_numpy(o_src).to(DEV), sf_flags=flags, sf_ld=ld,
+                        out=q, out_sf=sf, workspace=True if staged else None)
+    assert ops.device_status() == 0
+    o_q, o_sf = oracle.expand_cast_fp4(oracle.bf16_bits(x), o_pos, sorted_src=o_src, group=group,
+                                       flags=flags, ld=ld)
+    assert_equal(np_(q), o_q, "fp4 padded q")
+    _raw_equal(sf, o_sf, "fp4 padded sf")
+
+
+@pytest.mark.parametrize("group", [16, 32])
+def test_expand_fp4_format_edges(group):
+    H = 512
+    bf = torch.finfo(torch.bfloat16)
+    rows = [torch.full((H,), bf.max), torch.full((H,), -bf.tiny), torch.zeros(H),
+            torch.linspace(-3e4, 3e4, H), torch.randn(H) * 1e-38]
+    r = torch.zeros(H)
+    r[::2] = -0.0
+    rows.append(r)
+    r = torch.randn(H)
+    r[5] = 1e30
+    rows.append(r)
+    # every E2M1 midpoint and value, times a group max of 6 (scale exactly 1)
+    mids = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+                         -0.25, -5.0])
+    r = mids.repeat(H // 16)
+    rows.append(r)
+    r = torch.zeros(H)                              # multiply-by-inverse case
+    r[0::group] = 0.030517578125
+    r[1::group] = 0.003814697265625
+    rows.append(r)
+    x = torch.stack(rows).to(torch.bfloat16)
+    T = x.shape[0]
+    pos = workloads.random_permutation_pos(T, 2, seed=2)
+    q, sf = ops.expand_cast_fp4(x.to(DEV), pos.to(DEV), group=group)
+    o_q, o_sf = oracle.expand_cast_fp4(oracle.bf16_bits(x), pos.numpy(), group=group)
+    assert_equal(np_(q), o_q, "fp4 edges q")
+    _raw_equal(sf, o_sf, "fp4 edges sf")
+
+
+def test_expand_fp4_flags_pos_out_of_range():
+    T, k, H = 4, 2, 256
+    x = workloads.random_small(T, 16, k, H, seed=4)["x"].to(DEV)
+    pos = torch.tensor([[0, 1], [2, 3], [4, 8], [5, 6]], dtype=torch.int32, device=DEV)
+    q = torch.zeros(8, H // 2, dtype=torch.uint8, device=DEV)
+    sf = torch.zeros(8, H // 32, device=DEV)
+    ops.expand_cast_fp4(x, pos, 8, group=32, out=q, out_sf=sf)
+    assert ops.device_status() == ops.MOE_DEVERR_POS_RANGE
+    assert int(q[7].sum()) == 0
+
+
+def test_expand_fp4_full_size_sampled_rows():
+    """prefill_64k inputs, group 32 (the bench's FP4 launch): sampled tokens'
+    rows against the oracle."""
+    w = workloads.WORKLOADS["prefill_64k"]
+    inp = workloads.make_inputs(w, seed=0, device=DEV)
+    idx, _ = ops.topk_gate(inp["scores"], w.k)
+    _, _, pos, _ = ops.route_map(idx, w.E)
+    q, sf = ops.expand_cast_fp4(inp["x"], pos, group=32)
+    assert ops.device_status() == 0
+    rng = np.random.default_rng(0)
+    toks = np.sort(rng.choice(w.T, 300, replace=False))
+    xs = inp["x"][torch.from_numpy(toks).to(DEV)].cpu()
+    pos_np = np_(pos)[toks]
+    o_q, o_sf = oracle.expand_cast_fp4(oracle.bf16_bits(xs), np.arange(300, dtype=np.int32)[:, None],
+                                       group=32)
+    for i in range(300):
+        for j in range(w.k):
+            r = pos_np[i, j]
+            assert np.array_equal(np_(q[r]), o_q[i]) and np.array_equal(np_(sf[r]), o_sf[i])
