@@ -20,8 +20,11 @@
 namespace moe {
 namespace {
 
+// Measured on GB300 (prefill-sized expand, H = 7168, group 32): two CTAs per
+// SM (both resident by registers) 86 % of peak, three (one waiting for a
+// slot) 82 %; a second token of register prefetch did not help.
 constexpr int kFp4Buffers = 4;
-constexpr int kFp4CtasPerSm = 3;
+constexpr int kFp4CtasPerSm = 2;
 
 // clamp_min_value of float4_e2m1fn: 6 * 2^-126 = 1.5 * 2^-124.
 __device__ __forceinline__ float fp4_floor() { return __uint_as_float(0x01C00000u); }
@@ -75,6 +78,7 @@ __global__ void __launch_bounds__(1024) expand_cast_fp4_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
     int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf,
     const int32_t* __restrict__ zsrc, SfOut sfo, int sf_bulk, unsigned* err) {
+  static_assert(NBUF >= 2, "the buffer-reuse wait keeps NBUF - 2 copy groups in flight");
   extern __shared__ __align__(128) uint8_t s_buf[];
   pdl_enter();
   const int P = H >> 4;  // threads per token
@@ -117,10 +121,6 @@ __global__ void __launch_bounds__(1024) expand_cast_fp4_kernel(
     const float inv = __fdiv_rn(1.0f, sf);
     const uint2 q = quant16_bf16_e2m1(ca, cb, inv);
     const int buf = it % NBUF;
-    if (it >= NBUF) {  // this buffer's copies from NBUF tokens ago must have read it
-      if (tid == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(NBUF - 1) : "memory");
-      __syncthreads();
-    }
     uint8_t* sq = s_buf + (size_t)buf * stride;
     int32_t* spos = reinterpret_cast<int32_t*>(s_buf + (size_t)NBUF * stride) + buf * 32;
     if (act) {
@@ -153,7 +153,13 @@ __global__ void __launch_bounds__(1024) expand_cast_fp4_kernel(
           }
         }
       }
-      if (tid == 0) asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      if (tid == 0) {
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        // buffer (it + 2) % NBUF is written two tokens from now, after the
+        // next token's barrier: its copies (NBUF - 2 groups back) must have
+        // read it by then.  One barrier per token instead of two.
+        asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(NBUF - 2) : "memory");
+      }
     }
   }
   // the copies read shared memory until they complete: wait before exiting
