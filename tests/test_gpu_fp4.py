@@ -145,3 +145,23 @@ def test_expand_fp4_full_size_sampled_rows():
         for j in range(w.k):
             r = pos_np[i, j]
             assert np.array_equal(np_(q[r]), o_q[i]) and np.array_equal(np_(sf[r]), o_sf[i])
+
+
+def test_expand_fp4_skewed_size_sampled_rows():
+    """skewed_8k inputs (T=8192, H=7168, k=8; inputs above L2 size), group 32:
+    sampled tokens' rows against the oracle."""
+    w = workloads.WORKLOADS["skewed_8k"]
+    inp = workloads.make_inputs(w, seed=0, device=DEV)
+    idx, _ = ops.topk_gate(inp["scores"], w.k)
+    _, _, pos, _ = ops.route_map(idx, w.E)
+    q, sf = ops.expand_cast_fp4(inp["x"], pos, group=32)
+    assert ops.device_status() == 0
+    toks = np.sort(np.random.default_rng(1).choice(w.T, 200, replace=False))
+    xs = inp["x"][torch.from_numpy(toks).to(DEV)].cpu()
+    pos_np = np_(pos)[toks]
+    o_q, o_sf = oracle.expand_cast_fp4(oracle.bf16_bits(xs), np.arange(200, dtype=np.int32)[:, None],
+                                       group=32)
+    for i in range(200):
+        for j in range(w.k):
+            r = pos_np[i, j]
+            assert np.array_equal(np_(q[r]), o_q[i]) and np.array_equal(np_(sf[r]), o_sf[i])
