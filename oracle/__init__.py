@@ -57,6 +57,8 @@ def _load():
                 "oracle_e2m1_value": (ctypes.c_double, [ctypes.c_int]),
                 "oracle_e2m1_encode": (ctypes.c_uint8, [ctypes.c_float]),
                 "oracle_e2m1_encode_array": (None, [P, i64, P]),
+                "oracle_swiglu_cast_fp4": (ctypes.c_int, [P, i64, i32, i32, i32, ctypes.c_float, P,
+                                                          i32, i64, P, P, P]),
                 "oracle_expand_cast_fp4": (ctypes.c_int, [P, i64, i32, i32, P, P, i64, i32, i32,
                                                           i64, P, P]),
                 "oracle_bf16_from_double": (ctypes.c_uint16, [ctypes.c_double]),
@@ -319,6 +321,24 @@ def expand_cast_fp4(x_bits, pos, num_rows: int | None = None, sorted_src=None, g
                                           int(flags), int(ld), _ptr(q), _ptr(sf)),
            "expand_cast_fp4")
     return q, sf
+
+
+def swiglu_cast_fp4(x_bits, group: int = 32, clamp: float | None = None, weights=None,
+                    flags: int = 0, ld: int | None = None):
+    """TileKernels page, 3.3 with the FP4 output type: SwiGLU (optional clamp
+    and per-row weight) then the per-group E2M1 cast.  -> (q [M, N/2] packed,
+    scales in the flagged layout, clamp count)."""
+    x = _as(x_bits, np.uint16)
+    M, N2 = x.shape
+    N = N2 // 2
+    w = None if weights is None else _as(np.asarray(weights, np.float32), np.float32)
+    q = np.empty((M, N // 2), dtype=np.uint8)
+    sf, ld = sf_buffer(M, N // group, flags, ld)
+    cnt = np.zeros(1, dtype=np.uint64)
+    _check(_load().oracle_swiglu_cast_fp4(_ptr(x), M, N, group, int(clamp is not None),
+                                          float(clamp or 0.0), _ptr(w), int(flags), int(ld),
+                                          _ptr(q), _ptr(sf), _ptr(cnt)), "swiglu_cast_fp4")
+    return q, sf, int(cnt[0])
 
 
 def per_token_cast(x_bits, group: int = 128):

@@ -874,6 +874,72 @@ int oracle_expand_cast_fp4(const uint16_t *x, int64_t T, int32_t H, int32_t k,
     return 0;
 }
 
+/* SwiGLU + FP4 E2M1 cast: the SwiGLU values of oracle_swiglu_cast_fp8_ex
+ * (same clamp, weight and clamp count), cast per group of `group` channels
+ * with cast_group_fp4 (max 6, clamp_min 6 * 2^-126); codes packed two per
+ * byte, element 2i in the low nibble: q [M][N/2].  Scales as the options
+ * name them. */
+int oracle_swiglu_cast_fp4(const uint16_t *x, int64_t M, int32_t N, int32_t group,
+                           int32_t has_clamp, float clamp, const float *weights, int32_t flags,
+                           int64_t ld, uint8_t *q, void *out_sf, uint64_t *clamp_count)
+{
+    int64_t r;
+    int32_t c, g, G;
+    float *v;
+    uint8_t *codes;
+    uint64_t count = 0;
+
+    if (M < 0 || group < 2 || group % 2 != 0 || N < group || N % group != 0)
+        return 1;
+    if ((flags & ORACLE_SF_COLMAJOR) && ld < M)
+        return 1;
+    G = N / group;
+    v = (float *)malloc(sizeof(float) * (size_t)N);
+    codes = (uint8_t *)malloc((size_t)N);
+    if (!v || !codes) {
+        free(v); free(codes);
+        return 1;
+    }
+    for (r = 0; r < M; ++r) {
+        const uint16_t *row = x + r * 2 * (int64_t)N;
+        for (c = 0; c < N; ++c) {
+            float gt = bf16_bits_to_float(row[c]);
+            float u = bf16_bits_to_float(row[N + c]);
+            float e, den, silu, val;
+            if (has_clamp) {
+                if (gt > clamp) {
+                    gt = clamp;
+                    count += 1;
+                }
+                if (u > clamp) {
+                    u = clamp;
+                    count += 1;
+                } else if (u < -clamp) {
+                    u = -clamp;
+                    count += 1;
+                }
+            }
+            e = expf(-gt);
+            den = 1.0f + e;
+            silu = gt / den;
+            val = silu * u;
+            if (weights)
+                val = val * weights[r];
+            v[c] = val;
+        }
+        for (g = 0; g < G; ++g) {
+            float sf = cast_group_fp4(v + (int64_t)g * group, group, flags,
+                                      codes + (int64_t)g * group);
+            store_scale(out_sf, flags, ld, G, r, g, sf);
+        }
+        pack_e2m1(codes, N, q + r * (N / 2));
+    }
+    free(v); free(codes);
+    if (clamp_count)
+        *clamp_count += count;
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Step 5: weighted combine ("CuTeDSL at Perplexity", combine kernel)         */
 /* ------------------------------------------------------------------------ */

@@ -183,3 +183,45 @@ def test_codes_use_the_inverse_of_the_stored_scale():
     q, sf = oracle.expand_cast_fp4(xb, _ident(1), group=32)
     codes = oracle.e2m1_unpack(q)
     assert codes[0, 0] == 7 and codes[0, 1] == 1
+
+
+# ---------------------------------------------------------------- SwiGLU -> FP4
+
+def _sx(M, N, seed, scale=2.0):
+    g = torch.Generator().manual_seed(seed)
+    return oracle.bf16_bits((torch.randn(M, 2 * N, generator=g) * scale).to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("group", [16, 32, 128])
+def test_swiglu_fp4_is_the_fp4_cast_of_the_swiglu_values(group):
+    """The FP4 SwiGLU equals the FP4 cast (pinned above) of the SwiGLU values
+    (pinned in the FP8 pins), fed as bf16-exact rows where possible: here the
+    values are checked group by group through the scale and code definitions."""
+    xb = _sx(6, 256, seed=group)
+    q, sf, cnt = oracle.swiglu_cast_fp4(xb, group=group)
+    assert cnt == 0
+    v = oracle.swiglu_values(xb).astype(np.float64)
+    codes = oracle.e2m1_unpack(q)
+    vals = np.array([oracle.e2m1_value(c) for c in range(16)])[codes]
+    G = 256 // group
+    floor_v = 6.0 * 2.0 ** -126
+    for r in range(6):
+        for g in range(G):
+            seg = slice(g * group, (g + 1) * group)
+            amax = np.abs(v[r, seg]).max()
+            assert sf[r, g] == np.float32(np.float32(max(amax, floor_v)) / np.float32(6.0))
+            assert np.abs(vals[r, seg]).max() == 6.0 or amax < floor_v
+    err = np.abs(vals * np.repeat(sf.astype(np.float64), group, axis=1) - v)
+    assert (err <= np.repeat(sf.astype(np.float64), group, axis=1) * 1.0 + 1e-30).all()
+
+
+def test_swiglu_fp4_clamp_weight_and_count_match_the_fp8_variant():
+    xb = _sx(8, 256, seed=3, scale=3.0)
+    w = np.linspace(0.1, 1.0, 8).astype(np.float32)
+    _, _, c8 = oracle.swiglu_cast_fp8_ex(xb, clamp=2.0, weights=w)
+    _, _, c4 = oracle.swiglu_cast_fp4(xb, group=32, clamp=2.0, weights=w)
+    assert c4 == c8 > 0
+    # a weight of 2 doubles every scale and leaves the codes
+    q1, s1, _ = oracle.swiglu_cast_fp4(xb, group=32, clamp=2.0, weights=np.ones(8, np.float32))
+    q2, s2, _ = oracle.swiglu_cast_fp4(xb, group=32, clamp=2.0, weights=np.full(8, 2, np.float32))
+    assert np.array_equal(q1, q2) and np.array_equal(s2, 2 * s1)
