@@ -742,6 +742,21 @@ def cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak):
         "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
         "clamped_inputs_per_pass": int(cnt.item()) // (iters + 2),
         "timing": "after a 512 MB L2 flush, median"}
+    q5 = torch.empty(M, N // 2, dtype=torch.uint8, device=dev)
+    sf5 = torch.empty(M, N // 32, dtype=torch.float32, device=dev)
+
+    def sw4():
+        chk(L.swiglu_cast_fp4(hx.data_ptr(), M, N, q5.data_ptr(), sf5.data_ptr(), 0, 0, 0, 0.0,
+                              None, None, 32, sp), "swiglu_fp4")
+
+    ms = timed(sw4, iters)
+    b = M * 2 * N * 2 + M * (N // 2) + M * (N // 32) * 4
+    gbs = b / (ms * 1e-3) / 1e9
+    res["swiglu_64k_fp4_group32"] = {
+        "op": "swiglu_cast_fp4 (E2M1, 32-channel groups, f32 scales)",
+        "ms": round(ms, 4), "rows_per_s": round(M / (ms * 1e-3), 1), "algorithmic_bytes": b,
+        "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+        "timing": "after a 512 MB L2 flush, median"}
     if L.moe_get_device_status(sp, None) != 0:
         raise RuntimeError("device error in the cast-option workloads")
     return res

@@ -367,6 +367,20 @@ moe_status_t swiglu_cast_fp8_ex(const void *x, int64_t num_rows, int32_t n, uint
                                 uint64_t *clamp_count, int32_t group, void *stream);
 
 /*
+ * swiglu_cast_fp4 -- swiglu_cast_fp8_ex with the FP4 E2M1 output of
+ * moe_expand_cast_fp4: the same SwiGLU values (clamp, weight, clamp count),
+ * cast per group of `group` channels (16, 32, 64 or 128) with scale
+ * max(amax, 6 * 2^-126) / 6 (or its power-of-two round-up), codes packed two
+ * per byte, element 2i in the low nibble: out [M][N/2] u8; scales as
+ * swiglu_cast_fp8_ex with G = N / group.
+ * Requires N % group == 0, N % 32 == 0, x and out 16-byte aligned.
+ */
+moe_status_t swiglu_cast_fp4(const void *x, int64_t num_rows, int32_t n, uint8_t *out,
+                             void *out_sf, uint32_t sf_flags, int64_t sf_ld, int32_t has_clamp,
+                             float clamp, const float *weights, uint64_t *clamp_count,
+                             int32_t group, void *stream);
+
+/*
  * moe_combine -- [PX] combine: "accumulate in registers using the token
  * positions, then write the final tokens".  For every token t:
  *   out[t, c] = sum_{j=0..k-1, pos[t,j] >= 0} topk_weights[t,j] * y[pos[t,j], c]

@@ -324,6 +324,33 @@ moe_status_t moe_expand_cast_fp4(const void* x, int64_t num_tokens, int32_t hidd
   return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }
 
+moe_status_t swiglu_cast_fp4(const void* x, int64_t num_rows, int32_t n, uint8_t* out,
+                             void* out_sf, uint32_t sf_flags, int64_t sf_ld, int32_t has_clamp,
+                             float clamp, const float* weights, uint64_t* clamp_count,
+                             int32_t group, void* stream) {
+  if (group != 16 && group != 32 && group != 64 && group != 128) return MOE_ERR_UNSUPPORTED;
+  if (num_rows < 0 || n < 32 || n % 32 != 0 || n % group != 0) return MOE_ERR_INVALID_ARG;
+  if (num_rows * (n / 16) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (has_clamp && !(clamp >= 0.0f && clamp <= 3.0e38f)) return MOE_ERR_INVALID_ARG;
+  if (!sf_opts_ok(sf_flags, sf_ld, num_rows, out_sf)) return MOE_ERR_INVALID_ARG;
+  if (num_rows == 0) return MOE_OK;
+  if (!x || !out || !out_sf) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(weights, 4) || !aligned(clamp_count, 8))
+    return MOE_ERR_INVALID_ARG;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  SwigluExt ext;
+  ext.has_clamp = has_clamp ? 1 : 0;
+  ext.clamp = clamp;
+  ext.weights = weights;
+  ext.clamp_count = reinterpret_cast<unsigned long long*>(clamp_count);
+  ext.sf.flags = (int)sf_flags;
+  ext.sf.ld = sf_ld;
+  cudaError_t e = launch_swiglu_cast_fp4(c, x, num_rows, n, out, out_sf, ext, group);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
 moe_status_t swiglu_cast_fp8_ex(const void* x, int64_t num_rows, int32_t n, uint8_t* out,
                                 void* out_sf, uint32_t sf_flags, int64_t sf_ld, int32_t has_clamp,
                                 float clamp, const float* weights, uint64_t* clamp_count,

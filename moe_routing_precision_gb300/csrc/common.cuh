@@ -56,6 +56,10 @@ __device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
                : "memory");
 }
 
+__device__ __forceinline__ void st_stream_v2(void* p, uint2 v) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
 __device__ __forceinline__ void st_stream_f32(float* p, float v) {
   asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
@@ -175,6 +179,59 @@ __device__ __forceinline__ uint4 quant16_bf16(const uint4& a, const uint4& b, fl
            (e4m3x2(__fmul_rn(bf16_lo(w1), inv), __fmul_rn(bf16_hi(w1), inv)) << 16);
   }
   return make_uint4(c[0], c[1], c[2], c[3]);
+}
+
+// ---------------------------------------------------------------- FP4 E2M1
+// TileKernels article, 3.1: float4_e2m1fn's clamp_min_value is max_value *
+// 2^-126 with max_value = 6.
+// clamp_min_value of float4_e2m1fn: 6 * 2^-126 = 1.5 * 2^-124.
+__device__ __forceinline__ float fp4_floor() { return __uint_as_float(0x01C00000u); }
+
+__device__ __forceinline__ float fp4_scale(float amax, int flags) {
+  const float s = __fdiv_rn(fmaxf(amax, fp4_floor()), 6.0f);
+  return (flags & (MOE_SF_POW2 | MOE_SF_UE8M0)) ? round_pow2_up(s) : s;
+}
+
+// Two f32 values -> one byte of two E2M1 codes (round to nearest even,
+// saturate to +-6), `lo` in the low nibble: the hardware conversion
+// cvt.rn.satfinite.e2m1x2.f32, whose first source goes to the high nibble.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;\n}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 16 f32 values times `inv` -> 8 bytes of packed E2M1 codes.
+__device__ __forceinline__ uint2 quant16_e2m1(const float (&v)[16], float inv) {
+  uint32_t c[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t byte = e2m1x2(__fmul_rn(v[2 * i], inv), __fmul_rn(v[2 * i + 1], inv));
+    c[i >> 2] |= byte << (8 * (i & 3));
+  }
+  return make_uint2(c[0], c[1]);
+}
+
+// 16 bf16 values times `inv` -> 8 bytes of packed E2M1 codes.
+__device__ __forceinline__ uint2 quant16_bf16_e2m1(const uint4& a, const uint4& b, float inv) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t c[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t byte = e2m1x2(__fmul_rn(bf16_lo(w[i]), inv), __fmul_rn(bf16_hi(w[i]), inv));
+    c[i >> 2] |= byte << (8 * (i & 3));
+  }
+  return make_uint2(c[0], c[1]);
+}
+
+// Max over the L lanes of an aligned L-lane subgroup.
+template <int L>
+__device__ __forceinline__ float maxL(float m) {
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  return m;
 }
 
 // Max over the 8 lanes of an aligned 8-lane subgroup.
@@ -319,6 +376,8 @@ struct SwigluExt {
   unsigned long long* clamp_count = nullptr;
   SfOut sf;
 };
+cudaError_t launch_swiglu_cast_fp4(const LaunchCtx& c, const void* x, int64_t M, int N,
+                                   uint8_t* out, void* out_sf, const SwigluExt& ext, int group);
 cudaError_t launch_swiglu_cast_ex(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
                                   void* out_sf, const SwigluExt& ext);
 cudaError_t launch_combine(const LaunchCtx& c, const void* y, const float* w, const int32_t* pos,

@@ -40,13 +40,59 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return r;
 }
 
-// EXT: the variants of the TileKernels article, section 3.3 (clamp: gate
-// min(g, c), up clamped to [-c, c]; per-row top-k weight multiplied after
-// silu(g) * u; clamp counting) and the scale options.  The plain instance
-// (EXT = false) compiles none of it.  The clamp count is kept per thread over
-// the whole grid-stride loop and added with one atomic per warp.  The register
-// caps keep 5 (EXT) or 6 CTAs of 256 threads resident per SM without spills:
-// each warp's loop is latency-bound, so resident warps set the bandwidth.
+// The lane's 16 SwiGLU values of one (row, channel slice): the loaded gate and
+// up words, the EXT variants of the TileKernels article, section 3.3 (clamp:
+// gate min(g, c), up clamped to [-c, c]; the per-row top-k weight multiplied
+// after silu(g) * u; clamp counting into `clamped`), then the activation.
+// Every lane of the warp must call it (the clamp's fast-path vote).
+template <bool EXT>
+__device__ __forceinline__ void lane_values(const uint4& ga, const uint4& gb, const uint4& ua,
+                                            const uint4& ub, bool active, float wr,
+                                            const SwigluExt& ext, unsigned& clamped,
+                                            float (&v)[16]) {
+  float gv[16], uv[16];
+  unpack16(ga, gb, gv);
+  unpack16(ua, ub, uv);
+  if (EXT && ext.has_clamp) {
+    // Fast path: the clamp changes nothing unless some gate value or |up|
+    // value of the warp exceeds c (max over 16 values: two min/max per
+    // element, against seven for clamping and counting them all).
+    const float c = ext.clamp;
+    float mg = gv[0], mu = fabsf(uv[0]);
+#pragma unroll
+    for (int i = 1; i < 16; ++i) {
+      mg = fmaxf(mg, gv[i]);
+      mu = fmaxf(mu, fabsf(uv[i]));
+    }
+    if (__any_sync(0xFFFFFFFFu, active && (mg > c || mu > c))) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (active) clamped += (gv[i] > c) + (fabsf(uv[i]) > c);
+        gv[i] = min_nan(gv[i], c);  // NaN stays NaN, as min written as a compare
+        uv[i] = max_nan(min_nan(uv[i], c), -c);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = swiglu(gv[i], uv[i]);
+  if (EXT && ext.weights != nullptr) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], wr);
+  }
+}
+
+// One atomic per warp adds the warp's clamp count.
+__device__ __forceinline__ void add_clamp_count(const SwigluExt& ext, unsigned clamped, int lane) {
+  if (ext.clamp_count != nullptr) {
+    const unsigned total = __reduce_add_sync(0xFFFFFFFFu, clamped);
+    if (lane == 0 && total) atomicAdd(ext.clamp_count, (unsigned long long)total);
+  }
+}
+
+// E4M3 output.  EXT = false compiles none of the variants.  The clamp count
+// is kept per thread over the whole grid-stride loop.  The register caps keep
+// 5 (EXT) or 6 CTAs of 256 threads resident per SM without spills: each
+// warp's loop is latency-bound, so resident warps set the bandwidth.
 template <bool EXT>
 __global__ void __launch_bounds__(kThreads, EXT ? 5 : 6)
     swiglu_cast_kernel(const uint16_t* __restrict__ x, uint32_t units, int N,
@@ -77,35 +123,8 @@ __global__ void __launch_bounds__(kThreads, EXT ? 5 : 6)
       // issued with the row loads so that its latency overlaps theirs
       if (EXT && ext.weights != nullptr) wr = __ldg(ext.weights + r);
     }
-    float gv[16], uv[16], v[16];
-    unpack16(ga, gb, gv);
-    unpack16(ua, ub, uv);
-    if (EXT && ext.has_clamp) {
-      // Fast path: the clamp changes nothing unless some gate value or |up|
-      // value of the warp exceeds c (max over 16 values: two min/max per
-      // element, against seven for clamping and counting them all).
-      const float c = ext.clamp;
-      float mg = gv[0], mu = fabsf(uv[0]);
-#pragma unroll
-      for (int i = 1; i < 16; ++i) {
-        mg = fmaxf(mg, gv[i]);
-        mu = fmaxf(mu, fabsf(uv[i]));
-      }
-      if (__any_sync(0xFFFFFFFFu, active && (mg > c || mu > c))) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (active) clamped += (gv[i] > c) + (fabsf(uv[i]) > c);
-          gv[i] = min_nan(gv[i], c);  // NaN stays NaN, as min written as a compare
-          uv[i] = max_nan(min_nan(uv[i], c), -c);
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = swiglu(gv[i], uv[i]);
-    if (EXT && ext.weights != nullptr) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], wr);
-    }
+    float v[16];
+    lane_values<EXT>(ga, gb, ua, ub, active, wr, ext, clamped, v);
     const float amax = max8(absmax16(v));
     const float sf = EXT ? group_scale_opts(amax, ext.sf.flags) : group_scale(amax);
     const float inv = __fdiv_rn(1.0f, sf);
@@ -120,10 +139,59 @@ __global__ void __launch_bounds__(kThreads, EXT ? 5 : 6)
       }
     }
   }
-  if (EXT && ext.clamp_count != nullptr) {
-    const unsigned total = __reduce_add_sync(0xFFFFFFFFu, clamped);
-    if (lane == 0 && total) atomicAdd(ext.clamp_count, (unsigned long long)total);
+  if (EXT) add_clamp_count(ext, clamped, lane);
+}
+
+// FP4 E2M1 output (TileKernels article, 3.1's float4_e2m1fn: max 6,
+// clamp_min 6 * 2^-126): groups of 16 L channels, L lanes per group, 32 / L
+// groups per warp tile; 8 bytes of packed codes per lane.
+template <int L>
+__global__ void __launch_bounds__(kThreads, 5)
+    swiglu_cast_fp4_kernel(const uint16_t* __restrict__ x, uint32_t units, int N,
+                           uint8_t* __restrict__ out, float* __restrict__ out_sf, FastDiv fdG,
+                           SwigluExt ext) {
+  pdl_enter();
+  constexpr int U = 32 / L;  // groups per warp tile
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / L;
+  const int lg = lane % L;
+  const int G = N / (16 * L);
+  const uint32_t tiles = (units + U - 1) / U;
+  const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
+  unsigned clamped = 0;
+  for (uint32_t tile = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; tile < tiles; tile += warps) {
+    const uint32_t u = tile * U + sub;
+    const bool active = u < units;
+    const uint32_t r = active ? fdG.div(u) : 0;
+    const int g = active ? (int)(u - r * G) : 0;
+    const uint16_t* gate = x + (int64_t)r * 2 * N + g * 16 * L + lg * 16;
+    const uint16_t* up = gate + N;
+    uint4 ga = make_uint4(0, 0, 0, 0), gb = ga, ua = ga, ub = ga;
+    float wr = 0.0f;
+    if (active) {
+      ga = ld_stream_v4(gate);
+      gb = ld_stream_v4(gate + 8);
+      ua = ld_stream_v4(up);
+      ub = ld_stream_v4(up + 8);
+      if (ext.weights != nullptr) wr = __ldg(ext.weights + r);
+    }
+    float v[16];
+    lane_values<true>(ga, gb, ua, ub, active, wr, ext, clamped, v);
+    const float amax = maxL<L>(absmax16(v));
+    const float sf = fp4_scale(amax, ext.sf.flags);
+    const float inv = __fdiv_rn(1.0f, sf);
+    const uint2 q = quant16_e2m1(v, inv);
+    if (active) {
+      st_stream_v2(out + (int64_t)r * (N >> 1) + g * 8 * L + lg * 8, q);
+      if (lg == 0) {
+        if (ext.sf.flags != 0)
+          store_sf_opts(out_sf, ext.sf.flags, ext.sf.ld, G, r, g, sf);
+        else
+          st_stream_f32(out_sf + (int64_t)r * G + g, sf);
+      }
+    }
   }
+  add_clamp_count(ext, clamped, lane);
 }
 
 template <bool EXT>
@@ -144,7 +212,38 @@ cudaError_t launch_t(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_
                     ext);
 }
 
+template <int L>
+cudaError_t launch_fp4(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
+                       float* out_sf, const SwigluExt& ext) {
+  constexpr int U = 32 / L;
+  const int G = N / (16 * L);
+  const uint32_t units = (uint32_t)(M * G);  // < 2^31, checked by the caller
+  const uint32_t tiles = (units + U - 1) / U;
+  const int64_t need = ((int64_t)tiles + (kThreads / 32) - 1) / (kThreads / 32);
+  int per_sm = 0;
+  cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, swiglu_cast_fp4_kernel<L>,
+                                                                 kThreads, 0);
+  if (st != cudaSuccess) return st;
+  const int64_t cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
+  const int blocks = (int)(need < cap ? need : cap);
+  return launch_pdl(swiglu_cast_fp4_kernel<L>, blocks, kThreads, 0, c.stream,
+                    static_cast<const uint16_t*>(x), units, N, out, out_sf, FastDiv((uint32_t)G),
+                    ext);
+}
+
 }  // namespace
+
+cudaError_t launch_swiglu_cast_fp4(const LaunchCtx& c, const void* x, int64_t M, int N,
+                                   uint8_t* out, void* out_sf, const SwigluExt& ext, int group) {
+  float* sf = static_cast<float*>(out_sf);
+  switch (group) {
+    case 16: return launch_fp4<1>(c, x, M, N, out, sf, ext);
+    case 32: return launch_fp4<2>(c, x, M, N, out, sf, ext);
+    case 64: return launch_fp4<4>(c, x, M, N, out, sf, ext);
+    case 128: return launch_fp4<8>(c, x, M, N, out, sf, ext);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_swiglu_cast(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
                                float* out_sf) {

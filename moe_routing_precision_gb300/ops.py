@@ -47,6 +47,8 @@ SIGNATURES = {
                                            ctypes.c_uint32, _i64, _P, ctypes.c_size_t, _i32, _P]),
     "moe_expand_cast_fp4_workspace_bytes": (ctypes.c_size_t, [_i64, _i32, _i32,
                                                               ctypes.c_uint32]),
+    "swiglu_cast_fp4": (ctypes.c_int, [_P, _i64, _i32, _P, _P, ctypes.c_uint32, _i64, _i32,
+                                       ctypes.c_float, _P, _P, _i32, _P]),
     "moe_route_expand_cast_fp8": (ctypes.c_int, [_P, _i64, _i32, _i32, _P, _i32, _P, _P, _P, _P,
                                                  _P, _P, _P, _P, _P, ctypes.c_size_t, _i32, _i32,
                                                  _P]),
@@ -353,6 +355,31 @@ def expand_cast_fp4(x: torch.Tensor, pos: torch.Tensor, num_rows: int | None = N
     return q, out_sf
 
 
+def swiglu_cast_fp4(x: torch.Tensor, *, group: int = 32, clamp: float | None = None, weights=None,
+                    clamp_count=None, sf_flags: int = 0, sf_ld: int | None = None, out=None,
+                    out_sf=None, stream=None):
+    """SwiGLU (optional clamp, per-row weight, clamp counter) then the
+    per-group FP4 E2M1 cast -> (q [M, N/2] packed uint8, scales)."""
+    _dev(x, "x", torch.bfloat16)
+    M, N2 = x.shape
+    N = N2 // 2
+    if weights is not None:
+        _dev(weights, "weights", torch.float32, (M,))
+    if clamp_count is not None:
+        _dev(clamp_count, "clamp_count", torch.int64, (1,))
+    if sf_ld is None and (sf_flags & SF_COLMAJOR):
+        sf_ld = (M + 3) // 4 * 4
+    q = out if out is not None else _empty((M, N // 2), torch.uint8, x)
+    _dev(q, "out", torch.uint8, (M, N // 2))
+    if out_sf is None:
+        out_sf, sf_ld = sf_empty(M, N // group, sf_flags, sf_ld, x)
+    rc = lib().swiglu_cast_fp4(_ptr(x), M, N, _ptr(q), _ptr(out_sf), sf_flags, int(sf_ld or M),
+                               int(clamp is not None), float(clamp or 0.0), _ptr(weights),
+                               _ptr(clamp_count), group, _stream(stream))
+    _check(rc, "swiglu_cast_fp4")
+    return q, out_sf
+
+
 def swiglu_cast_fp8_ex(x: torch.Tensor, *, clamp: float | None = None, weights=None,
                        clamp_count=None, sf_flags: int = 0, sf_ld: int | None = None, out=None,
                        out_sf=None, stream=None):
@@ -466,6 +493,6 @@ def launch_count() -> int:
 __all__ = ["lib", "MoeError", "topk_gate", "route_map", "route_map_workspace_bytes",
            "route_map_aligned", "expand_cast_fp8_padded", "expand_cast_fp8_ex",
            "expand_cast_fp8_ex_workspace_bytes", "swiglu_cast_fp8_ex", "sf_empty",
-           "route_expand_cast_fp8", "route_expand_cast_workspace", "debug_set", "expand_cast_fp4",
+           "route_expand_cast_fp8", "route_expand_cast_workspace", "debug_set", "expand_cast_fp4", "swiglu_cast_fp4",
            "expand_cast_fp8", "swiglu_cast_fp8", "combine", "peak_copy", "device_status",
            "launch_count", "SIGNATURES"]

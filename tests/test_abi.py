@@ -237,3 +237,16 @@ def test_fp4_entry_point_rejects_bad_arguments(L):
     assert L.moe_expand_cast_fp4_workspace_bytes(1000, 7168, 32, 1) == (1000 * 224 * 4 + 255) // 256 * 256
     assert f(*args(flags=1, ld=8, ws=FAKE, wsb=need - 1)) == INVALID
     assert L.moe_kernel_launch_count() == 0
+
+
+def test_swiglu_fp4_rejects_bad_arguments(L):
+    f = L.swiglu_cast_fp4
+    args = lambda n=512, group=32, flags=0, ld=0, x=FAKE: (x, 4, n, FAKE, FAKE, flags, ld, 0, 0.0,
+                                                          None, None, group, None)
+    assert f(*args(group=8)) == UNSUPPORTED
+    assert f(*args(n=496)) == INVALID
+    assert f(*args(n=288, group=128)) == INVALID
+    assert f(*args(flags=4)) == INVALID
+    assert f(*args(x=FAKE + 8)) == INVALID
+    assert f(None, 0, 512, None, None, 0, 0, 0, 0.0, None, None, 32, None) == 0
+    assert L.moe_kernel_launch_count() == 0

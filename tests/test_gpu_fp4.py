@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from moe_routing_precision_gb300 import ops, workloads
-from tests.parity_util import assert_equal
+from tests.parity_util import assert_equal, check_swiglu_opts, fp4_ordinal
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -165,3 +165,44 @@ def test_expand_fp4_skewed_size_sampled_rows():
         for j in range(w.k):
             r = pos_np[i, j]
             assert np.array_equal(np_(q[r]), o_q[i]) and np.array_equal(np_(sf[r]), o_sf[i])
+
+
+# ---------------------------------------------------------------- SwiGLU -> FP4
+
+@pytest.mark.parametrize("group", [16, 32, 64, 128])
+@pytest.mark.parametrize("flags", [0, 1, 2, 7])
+@pytest.mark.parametrize("variant", ["plain", "clamp_weight"])
+@pytest.mark.parametrize("M,N", [(1, 128), (7, 384), (100, 2048), (1000, 256)])
+def test_swiglu_fp4_parity(group, flags, variant, M, N):
+    if N % group:
+        pytest.skip("N not a multiple of the group")
+    g = torch.Generator().manual_seed(M + N + group + flags)
+    x = (torch.randn(M, 2 * N, generator=g) * 2.0).to(torch.bfloat16)
+    clamp = 1.0 if variant == "clamp_weight" else None
+    w = torch.rand(M, generator=g) if variant == "clamp_weight" else None
+    ld = (M + 3) // 4 * 4 + 8 if flags & ops.SF_COLMAJOR else None
+    sf, ld = _sentinel_sf(M, N // group, flags, ld)
+    cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
+    q, _ = ops.swiglu_cast_fp4(x.to(DEV), group=group, clamp=clamp,
+                               weights=None if w is None else w.to(DEV), clamp_count=cnt,
+                               sf_flags=flags, sf_ld=ld, out_sf=sf)
+    xb = oracle.bf16_bits(x)
+    wn = None if w is None else w.numpy()
+    o_q, o_sf, o_cnt = oracle.swiglu_cast_fp4(xb, group=group, clamp=clamp, weights=wn,
+                                              flags=flags, ld=ld)
+    _, o_plain, _ = oracle.swiglu_cast_fp4(xb, group=group, clamp=clamp, weights=wn)
+    check_swiglu_opts(np_(q), np_(sf), o_q, o_sf, o_plain, flags, M, ordinal=fp4_ordinal)
+    assert int(cnt.item()) == o_cnt
+    assert ops.device_status() == 0
+
+
+def test_swiglu_fp4_full_size_sampled_rows():
+    """swiglu_64k (65536 rows x 2x2048), group 32: 2000 sampled rows."""
+    w = workloads.WORKLOADS["swiglu_64k"]
+    hx = workloads.make_inputs(w, seed=0, device=DEV)["swiglu_x"]
+    q, sf = ops.swiglu_cast_fp4(hx, group=32)
+    assert ops.device_status() == 0
+    rows = np.sort(np.random.default_rng(2).choice(w.M, 2000, replace=False))
+    xs = hx[torch.from_numpy(rows).to(DEV)].cpu()
+    o_q, o_sf, _ = oracle.swiglu_cast_fp4(oracle.bf16_bits(xs), group=32)
+    check_swiglu_opts(np_(q)[rows], np_(sf)[rows], o_q, o_sf, o_sf, 0, 2000, ordinal=fp4_ordinal)
