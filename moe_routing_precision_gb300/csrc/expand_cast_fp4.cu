@@ -25,6 +25,9 @@ namespace {
 // slot) 82 %; a second token of register prefetch did not help.
 constexpr int kFp4Buffers = 4;
 constexpr int kFp4CtasPerSm = 2;
+// Tokens per iteration: 2 (one barrier and one copy group per two tokens) was
+// measured at 86 % of peak at prefill size against 88 % for 1.
+constexpr int kFp4TokensPerIter = 1;
 
 __device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
@@ -34,91 +37,117 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t byt
 
 // L = lanes per group (group = 16 L channels).  sf_bulk: plain row-major f32
 // scales whose rows (4G bytes) are 16-byte multiples go out with the codes.
-template <int L, int NBUF>
-__global__ void __launch_bounds__(1024) expand_cast_fp4_kernel(
+// TPI tokens per iteration (adjacent tokens 2p, 2p + 1 for TPI = 2): one
+// barrier and one copy group per TPI tokens; buffer b holds TPI token slots.
+template <int L, int NBUF, int TPI>
+__global__ void __launch_bounds__(TPI == 1 ? 1024 : 448, TPI == 1 ? 1 : 2) expand_cast_fp4_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
     int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf,
     const int32_t* __restrict__ zsrc, SfOut sfo, int sf_bulk, unsigned* err) {
   static_assert(NBUF >= 2, "the buffer-reuse wait keeps NBUF - 2 copy groups in flight");
   extern __shared__ __align__(128) uint8_t s_buf[];
   pdl_enter();
-  const int P = H >> 4;  // threads per token
-  const int G = P / L;   // groups per token
-  const int HB = H >> 1; // code bytes per row
+  const int P = H >> 4;   // threads per token
+  const int G = P / L;    // groups per token
+  const int HB = H >> 1;  // code bytes per row
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const bool act = tid < P;
   const int g = tid / L;
   const bool lead = (tid % L) == 0;
-  const uint32_t stride = (uint32_t)((HB + 4 * G + 127) / 128 * 128);  // bytes per buffer
+  const uint32_t stride = (uint32_t)((HB + 4 * G + 127) / 128 * 128);  // bytes per token slot
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(s_buf);
+  int32_t* spos_all = reinterpret_cast<int32_t*>(s_buf + (size_t)NBUF * TPI * stride);
   bool bad = false;
-  int64_t t = blockIdx.x;
-  uint4 a = make_uint4(0, 0, 0, 0), b = a;
-  int32_t pnext = -1;  // warp 0: lane j holds pos[t, j] (j < k <= 32)
-  if (t < T) {
-    if (act) {
-      const uint16_t* src = x + t * H + tid * 16;
-      a = ld_stream_v4(src);
-      b = ld_stream_v4(src + 8);
-    }
-    if (tid < 32 && lane < k) pnext = __ldg(pos + t * k + lane);
-  }
-  int it = 0;
-  for (; t < T; t += gridDim.x, ++it) {
-    const uint4 ca = a, cb = b;
-    const int32_t pcur = pnext;
-    const int64_t tn = t + gridDim.x;
-    if (tn < T) {  // the next token's loads stay in flight during this one
-      if (act) {
-        const uint16_t* src = x + tn * H + tid * 16;
-        a = ld_stream_v4(src);
-        b = ld_stream_v4(src + 8);
+  const int64_t nit = (T + TPI - 1) / TPI;  // token groups
+  uint4 a[TPI], b[TPI];
+  int32_t pn[TPI];  // warp 0: lane j holds pos[t, j] (j < k <= 32)
+  auto load = [&](int64_t p) {
+#pragma unroll
+    for (int i = 0; i < TPI; ++i) {
+      const int64_t t = p * TPI + i;
+      a[i] = make_uint4(0, 0, 0, 0);
+      b[i] = a[i];
+      pn[i] = -1;
+      if (t < T) {
+        if (act) {
+          const uint16_t* src = x + t * H + tid * 16;
+          a[i] = ld_stream_v4(src);
+          b[i] = ld_stream_v4(src + 8);
+        }
+        if (tid < 32 && lane < k) pn[i] = __ldg(pos + t * k + lane);
       }
-      if (tid < 32) pnext = (lane < k) ? __ldg(pos + tn * k + lane) : -1;
     }
-    const float amax = maxL<L>(absmax16_bf16(ca, cb));
-    const float sf = fp4_scale(amax, sfo.flags);
-    const float inv = __fdiv_rn(1.0f, sf);
-    const uint2 q = quant16_bf16_e2m1(ca, cb, inv);
+  };
+  int64_t p = blockIdx.x;
+  if (p < nit) load(p);
+  int it = 0;
+  for (; p < nit; p += gridDim.x, ++it) {
+    uint4 ca[TPI], cb[TPI];
+    int32_t pc[TPI];
+#pragma unroll
+    for (int i = 0; i < TPI; ++i) {
+      ca[i] = a[i];
+      cb[i] = b[i];
+      pc[i] = pn[i];
+    }
+    if (p + gridDim.x < nit) load(p + gridDim.x);  // in flight during this group
     const int buf = it % NBUF;
-    uint8_t* sq = s_buf + (size_t)buf * stride;
-    int32_t* spos = reinterpret_cast<int32_t*>(s_buf + (size_t)NBUF * stride) + buf * 32;
-    if (act) {
-      *reinterpret_cast<uint2*>(sq + tid * 8) = q;
-      if (lead && sf_bulk) *reinterpret_cast<float*>(sq + HB + 4 * g) = sf;
+    float sfv[TPI];
+#pragma unroll
+    for (int i = 0; i < TPI; ++i) {
+      const bool valid = p * TPI + i < T;
+      const float amax = maxL<L>(absmax16_bf16(ca[i], cb[i]));
+      const float sf = fp4_scale(amax, sfo.flags);
+      const float inv = __fdiv_rn(1.0f, sf);
+      const uint2 q = quant16_bf16_e2m1(ca[i], cb[i], inv);
+      sfv[i] = sf;
+      uint8_t* sq = s_buf + (size_t)(buf * TPI + i) * stride;
+      if (act && valid) {
+        *reinterpret_cast<uint2*>(sq + tid * 8) = q;
+        if (lead && sf_bulk) *reinterpret_cast<float*>(sq + HB + 4 * g) = sf;
+      }
+      if (!sf_bulk && tid < 32) spos_all[(buf * TPI + i) * 32 + tid] = valid ? pc[i] : -1;
     }
-    if (!sf_bulk && tid < 32) spos[tid] = pcur;  // destinations, for every warp
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the copies
     __syncthreads();
     if (!sf_bulk && act && lead) {  // one lane per group stores its scale
-      if (sfo.stage != nullptr) {
-        store_stage(sfo.stage, sfo.flags, G, t, g, sf);
-      } else {
-        for (int j = 0; j < k; ++j) {
-          const int32_t r = spos[j];
-          if (r >= 0 && r < R) store_sf_opts(out_sf, sfo.flags, sfo.ld, G, r, g, sf);
+#pragma unroll
+      for (int i = 0; i < TPI; ++i) {
+        const int64_t t = p * TPI + i;
+        if (t >= T) continue;
+        if (sfo.stage != nullptr) {
+          store_stage(sfo.stage, sfo.flags, G, t, g, sfv[i]);
+        } else {
+          const int32_t* spos = spos_all + (buf * TPI + i) * 32;
+          for (int j = 0; j < k; ++j) {
+            const int32_t r = spos[j];
+            if (r >= 0 && r < R) store_sf_opts(out_sf, sfo.flags, sfo.ld, G, r, g, sfv[i]);
+          }
         }
       }
     }
     if (tid < 32) {
-      for (int j = 0; j < k; ++j) {
-        const int32_t r = __shfl_sync(0xFFFFFFFFu, pcur, j);
-        if (tid == 0 && r >= 0) {
-          if (r >= R) {
-            bad = true;
-          } else {
-            bulk_s2g(out + (int64_t)r * HB, sbase + buf * stride, (uint32_t)HB);
-            if (sf_bulk)
-              bulk_s2g(out_sf + (int64_t)r * G, sbase + buf * stride + HB, (uint32_t)(4 * G));
+#pragma unroll
+      for (int i = 0; i < TPI; ++i) {
+        const uint32_t slot = sbase + (uint32_t)(buf * TPI + i) * stride;
+        for (int j = 0; j < k; ++j) {
+          const int32_t r = __shfl_sync(0xFFFFFFFFu, pc[i], j);
+          if (tid == 0 && r >= 0) {
+            if (r >= R) {
+              bad = true;
+            } else {
+              bulk_s2g(out + (int64_t)r * HB, slot, (uint32_t)HB);
+              if (sf_bulk) bulk_s2g(out_sf + (int64_t)r * G, slot + HB, (uint32_t)(4 * G));
+            }
           }
         }
       }
       if (tid == 0) {
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        // buffer (it + 2) % NBUF is written two tokens from now, after the
-        // next token's barrier: its copies (NBUF - 2 groups back) must have
-        // read it by then.  One barrier per token instead of two.
+        // buffer (it + 2) % NBUF is written two groups from now, after the
+        // next group's barrier: its copies (NBUF - 2 groups back) must have
+        // read it by then.  One barrier per group of TPI tokens.
         asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(NBUF - 2) : "memory");
       }
     }
@@ -132,18 +161,18 @@ __global__ void __launch_bounds__(1024) expand_cast_fp4_kernel(
   if (bad) flag_error(err, MOE_DEVERR_POS_RANGE);
 }
 
-template <int L>
-cudaError_t launch_l(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
-                     const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
-                     const int32_t* zsrc, SfOut sfo) {
+template <int L, int TPI>
+cudaError_t launch_lt(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
+                      const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
+                      const int32_t* zsrc, SfOut sfo) {
   constexpr int NBUF = kFp4Buffers;
   const int P = H / 16;
   const int threads = (P + 31) / 32 * 32;
   const int G = P / L;
   const size_t stride = (size_t)(H / 2 + 4 * G + 127) / 128 * 128;
-  const size_t smem = stride * NBUF + sizeof(int32_t) * 32 * NBUF;
+  const size_t smem = (stride + sizeof(int32_t) * 32) * NBUF * TPI;
   if (smem > 48 * 1024) {
-    cudaError_t st = cudaFuncSetAttribute(expand_cast_fp4_kernel<L, NBUF>,
+    cudaError_t st = cudaFuncSetAttribute(expand_cast_fp4_kernel<L, NBUF, TPI>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (st != cudaSuccess) return st;
   }
@@ -152,10 +181,23 @@ cudaError_t launch_l(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                           ? 1
                           : 0;
   const int64_t cap = (int64_t)c.num_sms * kFp4CtasPerSm;
-  const int blocks = (int)(T < cap ? (T > 0 ? T : 1) : cap);  // >= 1: zero-fill with T = 0
-  return launch_pdl(expand_cast_fp4_kernel<L, NBUF>, blocks, threads, smem, c.stream,
+  const int64_t groups = (T + TPI - 1) / TPI;
+  const int blocks = (int)(groups < cap ? (groups > 0 ? groups : 1) : cap);  // >= 1: zero-fill
+  return launch_pdl(expand_cast_fp4_kernel<L, NBUF, TPI>, blocks, threads, smem, c.stream,
                     static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, zsrc, sfo,
                     sf_bulk, c.err);
+}
+
+// Two tokens per iteration where a token slice has at most 448 threads
+// (H <= 7168: two such CTAs per SM keep 72 registers a thread), else one.
+template <int L>
+cudaError_t launch_l(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
+                     const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
+                     const int32_t* zsrc, SfOut sfo) {
+  if constexpr (kFp4TokensPerIter == 2) {
+    if (H <= 7168) return launch_lt<L, 2>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
+  }
+  return launch_lt<L, 1>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
 }
 
 }  // namespace
