@@ -61,6 +61,10 @@ def algorithmic_bytes(T, E, k, H, N=SWIGLU_N, M=None):
     return b
 
 
+# GB300's nominal HBM3e bandwidth per GPU as NVIDIA states it (context for the
+# measured copy peak, which is what the fractions are taken against)
+NOMINAL_HBM_GBS = 7900.0
+
 KERNEL_OF_OP = {  # op -> (kernel name in ncu, source file), for E <= 256 and H <= 16384
     "topk_gate": ("topk_gate_sorted_kernel", "topk_gate.cu"),
     "expand_cast_fp8": ("expand_cast_bulk_kernel", "expand_cast.cu"),
@@ -352,6 +356,7 @@ def gpu_arm(args):
     breakdown["route_expand_cast"] = {
         "ms": round(rec_ms_mean, 4), "algorithmic_bytes": B["route_expand_cast"],
         "GB_s": round(rec_gbs, 1), "frac_of_peak": round(rec_gbs / peak, 4),
+        "frac_of_nominal": round(rec_gbs / NOMINAL_HBM_GBS, 4),
         "tokens_per_s": round(T * world / (rec_ms_mean * 1e-3), 1)}
     dom = max((n for n in ops_names if n in KERNEL_OF_OP and n in ran), key=lambda n: op_ms[n])
     dom_gbs = B[dom] / (op_ms[dom] * 1e-3) / 1e9
@@ -479,75 +484,79 @@ def extra_workloads(L, dev, stream, sp, chk, args):
                 ts.append(e0.elapsed_time(e1))
         return statistics.median(ts)
 
-    w = workloads.WORKLOADS["skewed_8k"]
-    inp = workloads.make_inputs(w, seed=0, device=dev)
-    s, x = inp["scores"], inp["x"]
-    T, E, k, H, R, G = w.T, w.E, w.k, w.H, w.R, w.G
-    i32 = dict(dtype=torch.int32, device=dev)
-    idx, wt = torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device=dev)
-    counts, offsets, pos, src = (torch.empty(E, **i32), torch.empty(E + 1, **i32),
-                                 torch.empty(T, k, **i32), torch.empty(R, **i32))
-    ws = torch.empty(max(1, ops.route_map_workspace_bytes(T, E, k)), dtype=torch.uint8, device=dev)
-    q = torch.empty(R, H, dtype=torch.uint8, device=dev)
-    sf = torch.empty(R, G, dtype=torch.float32, device=dev)
+    def skewed(name):
+        w = workloads.WORKLOADS[name]
+        inp = workloads.make_inputs(w, seed=0, device=dev)
+        s, x = inp["scores"], inp["x"]
+        T, E, k, H, R, G = w.T, w.E, w.k, w.H, w.R, w.G
+        i32 = dict(dtype=torch.int32, device=dev)
+        idx, wt = torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device=dev)
+        counts, offsets, pos, src = (torch.empty(E, **i32), torch.empty(E + 1, **i32),
+                                     torch.empty(T, k, **i32), torch.empty(R, **i32))
+        ws = torch.empty(max(1, ops.route_map_workspace_bytes(T, E, k)), dtype=torch.uint8, device=dev)
+        q = torch.empty(R, H, dtype=torch.uint8, device=dev)
+        sf = torch.empty(R, G, dtype=torch.float32, device=dev)
 
-    def rec():
-        chk(L.moe_topk_gate(s.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
-        chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
-                            pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
-        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
-                                  sf.data_ptr(), 128, sp), "expand")
+        def rec():
+            chk(L.moe_topk_gate(s.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
+            chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
+                                pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
+            chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
+                                      sf.data_ptr(), 128, sp), "expand")
 
-    def exp_only():
-        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
-                                  sf.data_ptr(), 128, sp), "expand")
+        def exp_only():
+            chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
+                                      sf.data_ptr(), 128, sp), "expand")
 
-    ms = timed(rec)
-    ms_e = timed(exp_only)
-    B = algorithmic_bytes(T, E, k, H)
-    gbs = B["route_expand_cast"] / (ms * 1e-3) / 1e9
-    gbs_e = B["expand_cast_fp8"] / (ms_e * 1e-3) / 1e9
-    # sustained: back-to-back batches over NSETS independent input sets (seeds
-    # 0..NSETS-1), so each batch's 125 MB of inputs was last touched NSETS-1
-    # batches (~1.8 GB of traffic) ago and is no longer in L2
-    nsets = 4
-    sets = [(s, x)] + [(d["scores"], d["x"]) for d in
-                       (workloads.make_inputs(w, seed=i, device=dev) for i in range(1, nsets))]
+        ms = timed(rec)
+        ms_e = timed(exp_only)
+        B = algorithmic_bytes(T, E, k, H)
+        gbs = B["route_expand_cast"] / (ms * 1e-3) / 1e9
+        gbs_e = B["expand_cast_fp8"] / (ms_e * 1e-3) / 1e9
+        # sustained: back-to-back batches over NSETS independent input sets (seeds
+        # 0..NSETS-1), so each batch's 125 MB of inputs was last touched NSETS-1
+        # batches (~1.8 GB of traffic) ago and is no longer in L2
+        nsets = 4
+        sets = [(s, x)] + [(d["scores"], d["x"]) for d in
+                           (workloads.make_inputs(w, seed=i, device=dev) for i in range(1, nsets))]
 
-    def rec_set(i):
-        si, xi = sets[i % nsets]
-        chk(L.moe_topk_gate(si.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
-        chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
-                            pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
-        chk(L.moe_expand_cast_fp8(xi.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
-                                  sf.data_ptr(), 128, sp), "expand")
+        def rec_set(i):
+            si, xi = sets[i % nsets]
+            chk(L.moe_topk_gate(si.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
+            chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
+                                pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
+            chk(L.moe_expand_cast_fp8(xi.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
+                                      sf.data_ptr(), 128, sp), "expand")
 
-    reps = max(8, 2 * iters)
-    for i in range(nsets):
-        rec_set(i)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(reps):
-        rec_set(i)
-    e1.record(stream)
-    e1.synchronize()
-    ms_s = e0.elapsed_time(e1) / reps
-    gbs_s = B["route_expand_cast"] / (ms_s * 1e-3) / 1e9
-    res["skewed_8k"] = {"op": "route+expand+cast",
-                        "single_shot": {"ms": round(ms, 4),
-                                        "routed_tokens_per_s": round(R / (ms * 1e-3), 1),
-                                        "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                                        "timing": "one batch after a 512 MB L2 flush, median"},
-                        "sustained": {"ms": round(ms_s, 4),
-                                      "routed_tokens_per_s": round(R / (ms_s * 1e-3), 1),
-                                      "GB_s": round(gbs_s, 1),
-                                      "frac_of_peak": round(gbs_s / peak, 4),
-                                      "timing": f"{reps} batches back to back over {nsets} input "
-                                                "sets (inputs not in L2), mean"},
-                        "expand_only_ms": round(ms_e, 4), "expand_only_GB_s": round(gbs_e, 1),
-                        "skew": workloads.skew_stats(counts.cpu())}
-    del inp, s, x, q, sf, sets
+        reps = max(8, 2 * iters)
+        for i in range(nsets):
+            rec_set(i)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            rec_set(i)
+        e1.record(stream)
+        e1.synchronize()
+        ms_s = e0.elapsed_time(e1) / reps
+        gbs_s = B["route_expand_cast"] / (ms_s * 1e-3) / 1e9
+        res[name] = {"op": "route+expand+cast",
+                            "single_shot": {"ms": round(ms, 4),
+                                            "routed_tokens_per_s": round(R / (ms * 1e-3), 1),
+                                            "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                                            "timing": "one batch after a 512 MB L2 flush, median"},
+                            "sustained": {"ms": round(ms_s, 4),
+                                          "routed_tokens_per_s": round(R / (ms_s * 1e-3), 1),
+                                          "GB_s": round(gbs_s, 1),
+                                          "frac_of_peak": round(gbs_s / peak, 4),
+                                          "timing": f"{reps} batches back to back over {nsets} input "
+                                                    "sets (inputs not in L2), mean"},
+                            "expand_only_ms": round(ms_e, 4), "expand_only_GB_s": round(gbs_e, 1),
+                            "skew": workloads.skew_stats(counts.cpu())}
+
+    skewed("skewed_8k")
+    torch.cuda.empty_cache()
+    skewed("skewed_8k_mild")
     w = workloads.WORKLOADS["swiglu_64k"]
     hx = workloads.make_inputs(w, seed=0, device=dev)["swiglu_x"]
     M, N = w.M, w.N
@@ -848,8 +857,31 @@ def cpu_baseline_leg(scores, x, k, E, tokens=16384, total=65536):
     oracle.expand_cast_fp8(xb, pos)
     dt = time.perf_counter() - t0
     return {"value": round(tokens * k / dt, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu": cpu_model(), "host_cores": os.cpu_count(),
             "sample": f"first {tokens} of {total} tokens of the benchmarked workload "
                       f"(topk_gate + route_map + expand_cast_fp8), {dt:.1f} s single-threaded"}
+
+
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, or the Arm
+    implementer/part codes), else the platform string."""
+    import platform
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        info = []
+    for key in ("model name", "Model name"):
+        for line in info:
+            if line.startswith(key):
+                return line.split(":", 1)[1].strip()
+    parts = {}
+    for line in info:
+        for key in ("CPU implementer", "CPU part"):
+            if line.startswith(key):
+                parts[key] = line.split(":", 1)[1].strip()
+    if parts:
+        return f"{platform.machine()} implementer {parts.get('CPU implementer')} part {parts.get('CPU part')}"
+    return platform.processor() or platform.machine()
 
 
 # ---------------------------------------------------------------- reference arm
@@ -894,6 +926,7 @@ def reference_arm(args):
                                f"{tokens} tokens per step", "T": tokens, "E": w.E, "k": w.k,
                    "H": w.H},
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "cpu": cpu_model(), "host_cores": os.cpu_count(),
                          "sample": f"{tokens} tokens per step (topk_gate + route_map + "
                                    f"expand_cast_fp8), single-threaded C"},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,

@@ -66,6 +66,10 @@ WORKLOADS = {
     "skewed_8k": Workload("skewed_8k", T=8192, E=256, k=8, H=7168, bias="zipf",
                           outlier_frac=0.01),
     "swiglu_64k": Workload("swiglu_64k", M=65536, N=2048),
+    # the skewed workload with the Zipf bias multiplier 0.4 instead of 2: about
+    # 10 % of the experts take half of the copies (a sensitivity variant)
+    "skewed_8k_mild": Workload("skewed_8k_mild", T=8192, E=256, k=8, H=7168, bias="zipf",
+                               zipf_mult=0.4, outlier_frac=0.01),
     "prefill_64k": Workload("prefill_64k", T=65536, E=256, k=8, H=7168, bias="uniform",
                             x_std=0.5),
 }
