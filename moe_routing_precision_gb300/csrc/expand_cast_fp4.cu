@@ -21,7 +21,7 @@ namespace moe {
 namespace {
 
 // Measured on GB300 (prefill-sized expand, H = 7168, group 32): two CTAs per
-// SM (both resident by registers) 86 % of peak, three (one waiting for a
+// SM (both resident by registers) 86-88 % of peak, three (one waiting for a
 // slot) 82 %; a second token of register prefetch did not help.
 constexpr int kFp4Buffers = 4;
 constexpr int kFp4CtasPerSm = 2;
