@@ -398,44 +398,66 @@ def gpu_arm(args):
 def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, src, ws, q, sf,
             T, E, k, H, R, chk, barrier, maxr):
     """route+expand+cast with the inputs copied from pinned host memory and
-    every output copied back to pinned host memory, all inside the timing."""
+    every output copied back to pinned host memory, all inside the timing.
+    Consecutive steps alternate between two streams, each with its own device
+    and host buffers, so one step's device-to-host copy overlaps the next
+    step's host-to-device copy and kernels (as a caller streaming batches
+    would run it); every step still makes all of its own copies."""
     import torch
     h_scores = torch.empty_like(scores, device="cpu").pin_memory()
     h_x = torch.empty_like(x, device="cpu").pin_memory()
     h_scores.copy_(scores)
     h_x.copy_(x)
-    outs = [idx, wt, counts, offsets, pos, src, q, sf]
-    h_outs = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    names = ["scores", "x", "idx", "wt", "counts", "offsets", "pos", "src", "ws", "q", "sf"]
+    slot0 = dict(zip(names, [scores, x, idx, wt, counts, offsets, pos, src, ws, q, sf]))
+    slots = [slot0, {n: torch.empty_like(t) for n, t in slot0.items()}]
+    out_names = ["idx", "wt", "counts", "offsets", "pos", "src", "q", "sf"]
+    h_outs = [[torch.empty_like(sl[n], device="cpu").pin_memory() for n in out_names]
+              for sl in slots]
+    streams = [torch.cuda.Stream(device=dev) for _ in slots]
     h2d = h_scores.numel() * 4 + h_x.numel() * 2
-    d2h = sum(t.numel() * t.element_size() for t in outs)
-    steps = max(3, min(args.steps, args.e2e_steps))
+    d2h = sum(slot0[n].numel() * slot0[n].element_size() for n in out_names)
+    steps = max(4, min(args.steps, args.e2e_steps))
 
-    def one():
-        scores.copy_(h_scores, non_blocking=True)
-        x.copy_(h_x, non_blocking=True)
-        chk(L.moe_topk_gate(scores.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
-        chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
-                            pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
-        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
-                                  sf.data_ptr(), 128, sp), "expand")
-        for h, d in zip(h_outs, outs):
-            h.copy_(d, non_blocking=True)
+    def one(i):
+        sl, st = slots[i % 2], streams[i % 2]
+        p = st.cuda_stream
+        with torch.cuda.stream(st):
+            sl["scores"].copy_(h_scores, non_blocking=True)
+            sl["x"].copy_(h_x, non_blocking=True)
+            chk(L.moe_topk_gate(sl["scores"].data_ptr(), T, E, k, sl["idx"].data_ptr(),
+                                sl["wt"].data_ptr(), 1, p), "topk")
+            chk(L.moe_route_map(sl["idx"].data_ptr(), T, E, k, sl["counts"].data_ptr(),
+                                sl["offsets"].data_ptr(), sl["pos"].data_ptr(), sl["src"].data_ptr(),
+                                sl["ws"].data_ptr(), sl["ws"].numel(), p), "route")
+            chk(L.moe_expand_cast_fp8(sl["x"].data_ptr(), T, H, k, sl["pos"].data_ptr(), R,
+                                      sl["q"].data_ptr(), sl["sf"].data_ptr(), 128, p), "expand")
+            for h, n in zip(h_outs[i % 2], out_names):
+                h.copy_(sl[n], non_blocking=True)
 
-    one()
+    one(0)
+    one(1)
     barrier()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(steps):
-        one()
+    for st in streams:
+        st.wait_event(a)
+    for i in range(steps):
+        one(i)
+    for st in streams:
+        ev = torch.cuda.Event()
+        ev.record(st)
+        stream.wait_event(ev)
     b.record(stream)
     barrier()
     ms = maxr(a.elapsed_time(b) / steps)
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    del slots, h_outs
     return {"value": round(R * world / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
             "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "path": "pinned host -> device, C ABI topk_gate/route_map/expand_cast_fp8, "
-                    "all outputs -> pinned host"}
+                    "all outputs -> pinned host; steps alternate between two streams"}
 
 
 def measure_peak_copy(L, dev, stream, sp):
