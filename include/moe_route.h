@@ -451,6 +451,19 @@ size_t moe_route_expand_cast_fp8_workspace_bytes(int64_t num_tokens, int32_t num
 moe_status_t moe_debug_set(int32_t key, int64_t value);
 
 /*
+ * moe_debug_cvt -- the device's value conversions on arbitrary f32 input, for
+ * tests: out[i] = the E4M3FN code (MOE_DEBUG_CVT_E4M3: round to nearest even,
+ * saturating at +-448, NaN -> NaN) or the E2M1 code in the low nibble
+ * (MOE_DEBUG_CVT_E2M1: round to nearest even, saturating at +-6) of in[i],
+ * exactly as the cast kernels convert x * (1 / scale).
+ *   in [n] f32, out [n] u8, both 16-byte aligned; n % 4 == 0.
+ */
+#define MOE_DEBUG_CVT_E4M3 0
+#define MOE_DEBUG_CVT_E2M1 1
+moe_status_t moe_debug_cvt(int32_t format, const float *in, uint8_t *out, int64_t n,
+                           void *stream);
+
+/*
  * moe_peak_copy -- a plain 16-byte vectorised device-to-device copy of
  * `bytes` bytes (a multiple of 16; both pointers 16-byte aligned), used to
  * measure the HBM bandwidth the kernels above are held against.

@@ -482,6 +482,19 @@ moe_status_t moe_debug_set(int32_t key, int64_t value) {
   return MOE_ERR_INVALID_ARG;
 }
 
+moe_status_t moe_debug_cvt(int32_t format, const float* in, uint8_t* out, int64_t n,
+                           void* stream) {
+  if (format != MOE_DEBUG_CVT_E4M3 && format != MOE_DEBUG_CVT_E2M1) return MOE_ERR_INVALID_ARG;
+  if (n < 0 || n % 4 != 0) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!in || !out || !aligned(in, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  cudaError_t e = launch_debug_cvt(c, format, in, out, n);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+
 moe_status_t moe_peak_copy(const void* src, void* dst, size_t bytes, void* stream) {
   if (bytes == 0) return MOE_OK;
   if (!src || !dst || bytes % 16 != 0 || !aligned(src, 16) || !aligned(dst, 16))

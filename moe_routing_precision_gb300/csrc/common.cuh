@@ -289,6 +289,10 @@ struct LaunchCtx {
   unsigned* err;  // device error word
 };
 
+// The device conversions on arbitrary f32 values, for tests (debug_cvt.cu).
+cudaError_t launch_debug_cvt(const LaunchCtx& c, int fmt, const float* in, uint8_t* out,
+                             int64_t n);
+
 // Fused decode path (decode_fused.cu) and its test hooks.
 extern std::atomic<int64_t> g_decode_timeout_ns;
 extern std::atomic<int> g_decode_skip_signal;

@@ -54,6 +54,7 @@ SIGNATURES = {
                                                  _P]),
     "moe_route_expand_cast_fp8_workspace_bytes": (ctypes.c_size_t, [_i64, _i32, _i32]),
     "moe_debug_set": (ctypes.c_int, [_i32, _i64]),
+    "moe_debug_cvt": (ctypes.c_int, [_i32, _P, _P, _i64, _P]),
     "swiglu_cast_fp8_ex": (ctypes.c_int, [_P, _i64, _i32, _P, _P, ctypes.c_uint32, _i64, _i32,
                                           ctypes.c_float, _P, _P, _i32, _P]),
     "moe_combine": (ctypes.c_int, [_P, _P, _P, _i64, _i32, _i32, _i64, _P, _i32, _P]),
@@ -283,6 +284,19 @@ def route_expand_cast_fp8(scores: torch.Tensor, x: torch.Tensor, k: int, *, mode
     return idx, w, counts, offsets, pos, src, q, sf
 
 
+CVT_E4M3, CVT_E2M1 = 0, 1
+
+
+def debug_cvt(values: torch.Tensor, fmt: int, out=None, stream=None) -> torch.Tensor:
+    """The device's f32 -> E4M3 / E2M1 conversion of every value (one code
+    per byte), as the cast kernels convert; for tests."""
+    _dev(values, "values", torch.float32)
+    out = out if out is not None else _empty(values.shape, torch.uint8, values)
+    _check(lib().moe_debug_cvt(fmt, _ptr(values), _ptr(out), values.numel(), _stream(stream)),
+           "moe_debug_cvt")
+    return out
+
+
 def debug_set(key: int, value: int) -> None:
     _check(lib().moe_debug_set(key, int(value)), "moe_debug_set")
 
@@ -493,6 +507,6 @@ def launch_count() -> int:
 __all__ = ["lib", "MoeError", "topk_gate", "route_map", "route_map_workspace_bytes",
            "route_map_aligned", "expand_cast_fp8_padded", "expand_cast_fp8_ex",
            "expand_cast_fp8_ex_workspace_bytes", "swiglu_cast_fp8_ex", "sf_empty",
-           "route_expand_cast_fp8", "route_expand_cast_workspace", "debug_set", "expand_cast_fp4", "swiglu_cast_fp4",
+           "route_expand_cast_fp8", "route_expand_cast_workspace", "debug_set", "debug_cvt", "expand_cast_fp4", "swiglu_cast_fp4",
            "expand_cast_fp8", "swiglu_cast_fp8", "combine", "peak_copy", "device_status",
            "launch_count", "SIGNATURES"]

@@ -250,3 +250,12 @@ def test_swiglu_fp4_rejects_bad_arguments(L):
     assert f(*args(x=FAKE + 8)) == INVALID
     assert f(None, 0, 512, None, None, 0, 0, 0, 0.0, None, None, 32, None) == 0
     assert L.moe_kernel_launch_count() == 0
+
+
+def test_debug_cvt_rejects_bad_arguments(L):
+    f = L.moe_debug_cvt
+    assert f(2, FAKE, FAKE, 16, None) == INVALID          # unknown format
+    assert f(0, FAKE, FAKE, 6, None) == INVALID           # n % 4
+    assert f(1, FAKE + 4, FAKE, 16, None) == INVALID      # alignment
+    assert f(0, None, None, 0, None) == 0
+    assert L.moe_kernel_launch_count() == 0
