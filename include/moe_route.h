@@ -10,6 +10,13 @@
  *   swiglu_cast_fp8      x [M,2N] bf16     -> out [M,N] E4M3 bytes, out_sf [M,N/128] f32
  *   moe_combine          y [R,H] bf16, topk_weights, pos -> out [T,H] bf16 or f32
  *
+ * and their widened forms: the padded expert layout (moe_route_map_aligned,
+ * moe_expand_cast_fp8_padded), the scale options and SwiGLU variants
+ * (moe_expand_cast_fp8_ex, swiglu_cast_fp8_ex), the FP4 E2M1 casts
+ * (moe_expand_cast_fp4, swiglu_cast_fp4), steps 1-3 in one call with a fused
+ * decode launch (moe_route_expand_cast_fp8), and the route map without a
+ * workspace (moe_route_map_noalloc).
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Pointers are DEVICE pointers into memory the caller owns (allocated by the
@@ -59,7 +66,8 @@ extern "C" {
 /* Largest supported expert count and top-k. */
 #define MOE_MAX_EXPERTS 1024
 #define MOE_MAX_TOPK 32
-/* The only scaling-group size implemented: one fp32 scale per 128 channels. */
+/* The FP8 casts' scaling group: one fp32 scale per 128 channels (the FP4
+ * casts take 16, 32, 64 or 128). */
 #define MOE_CAST_GROUP 128
 
 typedef enum moe_status {
