@@ -16,8 +16,8 @@ namespace moe {
 // do.  Every non-NaN key is >= 0x007FFFFF (the key of -inf), so 0 never
 // collides with a real score and marks a retired or absent slot.
 __device__ __forceinline__ uint32_t score_key(float s) {
-  uint32_t b = __float_as_uint(s == 0.0f ? 0.0f : s);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  const uint32_t b = __float_as_uint(s + 0.0f);  // -0.0 + 0.0 = +0.0 (round to nearest)
+  return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);  // negative: ~b; else b | sign
 }
 
 __device__ __forceinline__ float key_score(uint32_t key) {
@@ -31,8 +31,9 @@ __device__ __forceinline__ float key_score(uint32_t key) {
 // the larger packed value is the larger score, or on equal scores the lower
 // expert, so the packed order is exactly the selection order.
 //
-// Fast path: theta = the k-th largest of the 32 lane maxima.  At least k
-// distinct experts score >= theta, so every top-k expert does too; the lanes
+// Fast path: theta = the k-th largest distinct value among the 32 lane maxima
+// (at most the k-th largest lane maximum).  At least k distinct experts score
+// >= theta, so every top-k expert does too; the lanes
 // compact their experts scoring >= theta (usually 8-16 of them) one per lane,
 // and each candidate's rank (how many candidates beat it) is its output slot
 // if below k.
@@ -109,8 +110,12 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ row, int E,
   // expert out_e with score key out_key.
   int out_j = -1;
   uint32_t out_key = 0, out_e = 0;
-  // ---- candidate filter: theta = k-th largest of the 32 lane maxima; every
-  // top-k element scores >= theta (k distinct lane maxima do)
+  // ---- candidate filter: theta = the k-th largest distinct value among the
+  // 32 lane maxima (each round retires every lane holding the current
+  // maximum).  theta <= the k-th largest lane maximum, and the k largest lane
+  // maxima are k distinct experts, so every top-k element scores >= theta.
+  // With heavy ties theta falls lower and more candidates pass: the sorted
+  // merge below handles more than 32.
   uint32_t lmax = 0;
 #pragma unroll
   for (int i = 0; i < V; ++i) lmax = max(lmax, (uint32_t)(p[i] >> 32));
@@ -121,8 +126,7 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ row, int E,
     for (int r = 0; r < KMAX; ++r) {
       if (r < k) {
         theta = __reduce_max_sync(0xFFFFFFFFu, lm);
-        const unsigned holders = __ballot_sync(0xFFFFFFFFu, lm == theta);
-        if (lane == __ffs(holders) - 1) lm = 0u;  // retire one holder
+        if (lm == theta) lm = 0u;  // retire every holder
       }
     }
   }
