@@ -395,6 +395,26 @@ def gpu_arm(args):
     return line
 
 
+def gpu_numa_cpus(dev):
+    """(NUMA node, its CPU ids) of the host memory attached to `dev`, from
+    sysfs; (None, None) where the system does not say."""
+    import torch
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id.lower()
+        dom, rest = bus.split(":", 1)
+        path = f"/sys/bus/pci/devices/{int(dom, 16):04x}:{rest}/numa_node"
+        node = int(open(path).read().strip())
+        if node < 0:
+            return None, None
+        cpus = []
+        for part in open(f"/sys/devices/system/node/node{node}/cpulist").read().strip().split(","):
+            a, _, b = part.partition("-")
+            cpus.extend(range(int(a), int(b or a) + 1))
+        return node, cpus
+    except (OSError, ValueError, AttributeError, RuntimeError):
+        return None, None
+
+
 def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, src, ws, q, sf,
             T, E, k, H, R, chk, barrier, maxr):
     """route+expand+cast with the inputs copied from pinned host memory and
@@ -404,6 +424,16 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
     step's host-to-device copy and kernels (as a caller streaming batches
     would run it); every step still makes all of its own copies."""
     import torch
+    # pinned host buffers on the NUMA node the GPU is attached to: the thread
+    # runs there while it allocates and touches them (first touch places the
+    # pages); a buffer on the other socket crosses the socket link
+    node, cpus = gpu_numa_cpus(dev)
+    old_aff = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    if cpus and old_aff is not None:
+        try:
+            os.sched_setaffinity(0, cpus)
+        except OSError:
+            node = None
     h_scores = torch.empty_like(scores, device="cpu").pin_memory()
     h_x = torch.empty_like(x, device="cpu").pin_memory()
     h_scores.copy_(scores)
@@ -414,6 +444,9 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
     out_names = ["idx", "wt", "counts", "offsets", "pos", "src", "q", "sf"]
     h_outs = [[torch.empty_like(sl[n], device="cpu").pin_memory() for n in out_names]
               for sl in slots]
+    for hs in h_outs:
+        for h in hs:
+            h.zero_()  # touch every page now, on this node
     streams = [torch.cuda.Stream(device=dev) for _ in slots]
     h2d = h_scores.numel() * 4 + h_x.numel() * 2
     d2h = sum(slot0[n].numel() * slot0[n].element_size() for n in out_names)
@@ -454,8 +487,11 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
     ms = maxr(a.elapsed_time(b) / steps)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     del slots, h_outs
+    if cpus and old_aff is not None:
+        os.sched_setaffinity(0, old_aff)
     return {"value": round(R * world / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
             "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "host_numa_node": node,
             "path": "pinned host -> device, C ABI topk_gate/route_map/expand_cast_fp8, "
                     "all outputs -> pinned host; steps alternate between two streams"}
 
