@@ -142,3 +142,14 @@ def test_wait_that_runs_out_reports_timeout_and_leaves_a_usable_context():
     res = ops.route_expand_cast_fp8(s, xd, k, mode=ops.PATH_FUSED, workspace=ws)
     assert ops.device_status() == 0
     _check_against_oracle(scores, x, k, res)
+
+
+@pytest.mark.parametrize("mode", [ops.PATH_AUTO, ops.PATH_FUSED, ops.PATH_SEPARATE])
+def test_no_tokens(mode):
+    E, k, H = 64, 4, 256
+    s = torch.empty(0, E, device=DEV)
+    x = torch.empty(0, H, dtype=torch.bfloat16, device=DEV)
+    res = ops.route_expand_cast_fp8(s, x, k, mode=mode)
+    assert ops.device_status() == 0
+    assert int(res[2].abs().sum()) == 0 and int(res[3].abs().sum()) == 0   # counts, offsets
+    assert res[6].shape == (0, H)

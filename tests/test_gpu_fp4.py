@@ -206,3 +206,17 @@ def test_swiglu_fp4_full_size_sampled_rows():
     xs = hx[torch.from_numpy(rows).to(DEV)].cpu()
     o_q, o_sf, _ = oracle.swiglu_cast_fp4(oracle.bf16_bits(xs), group=32)
     check_swiglu_opts(np_(q)[rows], np_(sf)[rows], o_q, o_sf, o_sf, 0, 2000, ordinal=fp4_ordinal)
+
+
+def test_fp4_empty_inputs_and_zero_fill_only():
+    H, R = 512, 40
+    src = torch.full((R,), -1, dtype=torch.int32, device=DEV)
+    q = torch.full((R, H // 2), 0xAB, dtype=torch.uint8, device=DEV)
+    sf = torch.full((R, H // 32), 7.0, device=DEV)
+    ops.expand_cast_fp4(torch.empty(0, H, dtype=torch.bfloat16, device=DEV),
+                        torch.empty(0, 2, dtype=torch.int32, device=DEV), group=32,
+                        sorted_src=src, out=q, out_sf=sf)
+    assert ops.device_status() == 0
+    assert int(q.sum()) == 0 and float(sf.abs().sum()) == 0.0
+    q2, sf2 = ops.swiglu_cast_fp4(torch.empty(0, 2 * H, dtype=torch.bfloat16, device=DEV), group=32)
+    assert q2.shape == (0, H // 2) and sf2.shape == (0, H // 32)
