@@ -211,7 +211,7 @@ def gpu_arm(args):
     full = args.ops == "all"
     inp = workloads.make_inputs(w, seed=shard_seed(rank), device=dev, with_y=full, with_swiglu=full,
                                 swiglu_rows=R, swiglu_n=N)
-    ran = {"topk_gate", "route_map"} | ({"expand_cast_fp8"} if args.ops != "route" else set()) | \
+    ran = {"topk_gate", "route_map", "expand_cast_fp8"} | \
         ({"swiglu_cast_fp8", "combine"} if full else set())
     scores, x = inp["scores"], inp["x"]
     y, hx = inp.get("y"), inp.get("swiglu_x")
@@ -221,8 +221,8 @@ def gpu_arm(args):
     counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
     pos, src = torch.empty(T, k, **i32), torch.empty(R, **i32)
     ws = torch.empty(max(1, ops.route_map_workspace_bytes(T, E, k)), dtype=torch.uint8, device=dev)
-    q = torch.empty(R if args.ops != "route" else 1, H, dtype=torch.uint8, device=dev)
-    sf = torch.empty(R if args.ops != "route" else 1, G, dtype=torch.float32, device=dev)
+    q = torch.empty(R, H, dtype=torch.uint8, device=dev)
+    sf = torch.empty(R, G, dtype=torch.float32, device=dev)
     if full:
         q2 = torch.empty(R, N, dtype=torch.uint8, device=dev)
         sf2 = torch.empty(R, N // 128, dtype=torch.float32, device=dev)
@@ -255,9 +255,8 @@ def gpu_arm(args):
         chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
                             pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
         rec(2)
-        if args.ops != "route":
-            chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
-                                      sf.data_ptr(), 128, sp), "expand")
+        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
+                                  sf.data_ptr(), 128, sp), "expand")
         rec(3)
         if full:
             chk(L.swiglu_cast_fp8(hx.data_ptr(), R, N, q2.data_ptr(), sf2.data_ptr(), 128, sp),
@@ -1004,9 +1003,9 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=2048)
     ap.add_argument("--workload", choices=["prefill_64k", "skewed_8k", "decode_1k", "tiny"],
                     default=WORKLOAD)
-    ap.add_argument("--ops", choices=["all", "route_expand_cast", "route"], default="all",
-                    help="run only part of the step (profiling); the reported line always "
-                         "names what ran")
+    ap.add_argument("--ops", choices=["all", "route_expand_cast"], default="all",
+                    help="all: the whole step (route+expand+cast, SwiGLU, combine); "
+                         "route_expand_cast: the headline ops only")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
