@@ -370,6 +370,22 @@ def expand_cast_fp8(x_bits, pos, num_rows: int | None = None, group: int = 128,
     return q, sf
 
 
+def expand_cast_fp8_into(x_bits, pos, q, sf, group: int = 128):
+    """expand_cast_fp8 writing into the caller's arrays: q [R, H] uint8 and
+    sf [R, H/group] float32 (rows no pos names are left as they are).  Only
+    the marshalling differs, so token shards may run in separate threads (the
+    C call releases the GIL; each shard writes its own rows)."""
+    x = _as(x_bits, np.uint16)
+    p = _as(pos, np.int32)
+    T, H = x.shape
+    k = p.shape[1]
+    if q.dtype != np.uint8 or sf.dtype != np.float32 or q.shape[1] != H or \
+            sf.shape != (q.shape[0], H // group):
+        raise TypeError("q must be uint8 [R, H] and sf float32 [R, H/group]")
+    _check(_load().oracle_expand_cast_fp8(_ptr(x), T, H, k, _ptr(p), q.shape[0], group, _ptr(q),
+                                          _ptr(sf)), "expand_cast_fp8")
+
+
 def swiglu_values(x_bits):
     """TileKernels page, 3.3: fp32 silu(gate) * up, before the cast."""
     x = _as(x_bits, np.uint16)
