@@ -74,10 +74,12 @@ KERNEL_OF_OP = {  # op -> (kernel name in ncu, source file), for E <= 256 and H 
 
 
 def source_sha(fname):
-    p = os.path.join(ROOT, "moe_routing_precision_gb300", "csrc", fname)
+    """Hash of a kernel's source file and every header of the kernel tree
+    (a change to any of them invalidates the recorded traffic)."""
+    d = os.path.join(ROOT, "moe_routing_precision_gb300", "csrc")
     h = hashlib.sha256()
-    for q in (p, os.path.join(ROOT, "moe_routing_precision_gb300", "csrc", "common.cuh")):
-        with open(q, "rb") as f:
+    for q in [fname] + sorted(f for f in os.listdir(d) if f.endswith(".cuh")):
+        with open(os.path.join(d, q), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
