@@ -144,9 +144,11 @@ __global__ void __launch_bounds__(kThreads, EXT ? 5 : 6)
 
 // FP4 E2M1 output (TileKernels article, 3.1's float4_e2m1fn: max 6,
 // clamp_min 6 * 2^-126): groups of 16 L channels, L lanes per group, 32 / L
-// groups per warp tile; 8 bytes of packed codes per lane.
-template <int L>
-__global__ void __launch_bounds__(kThreads, 5)
+// groups per warp tile; 8 bytes of packed codes per lane.  EXT = false (no
+// clamp, weight, count or scale option) compiles none of the variants and
+// keeps 6 CTAs resident, as the E4M3 plain form.
+template <int L, bool EXT>
+__global__ void __launch_bounds__(kThreads, EXT ? 5 : 6)
     swiglu_cast_fp4_kernel(const uint16_t* __restrict__ x, uint32_t units, int N,
                            uint8_t* __restrict__ out, float* __restrict__ out_sf, FastDiv fdG,
                            SwigluExt ext) {
@@ -173,25 +175,25 @@ __global__ void __launch_bounds__(kThreads, 5)
       gb = ld_stream_v4(gate + 8);
       ua = ld_stream_v4(up);
       ub = ld_stream_v4(up + 8);
-      if (ext.weights != nullptr) wr = __ldg(ext.weights + r);
+      if (EXT && ext.weights != nullptr) wr = __ldg(ext.weights + r);
     }
     float v[16];
-    lane_values<true>(ga, gb, ua, ub, active, wr, ext, clamped, v);
+    lane_values<EXT>(ga, gb, ua, ub, active, wr, ext, clamped, v);
     const float amax = maxL<L>(absmax16(v));
-    const float sf = fp4_scale(amax, ext.sf.flags);
+    const float sf = fp4_scale(amax, EXT ? ext.sf.flags : 0);
     const float inv = __fdiv_rn(1.0f, sf);
     const uint2 q = quant16_e2m1(v, inv);
     if (active) {
       st_stream_v2(out + (int64_t)r * (N >> 1) + g * 8 * L + lg * 8, q);
       if (lg == 0) {
-        if (ext.sf.flags != 0)
+        if (EXT && ext.sf.flags != 0)
           store_sf_opts(out_sf, ext.sf.flags, ext.sf.ld, G, r, g, sf);
         else
           st_stream_f32(out_sf + (int64_t)r * G + g, sf);
       }
     }
   }
-  add_clamp_count(ext, clamped, lane);
+  if (EXT) add_clamp_count(ext, clamped, lane);
 }
 
 template <bool EXT>
@@ -212,23 +214,32 @@ cudaError_t launch_t(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_
                     ext);
 }
 
-template <int L>
-cudaError_t launch_fp4(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
-                       float* out_sf, const SwigluExt& ext) {
+template <int L, bool EXT>
+cudaError_t launch_fp4_t(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
+                         float* out_sf, const SwigluExt& ext) {
   constexpr int U = 32 / L;
   const int G = N / (16 * L);
   const uint32_t units = (uint32_t)(M * G);  // < 2^31, checked by the caller
   const uint32_t tiles = (units + U - 1) / U;
   const int64_t need = ((int64_t)tiles + (kThreads / 32) - 1) / (kThreads / 32);
   int per_sm = 0;
-  cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, swiglu_cast_fp4_kernel<L>,
-                                                                 kThreads, 0);
+  cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, swiglu_cast_fp4_kernel<L, EXT>, kThreads, 0);
   if (st != cudaSuccess) return st;
   const int64_t cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
   const int blocks = (int)(need < cap ? need : cap);
-  return launch_pdl(swiglu_cast_fp4_kernel<L>, blocks, kThreads, 0, c.stream,
+  return launch_pdl(swiglu_cast_fp4_kernel<L, EXT>, blocks, kThreads, 0, c.stream,
                     static_cast<const uint16_t*>(x), units, N, out, out_sf, FastDiv((uint32_t)G),
                     ext);
+}
+
+template <int L>
+cudaError_t launch_fp4(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_t* out,
+                       float* out_sf, const SwigluExt& ext) {
+  const bool plain = !ext.has_clamp && ext.weights == nullptr && ext.clamp_count == nullptr &&
+                     ext.sf.flags == 0;
+  return plain ? launch_fp4_t<L, false>(c, x, M, N, out, out_sf, ext)
+               : launch_fp4_t<L, true>(c, x, M, N, out, out_sf, ext);
 }
 
 }  // namespace
