@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from moe_routing_precision_gb300 import ops, workloads
-from tests.parity_util import assert_equal, check_swiglu_opts
+from tests.parity_util import assert_equal, check_swiglu_opts, fp4_ordinal
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -239,3 +239,39 @@ def test_swiglu_ex_empty_rows():
     cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
     q, sf = ops.swiglu_cast_fp8_ex(x, clamp=1.0, clamp_count=cnt, sf_flags=7, sf_ld=0)
     assert q.shape == (0, 256) and int(cnt.item()) == 0
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "fp4"])
+@pytest.mark.parametrize("clamp", [2.5, 2.51])
+def test_swiglu_clamp_fast_path_boundaries(fmt, clamp):
+    """The clamp's warp-level skip test: one value per row at, just above or
+    just below c (2.51 is not a bf16 value; 2.515625 is the next one above
+    it), in the gate or as |up|, among values far below c.  Only values
+    strictly above c are clamped and counted, wherever in the warp they sit
+    (bf16 steps are 2^-6 near 2.5)."""
+    M, N = 64, 256
+    g = torch.Generator().manual_seed(11)
+    x = (torch.rand(M, 2 * N, generator=g) - 0.5).to(torch.bfloat16)
+    cases = [2.515625, 2.5, 2.484375, -2.515625]       # above / at / below 2.5, and a negative one
+    expect = 0
+    for r in range(M):
+        v = cases[r % len(cases)]
+        col = (r * 37) % N
+        if r % 2 == 0:
+            x[r, col] = v                                  # gate
+            expect += v > clamp
+        else:
+            x[r, N + col] = v                              # up: |v| is compared
+            expect += abs(v) > clamp
+    cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
+    xb = oracle.bf16_bits(x)
+    if fmt == "fp8":
+        q, sf = ops.swiglu_cast_fp8_ex(x.to(DEV), clamp=clamp, clamp_count=cnt)
+        o_q, o_sf, o_cnt = oracle.swiglu_cast_fp8_ex(xb, clamp=clamp)
+        check_swiglu_opts(np_(q), np_(sf), o_q, o_sf, o_sf, 0, M)
+    else:
+        q, sf = ops.swiglu_cast_fp4(x.to(DEV), group=32, clamp=clamp, clamp_count=cnt)
+        o_q, o_sf, o_cnt = oracle.swiglu_cast_fp4(xb, group=32, clamp=clamp)
+        check_swiglu_opts(np_(q), np_(sf), o_q, o_sf, o_sf, 0, M, ordinal=fp4_ordinal)
+    assert o_cnt == expect
+    assert int(cnt.item()) == expect
