@@ -79,7 +79,7 @@ def _random_idx(T, E, k, seed, skew=False):
 
 @pytest.mark.parametrize("T,E,k", [(1, 16, 1), (127, 16, 2), (128, 16, 2), (129, 16, 2),
                                    (1000, 256, 8), (4133, 256, 8), (300, 1024, 32), (64, 1, 1),
-                                   (513, 33, 3)])
+                                   (513, 33, 3), (200003, 256, 8)])   # last: 391 chunks
 def test_route_map_parity(T, E, k):
     idx = _random_idx(T, E, k, seed=T + E)
     out = ops.route_map(idx.to(DEV), E)
@@ -123,7 +123,8 @@ def test_route_map_flags_repeated_expert():
 # ---------------------------------------------------------------- expand + cast
 
 @pytest.mark.parametrize("T,H,k", [(1, 128, 1), (3, 384, 2), (33, 256, 8), (64, 256, 2),
-                                   (200, 4096, 8), (37, 7168, 8), (5, 1152, 32)])
+                                   (200, 4096, 8), (37, 7168, 8), (5, 1152, 32),
+                                   (4, 16384, 3), (3, 20480, 2)])   # largest row form; tile form
 def test_expand_cast_parity(T, H, k):
     inp = workloads.random_small(T, 16, k, H, seed=T + H, zero_groups=True)
     x = inp["x"]
@@ -211,7 +212,8 @@ def test_swiglu_cast_limits():
 # ---------------------------------------------------------------- combine
 
 @pytest.mark.parametrize("T,H,k", [(1, 8, 1), (5, 256, 2), (64, 256, 2), (77, 4096, 8),
-                                   (9, 7168, 8), (13, 512, 9), (4, 1024, 32)])
+                                   (9, 7168, 8), (13, 512, 9), (4, 1024, 32), (7, 136, 3),
+                                   (3, 20480, 2)])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_combine_parity(T, H, k, dtype):
     g = torch.Generator().manual_seed(T * H + k)
