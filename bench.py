@@ -655,6 +655,8 @@ def extra_workloads(L, dev, stream, sp, chk, args):
     res.update(cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak))
     torch.cuda.empty_cache()
     res["decode_1k"] = decode_workload(L, dev, stream, sp, chk, flush, iters, peak)
+    for t in (64, 256):
+        res[f"decode_{t}"] = decode_workload(L, dev, stream, sp, chk, flush, iters, peak, T=t)
     del flush
     torch.cuda.empty_cache()
     return res
@@ -839,16 +841,19 @@ def cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak):
     return res
 
 
-def decode_workload(L, dev, stream, sp, chk, flush, iters, peak):
-    """route + expand + cast of the T=1024 decode batch (E=256, k=8, H=4096)
-    through moe_route_expand_cast_fp8: the four separate launches (chained by
-    programmatic dependent launch), the same four captured in a CUDA graph, and
-    the fused single cooperative launch.  Each timed after a 512 MB L2 flush
-    that also keeps the GPU busy while the host enqueues (device time only)."""
+def decode_workload(L, dev, stream, sp, chk, flush, iters, peak, T=1024):
+    """route + expand + cast of a decode batch of T tokens (E=256, k=8,
+    H=4096, the decode_1k recipe) through moe_route_expand_cast_fp8: the four
+    separate launches (chained by programmatic dependent launch), the same four
+    captured in a CUDA graph, the fused single cooperative launch, and the
+    replicated-routing single launch where the shape allows each.  Each timed
+    after a 512 MB L2 flush that also keeps the GPU busy while the host
+    enqueues (device time only)."""
     import torch
 
     from moe_routing_precision_gb300 import ops, workloads
-    w = workloads.WORKLOADS["decode_1k"]
+    base = workloads.WORKLOADS["decode_1k"]
+    w = workloads.Workload(f"decode_{T}", T=T, E=base.E, k=base.k, H=base.H)
     inp = workloads.make_inputs(w, seed=0, device=dev)
     s, x = inp["scores"], inp["x"]
     T, E, k, H, R, G = w.T, w.E, w.k, w.H, w.R, w.G
@@ -881,10 +886,11 @@ def decode_workload(L, dev, stream, sp, chk, flush, iters, peak):
                 ts.append(e0.elapsed_time(e1) * 1e3)
         return statistics.median(ts)
 
-    res = {"op": "topk + route_map + expand_cast_fp8 (T=1024, E=256, k=8, H=4096)"}
+    res = {"op": f"topk + route_map + expand_cast_fp8 (T={T}, E={E}, k={k}, H={H})"}
     B = algorithmic_bytes(T, E, k, H)["route_expand_cast"]
     sep = timed(lambda: call(ops.PATH_SEPARATE))
     fused = timed(lambda: call(ops.PATH_FUSED))
+    rep = timed(lambda: call(ops.PATH_REPLICATED)) if T <= 512 else None
     call(ops.PATH_SEPARATE)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
@@ -895,7 +901,9 @@ def decode_workload(L, dev, stream, sp, chk, flush, iters, peak):
     if L.moe_get_device_status(sp, None) != 0:
         raise RuntimeError("device error in the decode workload")
     for name, us in (("separate_launches", sep), ("separate_in_cuda_graph", graph),
-                     ("fused_single_launch", fused)):
+                     ("fused_single_launch", fused), ("replicated_single_launch", rep)):
+        if us is None:
+            continue
         gbs = B / (us * 1e-6) / 1e9
         res[name] = {"us": round(us, 2), "routed_tokens_per_s": round(R / (us * 1e-6), 1),
                      "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}

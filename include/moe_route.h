@@ -105,9 +105,11 @@ typedef enum moe_out_dtype {
 #define MOE_DEVERR_TIMEOUT 0x10u     /* fused decode path: a bounded wait ran out */
 
 /* Paths of moe_route_expand_cast_fp8. */
-#define MOE_PATH_AUTO 0     /* the library's choice: SEPARATE (measured fastest on GB300)  */
-#define MOE_PATH_FUSED 1    /* one cooperative launch (decode shapes only)               */
-#define MOE_PATH_SEPARATE 2 /* moe_topk_gate + moe_route_map + moe_expand_cast_fp8      */
+#define MOE_PATH_AUTO 0       /* the library's choice (see moe_route_expand_cast_fp8)     */
+#define MOE_PATH_FUSED 1      /* one cooperative launch (decode shapes only)              */
+#define MOE_PATH_SEPARATE 2   /* moe_topk_gate + moe_route_map + moe_expand_cast_fp8     */
+#define MOE_PATH_REPLICATED 3 /* one ordinary launch, routing repeated per block (small T) */
+#define MOE_AUTO_REPLICATED_MAX_TOKENS 96   /* AUTO's switch from REPLICATED to SEPARATE  */
 
 /*
  * moe_topk_gate -- [TK] 2.1 Top-K Gating, plus the "Weight Normalization" that
@@ -419,7 +421,13 @@ moe_status_t moe_combine(const void *y, const float *topk_weights,
  * blocks have arrived on a counter, and signals the others, which write their
  * rows.  Each wait is bounded (1 s); one that runs out sets
  * MOE_DEVERR_TIMEOUT.  It applies to T <= 2048, 32 < E <= 256, k <= 32,
- * T*k <= 16384, H <= 16384 (shared-memory staging permitting).  The SEPARATE path is the
+ * T*k <= 16384, H <= 16384 (shared-memory staging permitting).  The
+ * REPLICATED path is one ordinary launch (programmatic dependent launch, no
+ * cooperative launch, no wait on another block): every block selects the
+ * experts of all T tokens and builds the whole route map in its own shared
+ * memory, then casts and writes its own tokens' rows; block 0 writes idx, w,
+ * counts, offsets, pos and sorted_src.  It applies to T <= 512,
+ * 32 < E <= 256, k <= 32, T*k <= 4096, H <= 8192.  The SEPARATE path is the
  * four launches of the individual calls.
  *   scores [T,E] f32; x [T,H] bf16; topk_idx [T,k] i32; topk_weights [T,k]
  *   f32; counts [E], offsets [E+1], pos [T,k], sorted_src [T*k] i32;
@@ -429,12 +437,16 @@ moe_status_t moe_combine(const void *y, const float *topk_weights,
  *   control words: ZERO them once before the first call (each call leaves
  *   them zero; after a MOE_DEVERR_TIMEOUT, zero them again).  One workspace
  *   must not be used by two calls in flight at once.
- *   mode: MOE_PATH_AUTO, MOE_PATH_FUSED (MOE_ERR_UNSUPPORTED where it does not
- *   apply) or MOE_PATH_SEPARATE.  On GB300 the separate launches, chained by
- *   programmatic dependent launch, were measured as fast as the fused launch
- *   for T <= 64 and faster above (the single routing block and the
- *   cooperative launch cost more than the launch gaps they remove), so AUTO
- *   takes the separate path.
+ *   mode: MOE_PATH_AUTO, MOE_PATH_FUSED or MOE_PATH_REPLICATED
+ *   (MOE_ERR_UNSUPPORTED where they do not apply) or MOE_PATH_SEPARATE.  AUTO
+ *   takes the path measured fastest on GB300 for the shape: REPLICATED for
+ *   T <= MOE_AUTO_REPLICATED_MAX_TOKENS where it applies (E = 256, k = 8,
+ *   H = 4096: 8.8 against 16.0 us at T = 16, 12.9 against 18.0 at T = 64;
+ *   each block's share of the selection grows with T, and from T = 128 the
+ *   separate launches are faster), else SEPARATE (the separate launches,
+ *   chained by programmatic dependent launch, were as fast as the FUSED
+ *   launch for T <= 64 and faster above: its single routing block and the
+ *   cooperative launch cost more than the gaps they remove).
  * Requirements as the individual calls; group == 128.
  */
 moe_status_t moe_route_expand_cast_fp8(const float *scores, int64_t num_tokens,

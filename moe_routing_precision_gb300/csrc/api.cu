@@ -426,7 +426,8 @@ moe_status_t moe_route_expand_cast_fp8(const float* scores, int64_t num_tokens,
                                        void* workspace, size_t workspace_bytes, int32_t mode,
                                        int32_t group, void* stream) {
   if (group != MOE_CAST_GROUP) return MOE_ERR_UNSUPPORTED;
-  if (mode != MOE_PATH_AUTO && mode != MOE_PATH_FUSED && mode != MOE_PATH_SEPARATE)
+  if (mode != MOE_PATH_AUTO && mode != MOE_PATH_FUSED && mode != MOE_PATH_SEPARATE &&
+      mode != MOE_PATH_REPLICATED)
     return MOE_ERR_INVALID_ARG;
   if (num_tokens < 0 || !experts_ok(num_experts, num_topk)) return MOE_ERR_INVALID_ARG;
   if (hidden < MOE_CAST_GROUP || hidden % MOE_CAST_GROUP != 0) return MOE_ERR_INVALID_ARG;
@@ -451,7 +452,18 @@ moe_status_t moe_route_expand_cast_fp8(const float* scores, int64_t num_tokens,
   const bool fused_ok =
       num_tokens > 0 &&
       decode_fused_smem(num_tokens, num_experts, num_topk, hidden, c.num_sms, nullptr, nullptr) > 0;
+  const bool replicated_ok =
+      num_tokens > 0 && decode_replicated_ok(num_tokens, num_experts, num_topk, hidden);
   if (mode == MOE_PATH_FUSED && !fused_ok && num_tokens > 0) return MOE_ERR_UNSUPPORTED;
+  if (mode == MOE_PATH_REPLICATED && !replicated_ok && num_tokens > 0) return MOE_ERR_UNSUPPORTED;
+  if (mode == MOE_PATH_AUTO && replicated_ok && num_tokens <= MOE_AUTO_REPLICATED_MAX_TOKENS)
+    mode = MOE_PATH_REPLICATED;
+  if (mode == MOE_PATH_REPLICATED && replicated_ok) {
+    cudaError_t e = launch_decode_replicated(c, scores, num_tokens, num_experts, num_topk, x,
+                                             hidden, topk_idx, topk_weights, counts, offsets, pos,
+                                             sorted_src, out, out_sf);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+  }
   if (mode == MOE_PATH_FUSED && fused_ok) {
     cudaError_t e = launch_decode_fused(c, scores, num_tokens, num_experts, num_topk, x, hidden,
                                         topk_idx, topk_weights, counts, offsets, pos, sorted_src,

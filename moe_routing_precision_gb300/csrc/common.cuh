@@ -302,6 +302,15 @@ cudaError_t launch_decode_fused(const LaunchCtx& c, const float* scores, int64_t
                                 int32_t* offsets, int32_t* pos, int32_t* src, uint8_t* out,
                                 float* out_sf, unsigned* ctl);
 
+// Replicated-routing decode path (decode_replicated.cu): every block selects
+// and routes all T tokens itself, then writes its own tokens' rows.
+constexpr int kDecodeReplicatedMaxTokens = 512;
+bool decode_replicated_ok(int64_t T, int E, int k, int H);
+cudaError_t launch_decode_replicated(const LaunchCtx& c, const float* scores, int64_t T, int E,
+                                     int k, const void* x, int H, int32_t* idx, float* w,
+                                     int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* src,
+                                     uint8_t* out, float* out_sf);
+
 cudaError_t launch_topk_gate(const LaunchCtx& c, const float* scores, int64_t T, int E, int k,
                              int32_t* idx, float* w);
 cudaError_t launch_route_map(const LaunchCtx& c, const int32_t* idx, int64_t T, int E, int k,

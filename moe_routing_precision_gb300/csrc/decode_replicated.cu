@@ -1,0 +1,217 @@
+// decode_replicated.cu -- top-k gate, route map and expand + E4M3 cast of a
+// small decode batch in ONE ordinary launch with no communication between
+// blocks.
+//
+// "CuTeDSL at Perplexity" (perplexity.ai), the prefill/decode section: decode
+// kernels run at launch latency, so the fewer dependent launches the better;
+// the MoE dispatch section routes with shared-memory counters.  Here every
+// block selects the experts of ALL T tokens and builds the whole route map in
+// its own shared memory (T*k <= 4096 copies), then casts and writes only its
+// own tokens' rows.  The selection is repeated by every block, which is cheap
+// for small T (T / 16 tokens per warp); in exchange there is no grid barrier,
+// no wait on another block and no cooperative launch, and the launch takes
+// part in programmatic dependent launch like the separate kernels.  Block 0
+// also writes idx, w, counts, offsets, pos and sorted_src.
+//
+// Results are those of moe_topk_gate + moe_route_map + moe_expand_cast_fp8:
+// the same top-k routine, the route map's stable order (copies of one expert
+// in ascending token order, from per-expert 32-token bitmaps and popcounts),
+// and the same scale arithmetic.
+#include "topk_warp.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRepWarps = 16;
+constexpr int kRepThreads = kRepWarps * 32;
+
+struct RepArgs {
+  const float* scores;
+  const uint16_t* x;
+  int32_t* idx;
+  float* w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* pos;
+  int32_t* src;
+  uint8_t* out;
+  float* out_sf;
+  unsigned* err;
+  int T, E, k, H;
+  FastDiv fk;  // division by k
+};
+
+// Shared memory beyond the static arrays: idx and pos [T*k], offsets [E],
+// bitmaps [W][E] u32 and their word prefixes [W][E] u16 (W = ceil(T/32)).
+size_t rep_dyn_smem(int T, int E, int k) {
+  const size_t P = (size_t)T * k, W = ((size_t)T + 31) / 32;
+  return 4 * (2 * P + E) + 4 * W * E + ((2 * W * E + 15) / 16) * 16;
+}
+
+template <int V, bool VEC, int KMAX>
+__global__ void __launch_bounds__(kRepThreads, 1) decode_replicated_kernel(RepArgs a) {
+  __shared__ unsigned long long s_list[kRepWarps][V][32];
+  __shared__ unsigned long long s_cand[kRepWarps][32];
+  __shared__ int s_scan[2 * 32];  // warp totals, then exclusive warp prefixes
+  extern __shared__ __align__(16) int32_t s_dyn[];
+  const int T = a.T, E = a.E, k = a.k, H = a.H;
+  const int P = T * k, W = (T + 31) >> 5, G = H >> 7;
+  int32_t* s_idx = s_dyn;
+  int32_t* s_pos = s_idx + P;
+  int32_t* s_off = s_pos + P;
+  uint32_t* bm = reinterpret_cast<uint32_t*>(s_off + E);
+  uint16_t* pre = reinterpret_cast<uint16_t*>(bm + W * E);
+  pdl_enter();
+  const int tid = threadIdx.x, lane = tid & 31, wib = tid >> 5;
+  const bool b0 = blockIdx.x == 0;
+  const bool act = tid < (H >> 4);  // 16 channels per thread (H <= 8192)
+
+  // this block's first token: its loads go out before the selection
+  int t = blockIdx.x;
+  uint4 va = make_uint4(0, 0, 0, 0), vb = va;
+  if (t < T && act) {
+    va = ld_stream_v4(a.x + (int64_t)t * H + tid * 16);
+    vb = ld_stream_v4(a.x + (int64_t)t * H + tid * 16 + 8);
+  }
+  for (int i = tid; i < W * E; i += kRepThreads) bm[i] = 0u;
+
+  // ---- 1: the experts of every token (block 0: also the weights)
+  for (int tt = wib; tt < T; tt += kRepWarps)
+    topk_token<V, VEC, KMAX>(a.scores + (int64_t)tt * E, E, k, lane, s_list[wib], s_cand[wib],
+                             s_idx + tt * k,
+                             (b0 && a.w != nullptr) ? a.w + (int64_t)tt * k : nullptr);
+  __syncthreads();
+
+  // ---- 2: the route map.  Bit (t % 32) of bm[t / 32][e] <=> token t chose e;
+  // a copy's row is offsets[e] + (copies in earlier words) + popc(lower bits).
+  for (int p = tid; p < P; p += kRepThreads) {
+    const int e = s_idx[p];
+    if ((unsigned)e < (unsigned)E) {
+      const int tt = (int)a.fk.div((uint32_t)p);
+      atomicOr(bm + (tt >> 5) * E + e, 1u << (tt & 31));
+    }
+  }
+  __syncthreads();
+  int total = 0;
+  if (tid < E) {
+    for (int w = 0; w < W; ++w) {
+      pre[w * E + tid] = (uint16_t)total;
+      total += __popc(bm[w * E + tid]);
+    }
+  }
+  const int incl = warp_incl_scan(total, lane);  // exclusive scan of the totals over e
+  if (lane == 31) s_scan[wib] = incl;
+  __syncthreads();
+  if (wib == 0) {
+    const int v = lane < kRepWarps ? s_scan[lane] : 0;
+    const int sc = warp_incl_scan(v, lane);
+    if (lane < kRepWarps) s_scan[32 + lane] = sc - v;
+  }
+  __syncthreads();
+  if (tid < E) {
+    const int excl = s_scan[32 + wib] + incl - total;
+    s_off[tid] = excl;
+    if (b0) {
+      a.counts[tid] = total;
+      a.offsets[tid] = excl;
+    }
+  }
+  if (b0 && tid == 0) a.offsets[E] = s_scan[32 + kRepWarps - 1] + s_scan[kRepWarps - 1];
+  __syncthreads();
+  for (int p = tid; p < P; p += kRepThreads) {
+    const int e = s_idx[p];
+    int r = -1;
+    if ((unsigned)e < (unsigned)E) {
+      const int tt = (int)a.fk.div((uint32_t)p);
+      const int wd = (tt >> 5) * E + e;
+      r = s_off[e] + pre[wd] + __popc(bm[wd] & ((1u << (tt & 31)) - 1u));
+    } else if (b0) {
+      flag_error(a.err, MOE_DEVERR_EXPERT_RANGE);  // top-k never selects one
+    }
+    s_pos[p] = r;
+    if (b0) {
+      a.idx[p] = e;
+      a.pos[p] = r;
+      if (r >= 0) a.src[r] = p;
+    }
+  }
+  __syncthreads();
+
+  // ---- 3: this block's tokens, cast once and written to their k rows
+  for (; t < T; t += gridDim.x) {
+    const uint4 ca = va, cb = vb;
+    const int tn = t + gridDim.x;
+    if (tn < T && act) {  // the next token's loads stay in flight during this one
+      va = ld_stream_v4(a.x + (int64_t)tn * H + tid * 16);
+      vb = ld_stream_v4(a.x + (int64_t)tn * H + tid * 16 + 8);
+    }
+    const float amax = max8(absmax16_bf16(ca, cb));  // every lane: shuffles over 8 lanes
+    const float sf = group_scale(amax);
+    const float inv = __fdiv_rn(1.0f, sf);
+    const uint4 q = quant16_bf16(ca, cb, inv);
+    if (act) {
+      for (int j = 0; j < k; ++j) {
+        const int r = s_pos[t * k + j];
+        if (r < 0 || r >= P) continue;
+        st_stream_v4(a.out + (int64_t)r * H + tid * 16, q);
+        if ((tid & 7) == 0) st_stream_f32(a.out_sf + (int64_t)r * G + (tid >> 3), sf);
+      }
+    }
+  }
+}
+
+template <int V, bool VEC, int KMAX>
+cudaError_t launch_t(const LaunchCtx& c, const RepArgs& a, int blocks, size_t smem) {
+  auto kern = decode_replicated_kernel<V, VEC, KMAX>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, blocks, kRepThreads, smem, c.stream, a);
+}
+
+}  // namespace
+
+bool decode_replicated_ok(int64_t T, int E, int k, int H) {
+  return T >= 1 && T <= kDecodeReplicatedMaxTokens && E > 32 && E <= 256 && k <= 32 &&
+         T * k <= 4096 && H <= 8192;
+}
+
+cudaError_t launch_decode_replicated(const LaunchCtx& c, const float* scores, int64_t T, int E,
+                                     int k, const void* x, int H, int32_t* idx, float* w,
+                                     int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* src,
+                                     uint8_t* out, float* out_sf) {
+  if (!decode_replicated_ok(T, E, k, H)) return cudaErrorInvalidValue;
+  RepArgs a;
+  a.scores = scores;
+  a.x = static_cast<const uint16_t*>(x);
+  a.idx = idx;
+  a.w = w;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.pos = pos;
+  a.src = src;
+  a.out = out;
+  a.out_sf = out_sf;
+  a.err = c.err;
+  a.T = (int)T;
+  a.E = E;
+  a.k = k;
+  a.H = H;
+  a.fk = FastDiv((uint32_t)k);
+  const int blocks = (int)(T < c.num_sms ? T : c.num_sms);
+  const size_t smem = rep_dyn_smem((int)T, E, k);
+  const bool vec = (E % 128 == 0) && (reinterpret_cast<uintptr_t>(scores) % 16 == 0);
+  if (E <= 64) return k <= 8 ? launch_t<2, false, 8>(c, a, blocks, smem)
+                             : launch_t<2, false, 32>(c, a, blocks, smem);
+  if (E <= 128) {
+    if (vec) return k <= 8 ? launch_t<4, true, 8>(c, a, blocks, smem)
+                           : launch_t<4, true, 32>(c, a, blocks, smem);
+    return k <= 8 ? launch_t<4, false, 8>(c, a, blocks, smem)
+                  : launch_t<4, false, 32>(c, a, blocks, smem);
+  }
+  if (vec) return k <= 8 ? launch_t<8, true, 8>(c, a, blocks, smem)
+                         : launch_t<8, true, 32>(c, a, blocks, smem);
+  return k <= 8 ? launch_t<8, false, 8>(c, a, blocks, smem)
+                : launch_t<8, false, 32>(c, a, blocks, smem);
+}
+
+}  // namespace moe

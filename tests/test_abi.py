@@ -202,8 +202,9 @@ def test_route_expand_cast_rejects_bad_arguments(L):
     def args(mode=0, H=H, x=FAKE, ws=FAKE, wsb=need, group=128):
         return (FAKE, T, E, k, x, H, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, wsb,
                 mode, group, None)
-    assert f(*args(mode=3)) == INVALID
+    assert f(*args(mode=4)) == INVALID
     assert f(*args(mode=-1)) == INVALID
+    assert f(*args(mode=3, wsb=need - 1)) == INVALID   # REPLICATED checks the same arguments
     assert f(*args(group=64)) == UNSUPPORTED
     assert f(*args(H=200)) == INVALID
     assert f(*args(wsb=need - 1)) == INVALID

@@ -1,7 +1,9 @@
-"""GPU parity of the fused decode path (top-k gate, route map and expand +
-E4M3 cast in one cooperative launch) against the oracle, its agreement with
-the separate launches, path selection, and the bounded-wait failure path
-(a signal that is never sent; no fault, no hang)."""
+"""GPU parity of the decode paths of moe_route_expand_cast_fp8 (top-k gate,
+route map and expand + E4M3 cast in one launch: FUSED, one cooperative launch;
+REPLICATED, one ordinary launch with the routing repeated per block) against
+the oracle, their agreement with the separate launches, path selection, and
+the fused path's bounded-wait failure path (a signal that is never sent; no
+fault, no hang)."""
 import numpy as np
 import pytest
 import torch
@@ -94,10 +96,12 @@ def test_back_to_back_calls_share_a_workspace():
         _check_against_oracle(scores, x, k, res)
 
 
-def test_fused_is_one_launch_and_auto_takes_the_separate_path():
+def test_path_launch_counts_and_auto_choice():
     E, k, H = 256, 8, 512
-    for T, mode, launches in [(512, ops.PATH_FUSED, 1), (512, ops.PATH_AUTO, 4),
-                              (4096, ops.PATH_AUTO, 4)]:
+    for T, mode, launches in [(512, ops.PATH_FUSED, 1), (512, ops.PATH_REPLICATED, 1),
+                              (512, ops.PATH_AUTO, 4), (4096, ops.PATH_AUTO, 4),
+                              (64, ops.PATH_AUTO, 1), (96, ops.PATH_AUTO, 1),
+                              (97, ops.PATH_AUTO, 4)]:
         scores, x = _inputs(T, E, k, H, seed=T)
         s, xd = scores.to(DEV), x.to(DEV)
         ws = ops.route_expand_cast_workspace(T, E, k, xd)
@@ -106,7 +110,7 @@ def test_fused_is_one_launch_and_auto_takes_the_separate_path():
         res = ops.route_expand_cast_fp8(s, xd, k, mode=mode, workspace=ws)
         assert ops.launch_count() - n0 == launches
         assert ops.device_status() == 0
-        if T == 512:
+        if T <= 512:
             _check_against_oracle(scores, x, k, res)
 
 
@@ -144,7 +148,8 @@ def test_wait_that_runs_out_reports_timeout_and_leaves_a_usable_context():
     _check_against_oracle(scores, x, k, res)
 
 
-@pytest.mark.parametrize("mode", [ops.PATH_AUTO, ops.PATH_FUSED, ops.PATH_SEPARATE])
+@pytest.mark.parametrize("mode", [ops.PATH_AUTO, ops.PATH_FUSED, ops.PATH_SEPARATE,
+                                  ops.PATH_REPLICATED])
 def test_no_tokens(mode):
     E, k, H = 64, 4, 256
     s = torch.empty(0, E, device=DEV)
@@ -153,3 +158,56 @@ def test_no_tokens(mode):
     assert ops.device_status() == 0
     assert int(res[2].abs().sum()) == 0 and int(res[3].abs().sum()) == 0   # counts, offsets
     assert res[6].shape == (0, H)
+
+
+# ---------------------------------------------------------------- replicated path
+
+REP_CASES = [(1, 64, 2, 128), (7, 256, 8, 4096), (100, 256, 8, 7168), (33, 128, 4, 384),
+             (300, 64, 6, 1024), (512, 256, 8, 512), (128, 256, 32, 256), (151, 96, 3, 640),
+             (153, 256, 8, 8192), (16, 200, 1, 128), (64, 33, 32, 256), (40, 256, 9, 2048)]
+
+
+@pytest.mark.parametrize("T,E,k,H", REP_CASES)
+@pytest.mark.parametrize("ties", [False, True])
+def test_replicated_matches_oracle(T, E, k, H, ties):
+    scores, x = _inputs(T, E, k, H, seed=T + 3 * E + H, ties=ties)
+    res = ops.route_expand_cast_fp8(scores.to(DEV), x.to(DEV), k, mode=ops.PATH_REPLICATED)
+    assert ops.device_status() == 0
+    _check_against_oracle(scores, x, k, res)
+
+
+@pytest.mark.parametrize("T,E,k,H", [(64, 256, 8, 4096), (200, 128, 4, 1024)])
+def test_replicated_equals_separate_launches(T, E, k, H):
+    scores, x = _inputs(T, E, k, H, seed=6)
+    s, xd = scores.to(DEV), x.to(DEV)
+    a = ops.route_expand_cast_fp8(s, xd, k, mode=ops.PATH_REPLICATED)
+    b = ops.route_expand_cast_fp8(s, xd, k, mode=ops.PATH_SEPARATE)
+    assert ops.device_status() == 0
+    for u, v in zip(a, b):
+        assert torch.equal(u.view(torch.uint8) if u.dtype == torch.float32 else u,
+                           v.view(torch.uint8) if v.dtype == torch.float32 else v)
+
+
+def test_replicated_back_to_back_calls():
+    T, E, k, H = 96, 256, 8, 2048
+    outs = []
+    for seed in range(4):                           # no synchronisation between the calls
+        scores, x = _inputs(T, E, k, H, seed=20 + seed)
+        outs.append((scores, x, ops.route_expand_cast_fp8(scores.to(DEV), x.to(DEV), k,
+                                                          mode=ops.PATH_REPLICATED)))
+    assert ops.device_status() == 0
+    for scores, x, res in outs:
+        _check_against_oracle(scores, x, k, res)
+
+
+@pytest.mark.parametrize("T,E,k,H", [(513, 256, 8, 256), (300, 256, 16, 256), (8, 16, 2, 256),
+                                     (8, 512, 8, 256), (8, 256, 8, 8320)])
+def test_replicated_refuses_shapes_it_does_not_handle(T, E, k, H):
+    scores, x = _inputs(T, E, k, H, seed=2)
+    with pytest.raises(ops.MoeError) as ei:
+        ops.route_expand_cast_fp8(scores.to(DEV), x.to(DEV), k, mode=ops.PATH_REPLICATED)
+    assert ei.value.rc == ops.MOE_ERR_UNSUPPORTED
+    res = ops.route_expand_cast_fp8(scores.to(DEV), x.to(DEV), k, mode=ops.PATH_AUTO)
+    assert ops.device_status() == 0
+    _check_against_oracle(scores, x, k, res)
+
