@@ -846,7 +846,8 @@ def decode_workload(L, dev, stream, sp, chk, flush, iters, peak, T=1024):
     H=4096, the decode_1k recipe) through moe_route_expand_cast_fp8: the four
     separate launches (chained by programmatic dependent launch), the same four
     captured in a CUDA graph, the fused single cooperative launch, and the
-    replicated-routing single launch where the shape allows each.  Each timed
+    replicated-routing path (one launch for T <= 32, else the top-k launch and
+    one more) where the shape allows each.  Each timed
     after a 512 MB L2 flush that also keeps the GPU busy while the host
     enqueues (device time only)."""
     import torch
@@ -890,7 +891,7 @@ def decode_workload(L, dev, stream, sp, chk, flush, iters, peak, T=1024):
     B = algorithmic_bytes(T, E, k, H)["route_expand_cast"]
     sep = timed(lambda: call(ops.PATH_SEPARATE))
     fused = timed(lambda: call(ops.PATH_FUSED))
-    rep = timed(lambda: call(ops.PATH_REPLICATED)) if T <= 512 else None
+    rep = timed(lambda: call(ops.PATH_REPLICATED)) if T <= 2048 else None
     call(ops.PATH_SEPARATE)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
@@ -901,7 +902,7 @@ def decode_workload(L, dev, stream, sp, chk, flush, iters, peak, T=1024):
     if L.moe_get_device_status(sp, None) != 0:
         raise RuntimeError("device error in the decode workload")
     for name, us in (("separate_launches", sep), ("separate_in_cuda_graph", graph),
-                     ("fused_single_launch", fused), ("replicated_single_launch", rep)):
+                     ("fused_single_launch", fused), ("replicated_routing", rep)):
         if us is None:
             continue
         gbs = B / (us * 1e-6) / 1e9

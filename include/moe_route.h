@@ -109,7 +109,7 @@ typedef enum moe_out_dtype {
 #define MOE_PATH_FUSED 1      /* one cooperative launch (decode shapes only)              */
 #define MOE_PATH_SEPARATE 2   /* moe_topk_gate + moe_route_map + moe_expand_cast_fp8     */
 #define MOE_PATH_REPLICATED 3 /* one ordinary launch, routing repeated per block (small T) */
-#define MOE_AUTO_REPLICATED_MAX_TOKENS 96   /* AUTO's switch from REPLICATED to SEPARATE  */
+#define MOE_AUTO_REPLICATED_MAX_TOKENS 1024 /* AUTO's switch from REPLICATED to SEPARATE  */
 
 /*
  * moe_topk_gate -- [TK] 2.1 Top-K Gating, plus the "Weight Normalization" that
@@ -422,13 +422,14 @@ moe_status_t moe_combine(const void *y, const float *topk_weights,
  * rows.  Each wait is bounded (1 s); one that runs out sets
  * MOE_DEVERR_TIMEOUT.  It applies to T <= 2048, 32 < E <= 256, k <= 32,
  * T*k <= 16384, H <= 16384 (shared-memory staging permitting).  The
- * REPLICATED path is one ordinary launch (programmatic dependent launch, no
- * cooperative launch, no wait on another block): every block selects the
- * experts of all T tokens and builds the whole route map in its own shared
- * memory, then casts and writes its own tokens' rows; block 0 writes idx, w,
- * counts, offsets, pos and sorted_src.  It applies to T <= 512,
- * 32 < E <= 256, k <= 32, T*k <= 4096, H <= 8192.  The SEPARATE path is the
- * four launches of the individual calls.
+ * REPLICATED path has no wait on another block and no cooperative launch:
+ * every block builds the whole route map in its own shared memory, then casts
+ * and writes its own tokens' rows (and their pos and sorted_src entries).  For
+ * T <= 32 it is one launch in which every block also selects the experts of
+ * all T tokens (block 0 writes idx, w, counts and offsets); above, the top-k
+ * kernel runs first and a second launch does the rest.  It applies to
+ * T <= 2048, T*k <= 16384, 32 < E <= 256, k <= 32, H <= 8192.  The SEPARATE
+ * path is the four launches of the individual calls.
  *   scores [T,E] f32; x [T,H] bf16; topk_idx [T,k] i32; topk_weights [T,k]
  *   f32; counts [E], offsets [E+1], pos [T,k], sorted_src [T*k] i32;
  *   out [T*k,H] u8; out_sf [T*k,H/128] f32.
@@ -441,12 +442,12 @@ moe_status_t moe_combine(const void *y, const float *topk_weights,
  *   (MOE_ERR_UNSUPPORTED where they do not apply) or MOE_PATH_SEPARATE.  AUTO
  *   takes the path measured fastest on GB300 for the shape: REPLICATED for
  *   T <= MOE_AUTO_REPLICATED_MAX_TOKENS where it applies (E = 256, k = 8,
- *   H = 4096: 8.8 against 16.0 us at T = 16, 12.9 against 18.0 at T = 64;
- *   each block's share of the selection grows with T, and from T = 128 the
- *   separate launches are faster), else SEPARATE (the separate launches,
- *   chained by programmatic dependent launch, were as fast as the FUSED
- *   launch for T <= 64 and faster above: its single routing block and the
- *   cooperative launch cost more than the gaps they remove).
+ *   H = 4096, one call: 8.8 against 16.0 us at T = 16, 10.9 against 16.0 at
+ *   T = 128, 15.0 against 20.1 at T = 512, 21.1 against 22.1 at T = 1024; at
+ *   T = 2048 the separate launches are faster), else SEPARATE (the separate
+ *   launches, chained by programmatic dependent launch, were as fast as the
+ *   FUSED launch for T <= 64 and faster above: its single routing block and
+ *   the cooperative launch cost more than the gaps they remove).
  * Requirements as the individual calls; group == 128.
  */
 moe_status_t moe_route_expand_cast_fp8(const float *scores, int64_t num_tokens,

@@ -302,9 +302,11 @@ cudaError_t launch_decode_fused(const LaunchCtx& c, const float* scores, int64_t
                                 int32_t* offsets, int32_t* pos, int32_t* src, uint8_t* out,
                                 float* out_sf, unsigned* ctl);
 
-// Replicated-routing decode path (decode_replicated.cu): every block selects
-// and routes all T tokens itself, then writes its own tokens' rows.
-constexpr int kDecodeReplicatedMaxTokens = 512;
+// Replicated-routing decode path (decode_replicated.cu): every block builds
+// the route map of all T tokens itself (for small T also their selection),
+// then writes its own tokens' rows.
+constexpr int kDecodeReplicatedInlineTokens = 32;  // up to here the selection is repeated too
+constexpr int kDecodeReplicatedMaxTokens = 2048;
 bool decode_replicated_ok(int64_t T, int E, int k, int H);
 cudaError_t launch_decode_replicated(const LaunchCtx& c, const float* scores, int64_t T, int E,
                                      int k, const void* x, int H, int32_t* idx, float* w,

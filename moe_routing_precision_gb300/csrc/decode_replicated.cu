@@ -13,6 +13,12 @@
 // part in programmatic dependent launch like the separate kernels.  Block 0
 // also writes idx, w, counts, offsets, pos and sorted_src.
 //
+// For larger T the selection is not repeated: the top-k kernel runs first
+// (all SMs, once), and a second launch repeats only the route map in every
+// block, from the T*k expert ids in L2, positions its own tokens' copies
+// (writing their pos and sorted_src entries), and casts and writes their
+// rows.
+//
 // Results are those of moe_topk_gate + moe_route_map + moe_expand_cast_fp8:
 // the same top-k routine, the route map's stable order (copies of one expert
 // in ascending token order, from per-expert 32-token bitmaps and popcounts),
@@ -160,6 +166,123 @@ __global__ void __launch_bounds__(kRepThreads, 1) decode_replicated_kernel(RepAr
   }
 }
 
+// Shared memory of the route-only kernel: offsets [E], bitmaps [W][E] u32,
+// word prefixes [W][E] u16, and the rows of this block's copies [tpb * k].
+size_t route_rep_smem(int T, int E, int k, int tpb) {
+  const size_t W = ((size_t)T + 31) / 32;
+  return 4 * (size_t)E + 4 * W * E + ((2 * W * E + 15) / 16) * 16 + 4 * (size_t)tpb * k;
+}
+
+// The second launch of the two-launch form: a.idx holds the top-k launch's
+// expert ids.  Every block builds the route map of all T*k copies in its own
+// shared memory, then takes its tokens t = blockIdx.x + i * gridDim.x.
+__global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel(RepArgs a,
+                                                                               int tpb) {
+  __shared__ int s_scan[2 * 32];
+  extern __shared__ __align__(16) int32_t s_dyn[];
+  const int T = a.T, E = a.E, k = a.k, H = a.H;
+  const int P = T * k, W = (T + 31) >> 5, G = H >> 7;
+  int32_t* s_off = s_dyn;
+  uint32_t* bm = reinterpret_cast<uint32_t*>(s_off + E);
+  uint16_t* pre = reinterpret_cast<uint16_t*>(bm + W * E);
+  int32_t* s_pos = reinterpret_cast<int32_t*>(pre + ((W * E + 7) & ~7));
+  const int tid = threadIdx.x, lane = tid & 31, wib = tid >> 5;
+  const bool b0 = blockIdx.x == 0;
+  const bool act = tid < (H >> 4);
+  // This block's first token: x is read before the wait for the top-k launch.
+  // That launch itself waited for every earlier kernel before it could let
+  // this one start, so x (an input of both) is complete here.
+  int t = blockIdx.x;
+  uint4 va = make_uint4(0, 0, 0, 0), vb = va;
+  if (t < T && act) {
+    va = ld_stream_v4(a.x + (int64_t)t * H + tid * 16);
+    vb = ld_stream_v4(a.x + (int64_t)t * H + tid * 16 + 8);
+  }
+  for (int i = tid; i < W * E; i += kRepThreads) bm[i] = 0u;
+  __syncthreads();
+  pdl_enter();  // the expert ids
+
+  // ---- the route map of every copy, as in the one-launch form
+  for (int p = tid; p < P; p += kRepThreads) {
+    const int e = __ldcg(a.idx + p);
+    if ((unsigned)e < (unsigned)E) {
+      const int tt = (int)a.fk.div((uint32_t)p);
+      atomicOr(bm + (tt >> 5) * E + e, 1u << (tt & 31));
+    }
+  }
+  __syncthreads();
+  int total = 0;
+  if (tid < E) {
+    for (int w = 0; w < W; ++w) {
+      pre[w * E + tid] = (uint16_t)total;
+      total += __popc(bm[w * E + tid]);
+    }
+  }
+  const int incl = warp_incl_scan(total, lane);
+  if (lane == 31) s_scan[wib] = incl;
+  __syncthreads();
+  if (wib == 0) {
+    const int v = lane < kRepWarps ? s_scan[lane] : 0;
+    const int sc = warp_incl_scan(v, lane);
+    if (lane < kRepWarps) s_scan[32 + lane] = sc - v;
+  }
+  __syncthreads();
+  if (tid < E) {
+    const int excl = s_scan[32 + wib] + incl - total;
+    s_off[tid] = excl;
+    if (b0) {
+      a.counts[tid] = total;
+      a.offsets[tid] = excl;
+    }
+  }
+  if (b0 && tid == 0) a.offsets[E] = s_scan[32 + kRepWarps - 1] + s_scan[kRepWarps - 1];
+  __syncthreads();
+  // ---- this block's copies: their rows, pos and sorted_src entries
+  const int nt = (T - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // tokens here
+  bool bad = false;
+  for (int q = tid; q < nt * k; q += kRepThreads) {
+    const int i = (int)a.fk.div((uint32_t)q), j = q - i * k;
+    const int tt = (int)blockIdx.x + i * (int)gridDim.x;
+    const int p = tt * k + j;
+    const int e = __ldcg(a.idx + p);
+    int r = -1;
+    if ((unsigned)e < (unsigned)E) {
+      const int wd = (tt >> 5) * E + e;
+      r = s_off[e] + pre[wd] + __popc(bm[wd] & ((1u << (tt & 31)) - 1u));
+      a.src[r] = p;
+    } else {
+      bad = true;  // top-k never selects one
+    }
+    s_pos[q] = r;
+    a.pos[p] = r;
+  }
+  if (bad) flag_error(a.err, MOE_DEVERR_EXPERT_RANGE);
+  __syncthreads();
+
+  // ---- cast once, write k rows, as in the one-launch form
+  for (int i = 0; t < T; t += gridDim.x, ++i) {
+    const uint4 ca = va, cb = vb;
+    const int tn = t + gridDim.x;
+    if (tn < T && act) {
+      va = ld_stream_v4(a.x + (int64_t)tn * H + tid * 16);
+      vb = ld_stream_v4(a.x + (int64_t)tn * H + tid * 16 + 8);
+    }
+    const float amax = max8(absmax16_bf16(ca, cb));
+    const float sf = group_scale(amax);
+    const float inv = __fdiv_rn(1.0f, sf);
+    const uint4 q = quant16_bf16(ca, cb, inv);
+    if (act) {
+      for (int j = 0; j < k; ++j) {
+        const int r = s_pos[i * k + j];
+        if (r < 0 || r >= P) continue;
+        st_stream_v4(a.out + (int64_t)r * H + tid * 16, q);
+        if ((tid & 7) == 0) st_stream_f32(a.out_sf + (int64_t)r * G + (tid >> 3), sf);
+      }
+    }
+  }
+  (void)tpb;
+}
+
 template <int V, bool VEC, int KMAX>
 cudaError_t launch_t(const LaunchCtx& c, const RepArgs& a, int blocks, size_t smem) {
   auto kern = decode_replicated_kernel<V, VEC, KMAX>;
@@ -171,8 +294,9 @@ cudaError_t launch_t(const LaunchCtx& c, const RepArgs& a, int blocks, size_t sm
 }  // namespace
 
 bool decode_replicated_ok(int64_t T, int E, int k, int H) {
-  return T >= 1 && T <= kDecodeReplicatedMaxTokens && E > 32 && E <= 256 && k <= 32 &&
-         T * k <= 4096 && H <= 8192;
+  if (T < 1 || E <= 32 || E > 256 || k > 32 || H > 8192) return false;
+  if (T <= kDecodeReplicatedInlineTokens) return T * k <= 4096;  // one launch
+  return T <= kDecodeReplicatedMaxTokens && T * k <= 16384;      // top-k launch + route/expand
 }
 
 cudaError_t launch_decode_replicated(const LaunchCtx& c, const float* scores, int64_t T, int E,
@@ -198,6 +322,16 @@ cudaError_t launch_decode_replicated(const LaunchCtx& c, const float* scores, in
   a.H = H;
   a.fk = FastDiv((uint32_t)k);
   const int blocks = (int)(T < c.num_sms ? T : c.num_sms);
+  if (T > kDecodeReplicatedInlineTokens) {
+    cudaError_t e = launch_topk_gate(c, scores, T, E, k, idx, w);
+    if (e != cudaSuccess) return e;
+    const int tpb = (int)((T + blocks - 1) / blocks);
+    const size_t smem = route_rep_smem((int)T, E, k, tpb);
+    e = cudaFuncSetAttribute(route_expand_replicated_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(route_expand_replicated_kernel, blocks, kRepThreads, smem, c.stream, a, tpb);
+  }
   const size_t smem = rep_dyn_smem((int)T, E, k);
   const bool vec = (E % 128 == 0) && (reinterpret_cast<uintptr_t>(scores) % 16 == 0);
   if (E <= 64) return k <= 8 ? launch_t<2, false, 8>(c, a, blocks, smem)

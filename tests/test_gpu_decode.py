@@ -98,10 +98,11 @@ def test_back_to_back_calls_share_a_workspace():
 
 def test_path_launch_counts_and_auto_choice():
     E, k, H = 256, 8, 512
-    for T, mode, launches in [(512, ops.PATH_FUSED, 1), (512, ops.PATH_REPLICATED, 1),
-                              (512, ops.PATH_AUTO, 4), (4096, ops.PATH_AUTO, 4),
-                              (64, ops.PATH_AUTO, 1), (96, ops.PATH_AUTO, 1),
-                              (97, ops.PATH_AUTO, 4)]:
+    for T, mode, launches in [(512, ops.PATH_FUSED, 1), (512, ops.PATH_REPLICATED, 2),
+                              (32, ops.PATH_REPLICATED, 1), (33, ops.PATH_REPLICATED, 2),
+                              (4096, ops.PATH_AUTO, 4), (32, ops.PATH_AUTO, 1),
+                              (512, ops.PATH_AUTO, 2), (1024, ops.PATH_AUTO, 2),
+                              (1025, ops.PATH_AUTO, 4)]:
         scores, x = _inputs(T, E, k, H, seed=T)
         s, xd = scores.to(DEV), x.to(DEV)
         ws = ops.route_expand_cast_workspace(T, E, k, xd)
@@ -110,7 +111,7 @@ def test_path_launch_counts_and_auto_choice():
         res = ops.route_expand_cast_fp8(s, xd, k, mode=mode, workspace=ws)
         assert ops.launch_count() - n0 == launches
         assert ops.device_status() == 0
-        if T <= 512:
+        if T <= 1025:
             _check_against_oracle(scores, x, k, res)
 
 
@@ -162,9 +163,12 @@ def test_no_tokens(mode):
 
 # ---------------------------------------------------------------- replicated path
 
+# T <= 32: one launch (selection repeated per block); above: top-k launch + route/expand
 REP_CASES = [(1, 64, 2, 128), (7, 256, 8, 4096), (100, 256, 8, 7168), (33, 128, 4, 384),
              (300, 64, 6, 1024), (512, 256, 8, 512), (128, 256, 32, 256), (151, 96, 3, 640),
-             (153, 256, 8, 8192), (16, 200, 1, 128), (64, 33, 32, 256), (40, 256, 9, 2048)]
+             (153, 256, 8, 8192), (16, 200, 1, 128), (64, 33, 32, 256), (40, 256, 9, 2048),
+             (32, 256, 8, 1024), (33, 256, 8, 1024), (1024, 256, 8, 4096), (2048, 256, 8, 512),
+             (700, 256, 23, 256)]
 
 
 @pytest.mark.parametrize("T,E,k,H", REP_CASES)
@@ -200,8 +204,8 @@ def test_replicated_back_to_back_calls():
         _check_against_oracle(scores, x, k, res)
 
 
-@pytest.mark.parametrize("T,E,k,H", [(513, 256, 8, 256), (300, 256, 16, 256), (8, 16, 2, 256),
-                                     (8, 512, 8, 256), (8, 256, 8, 8320)])
+@pytest.mark.parametrize("T,E,k,H", [(2049, 256, 8, 256), (1100, 256, 16, 256), (8, 16, 2, 256),
+                                     (8, 512, 8, 256), (8, 256, 8, 8320), (300, 256, 8, 8320)])
 def test_replicated_refuses_shapes_it_does_not_handle(T, E, k, H):
     scores, x = _inputs(T, E, k, H, seed=2)
     with pytest.raises(ops.MoeError) as ei:
