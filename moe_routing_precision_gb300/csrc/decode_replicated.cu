@@ -30,6 +30,7 @@ namespace {
 
 constexpr int kRepWarps = 16;
 constexpr int kRepThreads = kRepWarps * 32;
+constexpr int kRepBatch = 8;  // ids a thread loads before their atomics (two-launch form)
 
 struct RepArgs {
   const float* scores;
@@ -202,12 +203,23 @@ __global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel
   __syncthreads();
   pdl_enter();  // the expert ids
 
-  // ---- the route map of every copy, as in the one-launch form
-  for (int p = tid; p < P; p += kRepThreads) {
-    const int e = __ldcg(a.idx + p);
-    if ((unsigned)e < (unsigned)E) {
-      const int tt = (int)a.fk.div((uint32_t)p);
-      atomicOr(bm + (tt >> 5) * E + e, 1u << (tt & 31));
+  // ---- the route map of every copy, as in the one-launch form.  The ids are
+  // loaded kRepBatch at a time before their atomics (one round of L2 latency
+  // per batch instead of one per copy).
+  for (int p0 = 0; p0 < P; p0 += kRepBatch * kRepThreads) {
+    int ev[kRepBatch];
+#pragma unroll
+    for (int u = 0; u < kRepBatch; ++u) {
+      const int p = p0 + tid + u * kRepThreads;
+      ev[u] = p < P ? __ldcg(a.idx + p) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kRepBatch; ++u) {
+      const int p = p0 + tid + u * kRepThreads;
+      if (p < P && (unsigned)ev[u] < (unsigned)E) {
+        const int tt = (int)a.fk.div((uint32_t)p);
+        atomicOr(bm + (tt >> 5) * E + ev[u], 1u << (tt & 31));
+      }
     }
   }
   __syncthreads();
