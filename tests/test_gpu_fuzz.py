@@ -1,8 +1,8 @@
 """Seeded random sweep over shapes and options, every op through the C ABI
 against the oracle: shapes the fixed parity cases do not name (odd T, E not a
 power of two, every k, H across the kernel forms, all scale layouts, every
-FP4 group size, padded alignments, decode shapes).  Each case is small enough
-for the oracle to finish at once."""
+FP4 group size, padded alignments, decode shapes on the fused and replicated
+paths).  Each case is small enough for the oracle to finish at once."""
 import numpy as np
 import pytest
 import torch
@@ -139,19 +139,23 @@ def test_fp4_and_swiglu(case):
 
 
 @pytest.mark.parametrize("case", range(CASES // 2))
-def test_decode_fused(case):
+@pytest.mark.parametrize("mode", ["fused", "replicated"])
+def test_decode_paths(case, mode):
     rng = np.random.default_rng(3000 + case)
     E = int(rng.choice([40, 64, 96, 128, 200, 256]))
     k = int(rng.integers(1, min(E, 32) + 1))
     T = int(rng.integers(1, max(2, min(2048, 16384 // k))))
     H = 128 * int(rng.integers(1, 33))
+    if mode == "replicated" and case % 3 == 0:
+        T = int(rng.integers(1, 33))          # the one-launch form
     inp = workloads.random_small(T, E, k, H, seed=case, ties=bool(rng.integers(0, 2)))
     s, x = inp["scores"], inp["x"]
+    path = ops.PATH_FUSED if mode == "fused" else ops.PATH_REPLICATED
     try:
-        res = ops.route_expand_cast_fp8(s.to(DEV), x.to(DEV), k, mode=ops.PATH_FUSED)
-    except ops.MoeError as e:               # shared memory beyond the fused form's budget
+        res = ops.route_expand_cast_fp8(s.to(DEV), x.to(DEV), k, mode=path)
+    except ops.MoeError as e:               # a shape outside the form's limits
         assert e.rc == ops.MOE_ERR_UNSUPPORTED
-        pytest.skip("shape outside the fused form")
+        pytest.skip(f"shape outside the {mode} form")
     assert ops.device_status() == 0
     o_idx, o_w = oracle.topk_gate(s.numpy(), k)
     o_c, o_o, o_p, o_s = oracle.route_map(o_idx, E)
