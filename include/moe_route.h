@@ -155,7 +155,10 @@ size_t moe_route_map_workspace_bytes(int64_t num_tokens, int32_t num_experts,
  * Rows of one expert are therefore in ascending token order.
  *   workspace: at least moe_route_map_workspace_bytes(...) bytes of device
  *   memory, 16-byte aligned; contents on entry are ignored; it is busy until
- *   the work enqueued on `stream` completes.
+ *   the work enqueued on `stream` completes.  (For T <= 1024, E <= 256 and
+ *   T*k <= 16384 the map is built in one launch in which every block builds
+ *   it in shared memory and writes its own tokens' entries; the workspace is
+ *   then not touched.  Otherwise a histogram launch and a rank launch.)
  * Each token's k experts must be distinct (as moe_topk_gate produces them); a
  * repeated expert sets MOE_DEVERR_DUPLICATE_EXPERT and leaves that token's
  * results unspecified (no write leaves the output buffers).  An index outside

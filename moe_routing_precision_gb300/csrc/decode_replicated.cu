@@ -176,9 +176,12 @@ size_t route_rep_smem(int T, int E, int k, int tpb) {
 
 // The second launch of the two-launch form: a.idx holds the top-k launch's
 // expert ids.  Every block builds the route map of all T*k copies in its own
-// shared memory, then takes its tokens t = blockIdx.x + i * gridDim.x.
-__global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel(RepArgs a,
-                                                                               int tpb) {
+// shared memory, then takes its tokens t = blockIdx.x + i * gridDim.x.  With
+// EXPAND = false it is the route map alone (moe_route_map for small T, where
+// the ids may come from anywhere: a token naming one expert twice is
+// flagged, as the two-kernel route map does).
+template <bool EXPAND>
+__global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel(RepArgs a) {
   __shared__ int s_scan[2 * 32];
   extern __shared__ __align__(16) int32_t s_dyn[];
   const int T = a.T, E = a.E, k = a.k, H = a.H;
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel
   // this one start, so x (an input of both) is complete here.
   int t = blockIdx.x;
   uint4 va = make_uint4(0, 0, 0, 0), vb = va;
-  if (t < T && act) {
+  if (EXPAND && t < T && act) {
     va = ld_stream_v4(a.x + (int64_t)t * H + tid * 16);
     vb = ld_stream_v4(a.x + (int64_t)t * H + tid * 16 + 8);
   }
@@ -206,6 +209,7 @@ __global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel
   // ---- the route map of every copy, as in the one-launch form.  The ids are
   // loaded kRepBatch at a time before their atomics (one round of L2 latency
   // per batch instead of one per copy).
+  bool dup = false;
   for (int p0 = 0; p0 < P; p0 += kRepBatch * kRepThreads) {
     int ev[kRepBatch];
 #pragma unroll
@@ -218,10 +222,12 @@ __global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel
       const int p = p0 + tid + u * kRepThreads;
       if (p < P && (unsigned)ev[u] < (unsigned)E) {
         const int tt = (int)a.fk.div((uint32_t)p);
-        atomicOr(bm + (tt >> 5) * E + ev[u], 1u << (tt & 31));
+        const uint32_t bit = 1u << (tt & 31);
+        dup |= (atomicOr(bm + (tt >> 5) * E + ev[u], bit) & bit) != 0u;
       }
     }
   }
+  if (dup && b0) flag_error(a.err, MOE_DEVERR_DUPLICATE_EXPERT);
   __syncthreads();
   int total = 0;
   if (tid < E) {
@@ -247,7 +253,11 @@ __global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel
       a.offsets[tid] = excl;
     }
   }
-  if (b0 && tid == 0) a.offsets[E] = s_scan[32 + kRepWarps - 1] + s_scan[kRepWarps - 1];
+  if (b0) {
+    const int all = s_scan[32 + kRepWarps - 1] + s_scan[kRepWarps - 1];  // copies counted
+    if (tid == 0) a.offsets[E] = all;
+    for (int r = all + tid; r < P; r += kRepThreads) a.src[r] = -1;  // rows no copy takes
+  }
   __syncthreads();
   // ---- this block's copies: their rows, pos and sorted_src entries
   const int nt = (T - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // tokens here
@@ -269,6 +279,7 @@ __global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel
     a.pos[p] = r;
   }
   if (bad) flag_error(a.err, MOE_DEVERR_EXPERT_RANGE);
+  if (!EXPAND) return;
   __syncthreads();
 
   // ---- cast once, write k rows, as in the one-launch form
@@ -292,7 +303,6 @@ __global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel
       }
     }
   }
-  (void)tpb;
 }
 
 template <int V, bool VEC, int KMAX>
@@ -339,10 +349,11 @@ cudaError_t launch_decode_replicated(const LaunchCtx& c, const float* scores, in
     if (e != cudaSuccess) return e;
     const int tpb = (int)((T + blocks - 1) / blocks);
     const size_t smem = route_rep_smem((int)T, E, k, tpb);
-    e = cudaFuncSetAttribute(route_expand_replicated_kernel,
+    e = cudaFuncSetAttribute(route_expand_replicated_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(route_expand_replicated_kernel, blocks, kRepThreads, smem, c.stream, a, tpb);
+    return launch_pdl(route_expand_replicated_kernel<true>, blocks, kRepThreads, smem, c.stream,
+                      a);
   }
   const size_t smem = rep_dyn_smem((int)T, E, k);
   const bool vec = (E % 128 == 0) && (reinterpret_cast<uintptr_t>(scores) % 16 == 0);
@@ -358,6 +369,35 @@ cudaError_t launch_decode_replicated(const LaunchCtx& c, const float* scores, in
                          : launch_t<8, true, 32>(c, a, blocks, smem);
   return k <= 8 ? launch_t<8, false, 8>(c, a, blocks, smem)
                 : launch_t<8, false, 32>(c, a, blocks, smem);
+}
+
+bool route_map_replicated_ok(int64_t T, int E, int k) {
+  return T >= 1 && T <= kRouteMapReplicatedMaxTokens && E >= 1 && E <= 256 && T * k <= 16384;
+}
+
+cudaError_t launch_route_map_replicated(const LaunchCtx& c, const int32_t* idx, int64_t T, int E,
+                                        int k, int32_t* counts, int32_t* offsets, int32_t* pos,
+                                        int32_t* src) {
+  if (!route_map_replicated_ok(T, E, k)) return cudaErrorInvalidValue;
+  RepArgs a = {};
+  a.idx = const_cast<int32_t*>(idx);  // read only
+  a.counts = counts;
+  a.offsets = offsets;
+  a.pos = pos;
+  a.src = src;
+  a.err = c.err;
+  a.T = (int)T;
+  a.E = E;
+  a.k = k;
+  a.H = 0;
+  a.fk = FastDiv((uint32_t)k);
+  const int blocks = (int)(T < c.num_sms ? T : c.num_sms);
+  const int tpb = (int)((T + blocks - 1) / blocks);
+  const size_t smem = route_rep_smem((int)T, E, k, tpb);
+  cudaError_t e = cudaFuncSetAttribute(route_expand_replicated_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(route_expand_replicated_kernel<false>, blocks, kRepThreads, smem, c.stream, a);
 }
 
 }  // namespace moe

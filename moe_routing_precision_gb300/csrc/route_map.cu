@@ -276,6 +276,9 @@ cudaError_t launch_route_map_aligned(const LaunchCtx& c, const int32_t* idx, int
 cudaError_t launch_route_map(const LaunchCtx& c, const int32_t* idx, int64_t T, int E, int k,
                              int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* sorted_src,
                              int32_t* ws, int64_t num_chunks) {
+  // small T: one launch in which every block builds the whole map itself
+  if (route_map_replicated_ok(T, E, k))
+    return launch_route_map_replicated(c, idx, T, E, k, counts, offsets, pos, sorted_src);
   return launch_route_map_aligned(c, idx, T, E, k, 1, T * k, counts, offsets, pos, sorted_src, ws,
                                   num_chunks);
 }

@@ -102,7 +102,7 @@ def test_path_launch_counts_and_auto_choice():
                               (32, ops.PATH_REPLICATED, 1), (33, ops.PATH_REPLICATED, 2),
                               (4096, ops.PATH_AUTO, 4), (32, ops.PATH_AUTO, 1),
                               (512, ops.PATH_AUTO, 2), (1024, ops.PATH_AUTO, 2),
-                              (1025, ops.PATH_AUTO, 4)]:
+                              (1025, ops.PATH_AUTO, 4), (1024, ops.PATH_SEPARATE, 3)]:
         scores, x = _inputs(T, E, k, H, seed=T)
         s, xd = scores.to(DEV), x.to(DEV)
         ws = ops.route_expand_cast_workspace(T, E, k, xd)
