@@ -432,7 +432,8 @@ moe_status_t moe_combine(const void *y, const float *topk_weights,
  * all T tokens (block 0 writes idx, w, counts and offsets); above, the top-k
  * kernel runs first and a second launch does the rest.  It applies to
  * T <= 2048, T*k <= 16384, 32 < E <= 256, k <= 32, H <= 8192.  The SEPARATE
- * path is the four launches of the individual calls.
+ * path is the launches of the individual calls (three or four: the route map
+ * is one launch for T <= 1024).
  *   scores [T,E] f32; x [T,H] bf16; topk_idx [T,k] i32; topk_weights [T,k]
  *   f32; counts [E], offsets [E+1], pos [T,k], sorted_src [T*k] i32;
  *   out [T*k,H] u8; out_sf [T*k,H/128] f32.
