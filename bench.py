@@ -843,7 +843,7 @@ def cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak):
 
 def decode_workload(L, dev, stream, sp, chk, flush, iters, peak, T=1024):
     """route + expand + cast of a decode batch of T tokens (E=256, k=8,
-    H=4096, the decode_1k recipe) through moe_route_expand_cast_fp8: the four
+    H=4096, the decode_1k recipe) through moe_route_expand_cast_fp8: the
     separate launches (chained by programmatic dependent launch; three up to
     T = 1024, where the route map is one launch, else four), the same
     captured in a CUDA graph, the fused single cooperative launch, and the
