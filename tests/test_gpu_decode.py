@@ -168,7 +168,7 @@ REP_CASES = [(1, 64, 2, 128), (7, 256, 8, 4096), (100, 256, 8, 7168), (33, 128, 
              (300, 64, 6, 1024), (512, 256, 8, 512), (128, 256, 32, 256), (151, 96, 3, 640),
              (153, 256, 8, 8192), (16, 200, 1, 128), (64, 33, 32, 256), (40, 256, 9, 2048),
              (32, 256, 8, 1024), (33, 256, 8, 1024), (1024, 256, 8, 4096), (2048, 256, 8, 512),
-             (700, 256, 23, 256)]
+             (700, 256, 23, 256), (500, 40, 5, 128), (500, 33, 32, 256)]
 
 
 @pytest.mark.parametrize("T,E,k,H", REP_CASES)
