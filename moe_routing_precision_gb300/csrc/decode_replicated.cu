@@ -1,28 +1,25 @@
 // decode_replicated.cu -- top-k gate, route map and expand + E4M3 cast of a
-// small decode batch in ONE ordinary launch with no communication between
-// blocks.
+// decode batch with no communication between blocks, and the route map alone
+// for small T.
 //
 // "CuTeDSL at Perplexity" (perplexity.ai), the prefill/decode section: decode
 // kernels run at launch latency, so the fewer dependent launches the better;
 // the MoE dispatch section routes with shared-memory counters.  Here every
-// block selects the experts of ALL T tokens and builds the whole route map in
-// its own shared memory (T*k <= 4096 copies), then casts and writes only its
-// own tokens' rows.  The selection is repeated by every block, which is cheap
-// for small T (T / 16 tokens per warp); in exchange there is no grid barrier,
-// no wait on another block and no cooperative launch, and the launch takes
-// part in programmatic dependent launch like the separate kernels.  Block 0
-// also writes idx, w, counts, offsets, pos and sorted_src.
+// block builds the whole route map in its own shared memory (per-expert
+// 32-token bitmaps and popcount ranks), then handles only its own tokens:
+// their pos and sorted_src entries, and their cast rows.  There is no grid
+// barrier, no wait on another block and no cooperative launch; every launch
+// takes part in programmatic dependent launch like the separate kernels.
 //
-// For larger T the selection is not repeated: the top-k kernel runs first
-// (all SMs, once), and a second launch repeats only the route map in every
-// block, from the T*k expert ids in L2, positions its own tokens' copies
-// (writing their pos and sorted_src entries), and casts and writes their
-// rows.
+//   * T <= 32: one launch; every block also selects the experts of all T
+//     tokens (T / 16 per warp), block 0 writing idx, w, counts and offsets.
+//   * larger T (to 2048): the top-k kernel runs first (once, on all SMs), then
+//     one launch builds the map in every block from the T*k ids in L2.
+//   * the same kernel without the expand is moe_route_map for T <= 1024.
 //
 // Results are those of moe_topk_gate + moe_route_map + moe_expand_cast_fp8:
 // the same top-k routine, the route map's stable order (copies of one expert
-// in ascending token order, from per-expert 32-token bitmaps and popcounts),
-// and the same scale arithmetic.
+// in ascending token order), and the same scale arithmetic.
 #include "topk_warp.cuh"
 
 namespace moe {
