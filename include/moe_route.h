@@ -109,7 +109,7 @@ typedef enum moe_out_dtype {
 #define MOE_PATH_FUSED 1      /* one cooperative launch (decode shapes only)              */
 #define MOE_PATH_SEPARATE 2   /* moe_topk_gate + moe_route_map + moe_expand_cast_fp8     */
 #define MOE_PATH_REPLICATED 3 /* one ordinary launch, routing repeated per block (small T) */
-#define MOE_AUTO_REPLICATED_MAX_TOKENS 512  /* AUTO's switch from REPLICATED to SEPARATE  */
+#define MOE_AUTO_REPLICATED_MAX_TOKENS 1024 /* AUTO's switch from REPLICATED to SEPARATE  */
 
 /*
  * moe_topk_gate -- [TK] 2.1 Top-K Gating, plus the "Weight Normalization" that
@@ -446,13 +446,14 @@ moe_status_t moe_combine(const void *y, const float *topk_weights,
  *   (MOE_ERR_UNSUPPORTED where they do not apply) or MOE_PATH_SEPARATE.  AUTO
  *   takes the path measured fastest on GB300 for the shape: REPLICATED for
  *   T <= MOE_AUTO_REPLICATED_MAX_TOKENS where it applies (E = 256, k = 8,
- *   H = 4096, one call: 8.8 against 16.0 us at T = 16, 10.9 against 12.9 at
- *   T = 128, 14.9 against 16.5 at T = 512; from T = 640 the separate
- *   launches, whose route map is itself one launch up to T = 1024, are as
- *   fast or faster), else SEPARATE (the separate launches, chained by
- *   programmatic dependent launch, were as fast as the FUSED launch for
- *   T <= 64 and faster above: its single routing block and the cooperative
- *   launch cost more than the gaps they remove).
+ *   H = 4096, one call: 8.8 against 14.0 us at T = 16, 12.9 against 14.0 at
+ *   T = 256, 15.0 against 16.0 at T = 512, 17.0 against 18.0 at T = 768,
+ *   20.1 against 20.1 at T = 1024 (14.2 against 14.6 back to back); at
+ *   T = 2048 the separate launches are faster back to back), else SEPARATE
+ *   (the separate launches, chained by programmatic dependent launch, were
+ *   as fast as the FUSED launch for T <= 64 and faster above: its single
+ *   routing block and the cooperative launch cost more than the gaps they
+ *   remove).
  * Requirements as the individual calls; group == 128.
  */
 moe_status_t moe_route_expand_cast_fp8(const float *scores, int64_t num_tokens,

@@ -52,14 +52,71 @@ size_t rep_dyn_smem(int T, int E, int k) {
   return 4 * (2 * P + E) + 4 * W * E + ((2 * W * E + 15) / 16) * 16;
 }
 
+// The block's own tokens are t = blockIdx.x + i * gridDim.x, i < own_tokens().
+// H/16 threads cast one token (16 channels each; an 8-lane group is one
+// 128-channel group), so kRepThreads / (H/16) tokens go at a time.
+__device__ __forceinline__ int own_tokens(int T) {
+  return (T - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+}
+
+// The first x loads of this thread's first own token.
+__device__ __forceinline__ void own_first_loads(const RepArgs& a, uint4& va, uint4& vb) {
+  const int P16 = a.H >> 4, slot = (int)threadIdx.x / P16, c = (int)threadIdx.x - slot * P16;
+  va = make_uint4(0, 0, 0, 0);
+  vb = va;
+  if (slot < kRepThreads / P16 && slot < own_tokens(a.T)) {
+    const int64_t t = (int64_t)blockIdx.x + (int64_t)slot * gridDim.x;
+    va = ld_stream_v4(a.x + t * a.H + c * 16);
+    vb = ld_stream_v4(a.x + t * a.H + c * 16 + 8);
+  }
+}
+
+// Cast the block's own tokens once each and write their k rows.  The row of
+// copy j of own token i (token t) is s_pos[OWN ? i * k + j : t * k + j].
+// Every thread runs the same number of iterations (the group maxima shuffle
+// across lanes); va/vb hold the first token's loads (own_first_loads).
+template <bool OWN>
+__device__ __forceinline__ void cast_own_tokens(const RepArgs& a, const int32_t* s_pos, uint4 va,
+                                                uint4 vb) {
+  const int H = a.H, k = a.k, G = H >> 7, P = a.T * k;
+  const int P16 = H >> 4, per = kRepThreads / P16;
+  const int slot = (int)threadIdx.x / P16, c = (int)threadIdx.x - slot * P16;
+  const int nt = own_tokens(a.T);
+  const int iters = (nt + per - 1) / per;
+  for (int it = 0; it < iters; ++it) {
+    const int i = it * per + slot;
+    const int t = (int)blockIdx.x + i * (int)gridDim.x;
+    const bool live = slot < per && i < nt;
+    const uint4 ca = va, cb = vb;
+    const int in = i + per;
+    if (slot < per && in < nt) {  // the next token's loads stay in flight during this one
+      const int64_t tn = (int64_t)blockIdx.x + (int64_t)in * gridDim.x;
+      va = ld_stream_v4(a.x + tn * H + c * 16);
+      vb = ld_stream_v4(a.x + tn * H + c * 16 + 8);
+    }
+    const float amax = max8(absmax16_bf16(ca, cb));  // every lane: shuffles over 8 lanes
+    const float sf = group_scale(amax);
+    const float inv = __fdiv_rn(1.0f, sf);
+    const uint4 q = quant16_bf16(ca, cb, inv);
+    if (live) {
+      for (int j = 0; j < k; ++j) {
+        const int r = s_pos[OWN ? i * k + j : t * k + j];
+        if (r < 0 || r >= P) continue;
+        st_stream_v4(a.out + (int64_t)r * H + c * 16, q);
+        if ((c & 7) == 0) st_stream_f32(a.out_sf + (int64_t)r * G + (c >> 3), sf);
+      }
+    }
+  }
+}
+
 template <int V, bool VEC, int KMAX>
 __global__ void __launch_bounds__(kRepThreads, 1) decode_replicated_kernel(RepArgs a) {
   __shared__ unsigned long long s_list[kRepWarps][V][32];
   __shared__ unsigned long long s_cand[kRepWarps][32];
   __shared__ int s_scan[2 * 32];  // warp totals, then exclusive warp prefixes
   extern __shared__ __align__(16) int32_t s_dyn[];
-  const int T = a.T, E = a.E, k = a.k, H = a.H;
-  const int P = T * k, W = (T + 31) >> 5, G = H >> 7;
+  const int T = a.T, E = a.E, k = a.k;
+  const int P = T * k, W = (T + 31) >> 5;
   int32_t* s_idx = s_dyn;
   int32_t* s_pos = s_idx + P;
   int32_t* s_off = s_pos + P;
@@ -68,15 +125,9 @@ __global__ void __launch_bounds__(kRepThreads, 1) decode_replicated_kernel(RepAr
   pdl_enter();
   const int tid = threadIdx.x, lane = tid & 31, wib = tid >> 5;
   const bool b0 = blockIdx.x == 0;
-  const bool act = tid < (H >> 4);  // 16 channels per thread (H <= 8192)
-
-  // this block's first token: its loads go out before the selection
-  int t = blockIdx.x;
-  uint4 va = make_uint4(0, 0, 0, 0), vb = va;
-  if (t < T && act) {
-    va = ld_stream_v4(a.x + (int64_t)t * H + tid * 16);
-    vb = ld_stream_v4(a.x + (int64_t)t * H + tid * 16 + 8);
-  }
+  // this block's first tokens: their loads go out before the selection
+  uint4 va, vb;
+  own_first_loads(a, va, vb);
   for (int i = tid; i < W * E; i += kRepThreads) bm[i] = 0u;
 
   // ---- 1: the experts of every token (block 0: also the weights)
@@ -142,26 +193,7 @@ __global__ void __launch_bounds__(kRepThreads, 1) decode_replicated_kernel(RepAr
   __syncthreads();
 
   // ---- 3: this block's tokens, cast once and written to their k rows
-  for (; t < T; t += gridDim.x) {
-    const uint4 ca = va, cb = vb;
-    const int tn = t + gridDim.x;
-    if (tn < T && act) {  // the next token's loads stay in flight during this one
-      va = ld_stream_v4(a.x + (int64_t)tn * H + tid * 16);
-      vb = ld_stream_v4(a.x + (int64_t)tn * H + tid * 16 + 8);
-    }
-    const float amax = max8(absmax16_bf16(ca, cb));  // every lane: shuffles over 8 lanes
-    const float sf = group_scale(amax);
-    const float inv = __fdiv_rn(1.0f, sf);
-    const uint4 q = quant16_bf16(ca, cb, inv);
-    if (act) {
-      for (int j = 0; j < k; ++j) {
-        const int r = s_pos[t * k + j];
-        if (r < 0 || r >= P) continue;
-        st_stream_v4(a.out + (int64_t)r * H + tid * 16, q);
-        if ((tid & 7) == 0) st_stream_f32(a.out_sf + (int64_t)r * G + (tid >> 3), sf);
-      }
-    }
-  }
+  cast_own_tokens<false>(a, s_pos, va, vb);
 }
 
 // Shared memory of the route-only kernel: offsets [E], bitmaps [W][E] u32,
@@ -181,24 +213,19 @@ template <bool EXPAND>
 __global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel(RepArgs a) {
   __shared__ int s_scan[2 * 32];
   extern __shared__ __align__(16) int32_t s_dyn[];
-  const int T = a.T, E = a.E, k = a.k, H = a.H;
-  const int P = T * k, W = (T + 31) >> 5, G = H >> 7;
+  const int T = a.T, E = a.E, k = a.k;
+  const int P = T * k, W = (T + 31) >> 5;
   int32_t* s_off = s_dyn;
   uint32_t* bm = reinterpret_cast<uint32_t*>(s_off + E);
   uint16_t* pre = reinterpret_cast<uint16_t*>(bm + W * E);
   int32_t* s_pos = reinterpret_cast<int32_t*>(pre + ((W * E + 7) & ~7));
   const int tid = threadIdx.x, lane = tid & 31, wib = tid >> 5;
   const bool b0 = blockIdx.x == 0;
-  const bool act = tid < (H >> 4);
-  // This block's first token: x is read before the wait for the top-k launch.
-  // That launch itself waited for every earlier kernel before it could let
-  // this one start, so x (an input of both) is complete here.
-  int t = blockIdx.x;
+  // This block's first tokens: x is read before the wait for the top-k
+  // launch.  That launch itself waited for every earlier kernel before it
+  // could let this one start, so x (an input of both) is complete here.
   uint4 va = make_uint4(0, 0, 0, 0), vb = va;
-  if (EXPAND && t < T && act) {
-    va = ld_stream_v4(a.x + (int64_t)t * H + tid * 16);
-    vb = ld_stream_v4(a.x + (int64_t)t * H + tid * 16 + 8);
-  }
+  if (EXPAND) own_first_loads(a, va, vb);
   for (int i = tid; i < W * E; i += kRepThreads) bm[i] = 0u;
   __syncthreads();
   pdl_enter();  // the expert ids
@@ -280,26 +307,7 @@ __global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel
   __syncthreads();
 
   // ---- cast once, write k rows, as in the one-launch form
-  for (int i = 0; t < T; t += gridDim.x, ++i) {
-    const uint4 ca = va, cb = vb;
-    const int tn = t + gridDim.x;
-    if (tn < T && act) {
-      va = ld_stream_v4(a.x + (int64_t)tn * H + tid * 16);
-      vb = ld_stream_v4(a.x + (int64_t)tn * H + tid * 16 + 8);
-    }
-    const float amax = max8(absmax16_bf16(ca, cb));
-    const float sf = group_scale(amax);
-    const float inv = __fdiv_rn(1.0f, sf);
-    const uint4 q = quant16_bf16(ca, cb, inv);
-    if (act) {
-      for (int j = 0; j < k; ++j) {
-        const int r = s_pos[i * k + j];
-        if (r < 0 || r >= P) continue;
-        st_stream_v4(a.out + (int64_t)r * H + tid * 16, q);
-        if ((tid & 7) == 0) st_stream_f32(a.out_sf + (int64_t)r * G + (tid >> 3), sf);
-      }
-    }
-  }
+  cast_own_tokens<true>(a, s_pos, va, vb);
 }
 
 template <int V, bool VEC, int KMAX>

@@ -101,7 +101,7 @@ def test_path_launch_counts_and_auto_choice():
     for T, mode, launches in [(512, ops.PATH_FUSED, 1), (512, ops.PATH_REPLICATED, 2),
                               (32, ops.PATH_REPLICATED, 1), (33, ops.PATH_REPLICATED, 2),
                               (4096, ops.PATH_AUTO, 4), (32, ops.PATH_AUTO, 1),
-                              (512, ops.PATH_AUTO, 2), (513, ops.PATH_AUTO, 3),
+                              (512, ops.PATH_AUTO, 2), (1024, ops.PATH_AUTO, 2),
                               (1025, ops.PATH_AUTO, 4), (1024, ops.PATH_SEPARATE, 3)]:
         scores, x = _inputs(T, E, k, H, seed=T)
         s, xd = scores.to(DEV), x.to(DEV)
