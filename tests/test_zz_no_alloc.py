@@ -67,7 +67,8 @@ def _no_alloc(L, idx, E):
 
 def test_noalloc_matches_route_map_on_two_calls_in_a_row(L):
     problems = [(65536, 256, 8, 1, True),     # prefill-sized, skewed (512 KiB of scratch)
-                (5000, 64, 6, 2, False)]      # a smaller problem right after it
+                (5000, 64, 6, 2, False),      # a smaller problem right after it
+                (300, 128, 4, 3, False)]      # decode-sized: the one-launch map, no scratch
     results = []
     for T, E, k, seed, skew in problems:
         idx = _idx(T, E, k, seed, skew)
