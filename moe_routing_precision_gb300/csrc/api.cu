@@ -63,6 +63,36 @@ bool experts_ok(int32_t E, int32_t k) {
 
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+cudaError_t allow_max_dynamic_smem(const void* kernel) {
+  // the cap per kernel, computed once per process (every GPU here is the same part)
+  static std::mutex mu;
+  static const void* keys[64];
+  static int caps[64];
+  static int n = 0;
+  int cap = -1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+      if (keys[i] == kernel) cap = caps[i];
+  }
+  if (cap < 0) {
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    cap = optin - (int)fa.sharedSizeBytes;
+    std::lock_guard<std::mutex> lock(mu);
+    if (n < 64) {
+      keys[n] = kernel;
+      caps[n] = cap;
+      ++n;
+    }
+  }
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, cap);
+}
+
 }  // namespace moe
 
 using namespace moe;

@@ -431,6 +431,18 @@ inline int64_t route_num_chunks(int64_t T) {
 // Kernel launch counter (api.cu).
 void count_launches(int n);
 
+// Let `kernel` take any dynamic shared memory a block can opt in to (the
+// device's opt-in maximum minus the kernel's static shared memory; api.cu).
+// Every call sets the same value for a kernel, so calls from several host
+// threads cannot undo one another, as a per-call size could (a smaller value
+// landing between another thread's set and its launch).  The cap does not
+// change what a launch uses: that is the launch's own size.
+cudaError_t allow_max_dynamic_smem(const void* kernel);
+template <typename... KArgs>
+inline cudaError_t allow_max_dynamic_smem(void (*kernel)(KArgs...)) {
+  return allow_max_dynamic_smem(reinterpret_cast<const void*>(kernel));
+}
+
 // Launch `kernel` on `stream` with programmatic stream serialization (see
 // pdl_enter) and count it.
 template <typename... KArgs, typename... Args>

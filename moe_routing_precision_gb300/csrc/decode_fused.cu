@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(DecodeArgs
 template <int V, bool VEC, int KMAX>
 cudaError_t launch_t(const LaunchCtx& c, const DecodeArgs& a, int blocks, size_t smem) {
   auto kern = decode_fused_kernel<V, VEC, KMAX>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_max_dynamic_smem(kern);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecThreads, smem);

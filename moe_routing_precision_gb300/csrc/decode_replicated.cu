@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel
 template <int V, bool VEC, int KMAX>
 cudaError_t launch_t(const LaunchCtx& c, const RepArgs& a, int blocks, size_t smem) {
   auto kern = decode_replicated_kernel<V, VEC, KMAX>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_max_dynamic_smem(kern);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, blocks, kRepThreads, smem, c.stream, a);
 }
@@ -354,8 +354,7 @@ cudaError_t launch_decode_replicated(const LaunchCtx& c, const float* scores, in
     if (e != cudaSuccess) return e;
     const int tpb = (int)((T + blocks - 1) / blocks);
     const size_t smem = route_rep_smem((int)T, E, k, tpb);
-    e = cudaFuncSetAttribute(route_expand_replicated_kernel<true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = allow_max_dynamic_smem(route_expand_replicated_kernel<true>);
     if (e != cudaSuccess) return e;
     return launch_pdl(route_expand_replicated_kernel<true>, blocks, kRepThreads, smem, c.stream,
                       a);
@@ -399,8 +398,7 @@ cudaError_t launch_route_map_replicated(const LaunchCtx& c, const int32_t* idx, 
   const int blocks = (int)(T < c.num_sms ? T : c.num_sms);
   const int tpb = (int)((T + blocks - 1) / blocks);
   const size_t smem = route_rep_smem((int)T, E, k, tpb);
-  cudaError_t e = cudaFuncSetAttribute(route_expand_replicated_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_max_dynamic_smem(route_expand_replicated_kernel<false>);
   if (e != cudaSuccess) return e;
   return launch_pdl(route_expand_replicated_kernel<false>, blocks, kRepThreads, smem, c.stream, a);
 }

@@ -378,8 +378,7 @@ cudaError_t launch_bulk(const LaunchCtx& c, const void* x, int64_t T, int H, int
   const size_t stride = (size_t)(H + 4 * G + 127) / 128 * 128;
   const size_t smem = stride * NBUF + sizeof(int32_t) * 32 * NBUF;  // + per-buffer destinations
   if (smem > 48 * 1024) {
-    cudaError_t st = cudaFuncSetAttribute(expand_cast_bulk_kernel<NBUF>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t st = allow_max_dynamic_smem(expand_cast_bulk_kernel<NBUF>);
     if (st != cudaSuccess) return st;
   }
   const int64_t cap = (int64_t)c.num_sms * ctas_per_sm;

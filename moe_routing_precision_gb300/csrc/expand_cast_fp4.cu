@@ -172,8 +172,7 @@ cudaError_t launch_lt(const LaunchCtx& c, const void* x, int64_t T, int H, int k
   const size_t stride = (size_t)(H / 2 + 4 * G + 127) / 128 * 128;
   const size_t smem = (stride + sizeof(int32_t) * 32) * NBUF * TPI;
   if (smem > 48 * 1024) {
-    cudaError_t st = cudaFuncSetAttribute(expand_cast_fp4_kernel<L, NBUF, TPI>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t st = allow_max_dynamic_smem(expand_cast_fp4_kernel<L, NBUF, TPI>);
     if (st != cudaSuccess) return st;
   }
   const int sf_bulk = (sfo.flags == 0 && sfo.stage == nullptr && G % 4 == 0 &&

@@ -264,8 +264,7 @@ cudaError_t launch_route_map_aligned(const LaunchCtx& c, const int32_t* idx, int
   if (st != cudaSuccess) return st;
   const size_t rank_smem = sizeof(int32_t) * (size_t)E * (2 + 2 * kRankWarps);
   if (rank_smem > 48 * 1024) {
-    st = cudaFuncSetAttribute(route_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)rank_smem);
+    st = allow_max_dynamic_smem(route_rank_kernel);
     if (st != cudaSuccess) return st;
   }
   return launch_pdl(route_rank_kernel, (unsigned)num_chunks, kRankThreads, rank_smem, c.stream,

@@ -2,8 +2,10 @@
 with its own buffers (the header allows calls on distinct streams to run
 concurrently): every result must equal what the same call gives alone, the
 launch counter must count every launch, and the device error word stays 0.
-The fused decode launch is not run concurrently (it is a cooperative launch;
-nothing here depends on how two of them would share the SMs)."""
+Each thread also runs a decode-sized call of a different size, so that the
+threads launch one kernel with different amounts of dynamic shared memory at
+once.  The fused decode launch is not run concurrently (it is a cooperative
+launch; nothing here depends on how two of them would share the SMs)."""
 import threading
 
 import pytest
@@ -36,15 +38,18 @@ def _inputs(seed):
     return [t.to(DEV) for t in (inp["scores"], inp["x"], y, xs)]
 
 
-def _chain(scores, x, y, xs):
-    """Every op once on the current stream; returns all outputs."""
+def _chain(scores, x, y, xs, t_dec):
+    """Every op once on the current stream; returns all outputs.  t_dec: the
+    token count of a decode-sized call (a different one per thread, so the
+    threads' launches need different amounts of shared memory)."""
     idx, w = ops.topk_gate(scores, K)
     counts, offsets, pos, src = ops.route_map(idx, E)
     q, sf = ops.expand_cast_fp8(x, pos)
     out = ops.combine(y, w, pos, torch.float32)
     q2, sf2 = ops.swiglu_cast_fp8(xs)
     q4, sf4 = ops.expand_cast_fp4(x, pos, group=32)
-    return [idx, w, counts, offsets, pos, src, q, sf, out, q2, sf2, q4, sf4]
+    dec = ops.route_expand_cast_fp8(scores[:t_dec].contiguous(), x[:t_dec].contiguous(), K)
+    return [idx, w, counts, offsets, pos, src, q, sf, out, q2, sf2, q4, sf4, *dec]
 
 
 def _same(a, b):
@@ -54,11 +59,13 @@ def _same(a, b):
 
 def test_threads_on_distinct_streams_match_serial_results():
     inputs = [_inputs(100 + i) for i in range(THREADS)]
+    t_dec = [100 + 300 * i for i in range(THREADS)]   # 100, 400, 700, 1000 tokens
     n0 = ops.launch_count()
-    ref = [[t.clone() for t in _chain(*inp)] for inp in inputs]
+    ref = [[t.clone() for t in _chain(*inp, td)] for inp, td in zip(inputs, t_dec)]
     torch.cuda.synchronize()
-    per_chain = (ops.launch_count() - n0) // THREADS
-    assert per_chain > 0
+    total = ops.launch_count() - n0   # every thread's chain makes the same launches
+    assert total > 0 and total % THREADS == 0
+    per_chain = total // THREADS
 
     errors = []
     start = threading.Barrier(THREADS)
@@ -70,7 +77,7 @@ def test_threads_on_distinct_streams_match_serial_results():
             start.wait()
             with torch.cuda.stream(stream):
                 for it in range(ITERS):
-                    got = _chain(*inputs[i])
+                    got = _chain(*inputs[i], t_dec[i])
                     stream.synchronize()
                     for j, (a, b) in enumerate(zip(got, ref[i])):
                         if not _same(a, b):
