@@ -487,12 +487,36 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
     barrier()
     ms = maxr(a.elapsed_time(b) / steps)
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    # the host link on its own, for context: the largest output alone back to
+    # pinned host memory, and x alone to the device (best of 3 each)
+    qd, qh = slots[0]["q"], h_outs[0][out_names.index("q")]
+
+    def copy_ms(dst, src):
+        best = float("inf")
+        for _ in range(3):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        return best
+
+    d2h_gbs = qd.numel() / (copy_ms(qh, qd) * 1e-3) / 1e9
+    h2d_gbs = h_x.numel() * 2 / (copy_ms(slots[0]["x"], h_x) * 1e-3) / 1e9
+    bound_ms = max(d2h / (d2h_gbs * 1e9), h2d / (h2d_gbs * 1e9)) * 1e3
     del slots, h_outs
     if cpus and old_aff is not None:
         os.sched_setaffinity(0, old_aff)
     return {"value": round(R * world / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
             "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "host_numa_node": node,
+            "link": {"d2h_GB_s": round(d2h_gbs, 1), "h2d_GB_s": round(h2d_gbs, 1),
+                     "copy_bound_ms_per_step": round(bound_ms, 3),
+                     "note": "one direction at a time, best of 3; the step's copies cannot "
+                             "finish sooner than the slower direction allows"},
             "path": "pinned host -> device, C ABI topk_gate/route_map/expand_cast_fp8, "
                     "all outputs -> pinned host; steps alternate between two streams"}
 
