@@ -218,8 +218,10 @@ moe_status_t moe_route_map_aligned(const int32_t *topk_idx, int64_t num_tokens,
  * - All calls share the one array.  Nothing in it needs clearing (each call
  *   writes every entry it reads), but calls that overlap on the GPU (other
  *   streams, other threads) race on it and give wrong results: serialise them.
- * - Expert indices outside [0, E) are skipped (their pos is -1) but, unlike
- *   moe_route_map, not reported through moe_get_device_status.
+ * - Argument checks, including 4-byte alignment of every array, and data
+ *   errors are those of moe_route_map: an expert index outside [0, E) or a
+ *   token naming one expert twice sets its bit in the device error word that
+ *   moe_get_device_status reports.
  */
 #define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (1u << 20)
 moe_status_t moe_route_map_noalloc(const int32_t *topk_idx, int64_t num_tokens,

@@ -26,6 +26,15 @@ DeviceState g_devices[kMaxDevices];
 std::atomic<uint64_t> g_launches{0};
 thread_local char g_last_cuda_error[256] = "no CUDA error";
 
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool experts_ok(int32_t E, int32_t k) {
+  return E >= 1 && E <= MOE_MAX_EXPERTS && k >= 1 && k <= MOE_MAX_TOPK && k <= E;
+}
+
+
+}  // namespace
+
 moe_status_t cuda_fail(cudaError_t e) {
   snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", cudaGetErrorName(e),
            cudaGetErrorString(e));
@@ -51,15 +60,6 @@ moe_status_t context(void* stream, LaunchCtx* ctx) {
   ctx->err = d.err;
   return MOE_OK;
 }
-
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-bool experts_ok(int32_t E, int32_t k) {
-  return E >= 1 && E <= MOE_MAX_EXPERTS && k >= 1 && k <= MOE_MAX_TOPK && k <= E;
-}
-
-
-}  // namespace
 
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 

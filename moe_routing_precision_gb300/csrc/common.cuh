@@ -431,6 +431,13 @@ inline int64_t route_num_chunks(int64_t T) {
 // Kernel launch counter (api.cu).
 void count_launches(int n);
 
+// api.cu: record a CUDA error for moe_last_cuda_error_string and return
+// MOE_ERR_CUDA; and the current device's launch context (SM count, the address
+// of the device error word), looked up once per device.  context() returns
+// MOE_ERR_UNSUPPORTED for a device ordinal beyond the library's table.
+moe_status_t cuda_fail(cudaError_t e);
+moe_status_t context(void* stream, LaunchCtx* ctx);
+
 // Let `kernel` take any dynamic shared memory a block can opt in to (the
 // device's opt-in maximum minus the kernel's static shared memory; api.cu).
 // Every call sets the same value for a kernel, so calls from several host

@@ -218,13 +218,13 @@ __global__ void __launch_bounds__(1024) expand_cast_rows_kernel(
 }
 
 // ---- bulk-store form --------------------------------------------------------
-// Same thread layout as the row form (one CTA holds a token, thread c owns
-// channels 16c..16c+15), but the token's codes and scales are assembled in a
-// shared-memory buffer and written by k TMA bulk copies (cp.async.bulk,
-// shared -> global) issued by one thread.  The CTA goes on to the next token
-// while the copies drain, so the SM's warps no longer wait on k store
-// instructions per slice; NBUF buffers are rotated, and a buffer is reused only
-// after cp.async.bulk.wait_group.read reports its copies have read it.
+// Same thread layout as the row form (thread c of a token owns channels
+// 16c..16c+15), one CTA per TOK consecutive tokens.  Every x load of the CTA's
+// tokens is issued first; each token's codes and scales are then assembled in
+// its own shared-memory slot and written by k TMA bulk copies (cp.async.bulk,
+// shared -> global) issued by one thread, so no warp waits on k store
+// instructions per slice.  The CTA retires once the copies have read shared
+// memory (cp.async.bulk.wait_group.read).
 // Needs G % 4 == 0 and 16-byte aligned out / out_sf (bulk copies move
 // multiples of 16 bytes between 16-byte aligned addresses).
 __device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
@@ -252,12 +252,15 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return p;
 }
 
-template <int NBUF>
+// OPTS: scale options (sfo.flags != 0) are compiled in; ZF: the zero-fill of
+// the padding rows (zsrc non-null) is.  The plain form (row-major f32 scales,
+// copied in bulk with the codes; no padding) keeps fewer registers, so more
+// CTAs are resident.
+template <int TOK, bool OPTS, bool ZF>
 __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
     int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf,
     const int32_t* __restrict__ zsrc, SfOut sfo, unsigned* err) {
-  static_assert(NBUF >= 2, "the buffer-reuse wait keeps NBUF - 2 copy groups in flight");
   extern __shared__ __align__(128) uint8_t s_buf[];
   pdl_enter();
   const int P = H >> 4;  // threads per token
@@ -267,125 +270,150 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
   const bool act = tid < P;
   const int g = tid >> 3;
   const int l8 = tid & 7;
-  const uint32_t stride = (uint32_t)((H + 4 * G + 127) / 128 * 128);  // bytes per buffer
+  const uint32_t stride = (uint32_t)((H + 4 * G + 127) / 128 * 128);  // bytes per token slot
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(s_buf);
+  int32_t* spos_all = reinterpret_cast<int32_t*>(s_buf + (size_t)TOK * stride);  // [TOK][32]
   bool bad = false;
+  const int flags = OPTS ? sfo.flags : 0;
   // only the column-major and byte scale layouts store partial lines
-  const bool hint = (sfo.flags & (MOE_SF_COLMAJOR | MOE_SF_UE8M0)) != 0 && sfo.stage == nullptr;
+  const bool hint = OPTS && (flags & (MOE_SF_COLMAJOR | MOE_SF_UE8M0)) != 0 && sfo.stage == nullptr;
   const uint64_t policy = l2_evict_first_policy();
-  int64_t t = blockIdx.x;
-  uint4 a = make_uint4(0, 0, 0, 0), b = a;
-  int32_t pnext = -1;  // warp 0: lane j holds pos[t, j] (j < k <= 32)
-  if (t < T) {
-    if (act) {
-      const uint16_t* src = x + t * H + tid * 16;
-      a = ld_stream_v4(src);
-      b = ld_stream_v4(src + 8);
-    }
-    if (tid < 32 && lane < k) pnext = __ldg(pos + t * k + lane);
-  }
-  int it = 0;
-  for (; t < T; t += gridDim.x, ++it) {
-    const uint4 ca = a, cb = b;
-    const int32_t pcur = pnext;
-    const int64_t tn = t + gridDim.x;
-    if (tn < T) {  // the next token's loads stay in flight during this one
+  const int64_t t0 = (int64_t)blockIdx.x * TOK;
+  // every load of the CTA's tokens is issued before any of them is used
+  uint4 a[TOK], b[TOK];
+  int32_t pv[TOK];  // warp 0: lane j holds pos[t, j] (j < k <= 32)
+#pragma unroll
+  for (int i = 0; i < TOK; ++i) {
+    const int64_t t = t0 + i;
+    a[i] = make_uint4(0, 0, 0, 0);
+    b[i] = a[i];
+    pv[i] = -1;
+    if (t < T) {
       if (act) {
-        const uint16_t* src = x + tn * H + tid * 16;
+        const uint16_t* src = x + t * H + tid * 16;
         if (hint) {
-          a = ld_stream_v4_hint(src, policy);
-          b = ld_stream_v4_hint(src + 8, policy);
+          a[i] = ld_stream_v4_hint(src, policy);
+          b[i] = ld_stream_v4_hint(src + 8, policy);
         } else {
-          a = ld_stream_v4(src);
-          b = ld_stream_v4(src + 8);
+          a[i] = ld_stream_v4(src);
+          b[i] = ld_stream_v4(src + 8);
         }
       }
-      if (tid < 32) pnext = (lane < k) ? __ldg(pos + tn * k + lane) : -1;
+      if (tid < 32 && lane < k) pv[i] = __ldg(pos + t * k + lane);
     }
-    const float amax = max8(absmax16_bf16(ca, cb));
-    const float sf = group_scale_opts(amax, sfo.flags);
-    const float inv = __fdiv_rn(1.0f, sf);
-    const uint4 q = quant16_bf16(ca, cb, inv);
-    const int buf = it % NBUF;
-    uint8_t* sq = s_buf + (size_t)buf * stride;
-    int32_t* spos = reinterpret_cast<int32_t*>(s_buf + (size_t)NBUF * stride) + buf * 32;
-    if (act) {
+  }
+  float sfv[TOK];
+#pragma unroll
+  for (int i = 0; i < TOK; ++i) {
+    const float amax = max8(absmax16_bf16(a[i], b[i]));
+    sfv[i] = group_scale_opts(amax, flags);
+    const float inv = __fdiv_rn(1.0f, sfv[i]);
+    const uint4 q = quant16_bf16(a[i], b[i], inv);
+    uint8_t* sq = s_buf + (size_t)i * stride;
+    if (act && t0 + i < T) {
       *reinterpret_cast<uint4*>(sq + tid * 16) = q;
-      if (l8 == 0 && sfo.flags == 0) *reinterpret_cast<float*>(sq + H + 4 * g) = sf;
+      if (l8 == 0 && flags == 0) *reinterpret_cast<float*>(sq + H + 4 * g) = sfv[i];
     }
-    if (sfo.flags != 0 && tid < 32) spos[tid] = pcur;  // destinations, for every warp
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the copies
-    __syncthreads();
-    if (sfo.flags != 0 && act && l8 == 0) {  // scale options: per-group scale stores
+    if (flags != 0 && tid < 32) spos_all[i * 32 + tid] = pv[i];  // for every warp
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the copies
+  __syncthreads();
+  if (flags != 0 && act && l8 == 0) {  // scale options: per-group scale stores
+#pragma unroll
+    for (int i = 0; i < TOK; ++i) {
+      const int64_t t = t0 + i;
+      if (t >= T) continue;
       if (sfo.stage != nullptr) {
-        store_stage(sfo.stage, sfo.flags, G, t, g, sf);
+        store_stage(sfo.stage, flags, G, t, g, sfv[i]);
       } else {
         for (int j = 0; j < k; ++j) {
-          const int32_t r = spos[j];
-          if (r >= 0 && r < R) store_sf_opts(out_sf, sfo.flags, sfo.ld, G, r, g, sf);
+          const int32_t r = spos_all[i * 32 + j];
+          if (r >= 0 && r < R) store_sf_opts(out_sf, flags, sfo.ld, G, r, g, sfv[i]);
         }
       }
     }
-    if (tid < 32) {
+  }
+  if (tid < 32) {
+#pragma unroll
+    for (int i = 0; i < TOK; ++i) {
+      if (t0 + i >= T) continue;  // the same for the whole warp
+      const uint32_t slot = sbase + (uint32_t)i * stride;
       for (int j = 0; j < k; ++j) {
-        const int32_t r = __shfl_sync(0xFFFFFFFFu, pcur, j);
+        const int32_t r = __shfl_sync(0xFFFFFFFFu, pv[i], j);
         if (tid == 0 && r >= 0) {
           if (r >= R) {
             bad = true;
           } else {
             if (hint)
-              bulk_s2g_hint(out + (int64_t)r * H, sbase + buf * stride, (uint32_t)H, policy);
+              bulk_s2g_hint(out + (int64_t)r * H, slot, (uint32_t)H, policy);
             else
-              bulk_s2g(out + (int64_t)r * H, sbase + buf * stride, (uint32_t)H);
-            if (sfo.flags == 0)
-              bulk_s2g(out_sf + (int64_t)r * G, sbase + buf * stride + H, (uint32_t)(4 * G));
+              bulk_s2g(out + (int64_t)r * H, slot, (uint32_t)H);
+            if (flags == 0) bulk_s2g(out_sf + (int64_t)r * G, slot + H, (uint32_t)(4 * G));
           }
         }
       }
-      if (tid == 0) {
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        // buffer (it + 2) % NBUF is written two tokens from now, after the
-        // next token's barrier: its copies (NBUF - 2 groups back) must have
-        // read it by then.  One barrier per token instead of two.
-        asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(NBUF - 2) : "memory");
-      }
+    }
+    if (tid == 0) {
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      // shared memory must stay valid until the copies have read it; their
+      // global writes complete on their own after the CTA exits
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     }
   }
-  // the copies read shared memory until they complete: wait before exiting
-  if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   // warps numbered CTA-major, so consecutive 32-row groups (the all-padding
   // tail is one contiguous run) go to different CTAs instead of a few late ones
-  if (zsrc != nullptr)
+  if (ZF && zsrc != nullptr)
     zero_fill_rows(zsrc, R, H, H >> 7, out, out_sf,
                    (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x,
                    ((int64_t)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31, sfo);
   if (bad) flag_error(err, MOE_DEVERR_POS_RANGE);
 }
 
-// Buffers and CTAs per SM for the bulk form, measured on GB300 (prefill- and
-// skewed-sized expand, H = 7168): 4 buffers, 3 CTAs per SM (of which two fit
-// by registers at a time) ran 6.10 TB/s against 5.66 for the row form.
-constexpr int kBulkBuffers = 4;
-constexpr int kBulkCtasPerSm = 3;
+// Tokens per CTA of the bulk form.  The grid is not persistent: one CTA per
+// TOK consecutive tokens, retiring when its copies have read shared memory.
+// Measured on GB300 (H = 7168, k = 8, after an L2 flush): 0.705 ms (1.01 of
+// the measured copy peak) at T = 65536 and 94.8 us (0.94) at T = 8192, against
+// 0.80 ms and 104 us for a persistent grid of 3 CTAs per SM that strode over
+// the tokens with the next token's loads in flight.  The persistent grid kept
+// the accesses in flight at any moment spread over the whole of x and q; here
+// the CTAs in flight at once cover a compact run of consecutive tokens.
+constexpr int kBulkTokensPerCta = 2;
 
-template <int NBUF>
-cudaError_t launch_bulk(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
+template <int TOK, bool OPTS, bool ZF>
+cudaError_t launch_bulk_t(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                         const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
-                        int ctas_per_sm, const int32_t* zsrc, SfOut sfo) {
+                        const int32_t* zsrc, SfOut sfo) {
   const int P = H / 16;
   const int threads = (P + 31) / 32 * 32;
   const int G = H / kGroup;
   const size_t stride = (size_t)(H + 4 * G + 127) / 128 * 128;
-  const size_t smem = stride * NBUF + sizeof(int32_t) * 32 * NBUF;  // + per-buffer destinations
+  const size_t smem = (stride + sizeof(int32_t) * 32) * TOK;  // + per-token destinations
   if (smem > 48 * 1024) {
-    cudaError_t st = allow_max_dynamic_smem(expand_cast_bulk_kernel<NBUF>);
+    cudaError_t st = allow_max_dynamic_smem(expand_cast_bulk_kernel<TOK, OPTS, ZF>);
     if (st != cudaSuccess) return st;
   }
-  const int64_t cap = (int64_t)c.num_sms * ctas_per_sm;
-  const int blocks = (int)(T < cap ? (T > 0 ? T : 1) : cap);  // >= 1: zero-fill with T = 0
-  return launch_pdl(expand_cast_bulk_kernel<NBUF>, blocks, threads, smem, c.stream,
+  int64_t blocks = (T + TOK - 1) / TOK;
+  if (zsrc != nullptr) {  // enough warps for one 32-row group of the zero-fill each
+    const int64_t zb = ((R + 31) / 32 + threads / 32 - 1) / (threads / 32);
+    blocks = blocks > zb ? blocks : zb;
+  }
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(expand_cast_bulk_kernel<TOK, OPTS, ZF>, (unsigned)blocks, threads, smem, c.stream,
                     static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, zsrc, sfo,
                     c.err);
+}
+
+cudaError_t launch_bulk(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
+                        const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
+                        const int32_t* zsrc, SfOut sfo) {
+  constexpr int TOK = kBulkTokensPerCta;
+  if (sfo.flags != 0)
+    return zsrc != nullptr
+               ? launch_bulk_t<TOK, true, true>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo)
+               : launch_bulk_t<TOK, true, false>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
+  return zsrc != nullptr
+             ? launch_bulk_t<TOK, false, true>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo)
+             : launch_bulk_t<TOK, false, false>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
 }
 
 // CTAs per SM for the row form, measured on GB300 (prefill-sized expand).
@@ -485,8 +513,7 @@ cudaError_t launch_expand_cast_kernel(const LaunchCtx& c, const void* x, int64_t
   const bool aligned16 = (reinterpret_cast<uintptr_t>(out) % 16) == 0;
   const bool bulk_ok = sfo.flags != 0 || g4;  // scale options don't use the bulk scale copy
   if (H <= 16384 && bulk_ok && (H / kGroup) % 4 == 0 && aligned16)
-    return launch_bulk<kBulkBuffers>(c, x, T, H, k, pos, R, out, out_sf, kBulkCtasPerSm,
-                                     zero_rows, sfo);
+    return launch_bulk(c, x, T, H, k, pos, R, out, out_sf, zero_rows, sfo);
   if (H <= 16384)
     return g4 ? launch_rows<true>(c, x, T, H, k, pos, R, out, out_sf, kRowCtasPerSm, zero_rows, sfo)
               : launch_rows<false>(c, x, T, H, k, pos, R, out, out_sf, kRowCtasPerSm, zero_rows,

@@ -9,25 +9,23 @@
 // scales to the rows pos names.  Two codes per byte, element 2i in the low
 // nibble.  Group sizes 16, 32, 64 and 128 (1, 2, 4 or 8 lanes of 16 channels).
 //
-// Same structure as the E4M3 bulk-store kernel: one CTA per token slice,
-// thread c owning channels 16c..16c+15; the token's packed codes (H/2 bytes)
-// and, for plain row-major f32 scales with G % 4 == 0, its scales are staged
-// in shared memory and leave with TMA bulk copies (cp.async.bulk) issued by one
-// thread; other scale layouts are stored per group by one lane, or staged per
-// token for the column-major gather.
+// Same structure as the E4M3 bulk-store kernel: one CTA per two consecutive
+// tokens, thread c owning channels 16c..16c+15; each token's packed codes
+// (H/2 bytes) and, for plain row-major f32 scales with G % 4 == 0, its scales
+// are staged in shared memory and leave with TMA bulk copies (cp.async.bulk)
+// issued by one thread; other scale layouts are stored per group by one lane,
+// or staged per token for the column-major gather.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-// Measured on GB300 (prefill-sized expand, H = 7168, group 32): two CTAs per
-// SM (both resident by registers) 86-88 % of peak, three (one waiting for a
-// slot) 82 %; a second token of register prefetch did not help.
-constexpr int kFp4Buffers = 4;
-constexpr int kFp4CtasPerSm = 2;
-// Tokens per iteration: 2 (one barrier and one copy group per two tokens) was
-// measured at 86 % of peak at prefill size against 88 % for 1.
-constexpr int kFp4TokensPerIter = 1;
+// Tokens per CTA.  The grid is not persistent: one CTA per TOK consecutive
+// tokens, retiring once its copies have read shared memory, so the CTAs in
+// flight at any moment cover a compact run of tokens (the E4M3 bulk form's
+// layout; there a persistent grid striding over the tokens ran at 0.89 of the
+// measured copy peak against 1.01).
+constexpr int kFp4TokensPerCta = 2;
 
 __device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
@@ -37,14 +35,12 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t byt
 
 // L = lanes per group (group = 16 L channels).  sf_bulk: plain row-major f32
 // scales whose rows (4G bytes) are 16-byte multiples go out with the codes.
-// TPI tokens per iteration (adjacent tokens 2p, 2p + 1 for TPI = 2): one
-// barrier and one copy group per TPI tokens; buffer b holds TPI token slots.
-template <int L, int NBUF, int TPI>
-__global__ void __launch_bounds__(TPI == 1 ? 1024 : 448, TPI == 1 ? 1 : 2) expand_cast_fp4_kernel(
+// ZF: the zero-fill of the padding rows (zsrc non-null) is compiled in.
+template <int L, int TOK, bool ZF>
+__global__ void __launch_bounds__(1024) expand_cast_fp4_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
     int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf,
     const int32_t* __restrict__ zsrc, SfOut sfo, int sf_bulk, unsigned* err) {
-  static_assert(NBUF >= 2, "the buffer-reuse wait keeps NBUF - 2 copy groups in flight");
   extern __shared__ __align__(128) uint8_t s_buf[];
   pdl_enter();
   const int P = H >> 4;   // threads per token
@@ -57,146 +53,126 @@ __global__ void __launch_bounds__(TPI == 1 ? 1024 : 448, TPI == 1 ? 1 : 2) expan
   const bool lead = (tid % L) == 0;
   const uint32_t stride = (uint32_t)((HB + 4 * G + 127) / 128 * 128);  // bytes per token slot
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(s_buf);
-  int32_t* spos_all = reinterpret_cast<int32_t*>(s_buf + (size_t)NBUF * TPI * stride);
+  int32_t* spos_all = reinterpret_cast<int32_t*>(s_buf + (size_t)TOK * stride);  // [TOK][32]
   bool bad = false;
-  const int64_t nit = (T + TPI - 1) / TPI;  // token groups
-  uint4 a[TPI], b[TPI];
-  int32_t pn[TPI];  // warp 0: lane j holds pos[t, j] (j < k <= 32)
-  auto load = [&](int64_t p) {
+  const int64_t t0 = (int64_t)blockIdx.x * TOK;
+  // every load of the CTA's tokens is issued before any of them is used
+  uint4 a[TOK], b[TOK];
+  int32_t pv[TOK];  // warp 0: lane j holds pos[t, j] (j < k <= 32)
 #pragma unroll
-    for (int i = 0; i < TPI; ++i) {
-      const int64_t t = p * TPI + i;
-      a[i] = make_uint4(0, 0, 0, 0);
-      b[i] = a[i];
-      pn[i] = -1;
-      if (t < T) {
-        if (act) {
-          const uint16_t* src = x + t * H + tid * 16;
-          a[i] = ld_stream_v4(src);
-          b[i] = ld_stream_v4(src + 8);
-        }
-        if (tid < 32 && lane < k) pn[i] = __ldg(pos + t * k + lane);
+  for (int i = 0; i < TOK; ++i) {
+    const int64_t t = t0 + i;
+    a[i] = make_uint4(0, 0, 0, 0);
+    b[i] = a[i];
+    pv[i] = -1;
+    if (t < T) {
+      if (act) {
+        const uint16_t* src = x + t * H + tid * 16;
+        a[i] = ld_stream_v4(src);
+        b[i] = ld_stream_v4(src + 8);
       }
+      if (tid < 32 && lane < k) pv[i] = __ldg(pos + t * k + lane);
     }
-  };
-  int64_t p = blockIdx.x;
-  if (p < nit) load(p);
-  int it = 0;
-  for (; p < nit; p += gridDim.x, ++it) {
-    uint4 ca[TPI], cb[TPI];
-    int32_t pc[TPI];
+  }
+  float sfv[TOK];
 #pragma unroll
-    for (int i = 0; i < TPI; ++i) {
-      ca[i] = a[i];
-      cb[i] = b[i];
-      pc[i] = pn[i];
+  for (int i = 0; i < TOK; ++i) {
+    const bool valid = t0 + i < T;
+    const float amax = maxL<L>(absmax16_bf16(a[i], b[i]));
+    sfv[i] = fp4_scale(amax, sfo.flags);
+    const float inv = __fdiv_rn(1.0f, sfv[i]);
+    const uint2 q = quant16_bf16_e2m1(a[i], b[i], inv);
+    uint8_t* sq = s_buf + (size_t)i * stride;
+    if (act && valid) {
+      *reinterpret_cast<uint2*>(sq + tid * 8) = q;
+      if (lead && sf_bulk) *reinterpret_cast<float*>(sq + HB + 4 * g) = sfv[i];
     }
-    if (p + gridDim.x < nit) load(p + gridDim.x);  // in flight during this group
-    const int buf = it % NBUF;
-    float sfv[TPI];
+    if (!sf_bulk && tid < 32) spos_all[i * 32 + tid] = valid ? pv[i] : -1;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the copies
+  __syncthreads();
+  if (!sf_bulk && act && lead) {  // one lane per group stores its scale
 #pragma unroll
-    for (int i = 0; i < TPI; ++i) {
-      const bool valid = p * TPI + i < T;
-      const float amax = maxL<L>(absmax16_bf16(ca[i], cb[i]));
-      const float sf = fp4_scale(amax, sfo.flags);
-      const float inv = __fdiv_rn(1.0f, sf);
-      const uint2 q = quant16_bf16_e2m1(ca[i], cb[i], inv);
-      sfv[i] = sf;
-      uint8_t* sq = s_buf + (size_t)(buf * TPI + i) * stride;
-      if (act && valid) {
-        *reinterpret_cast<uint2*>(sq + tid * 8) = q;
-        if (lead && sf_bulk) *reinterpret_cast<float*>(sq + HB + 4 * g) = sf;
-      }
-      if (!sf_bulk && tid < 32) spos_all[(buf * TPI + i) * 32 + tid] = valid ? pc[i] : -1;
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the copies
-    __syncthreads();
-    if (!sf_bulk && act && lead) {  // one lane per group stores its scale
-#pragma unroll
-      for (int i = 0; i < TPI; ++i) {
-        const int64_t t = p * TPI + i;
-        if (t >= T) continue;
-        if (sfo.stage != nullptr) {
-          store_stage(sfo.stage, sfo.flags, G, t, g, sfv[i]);
-        } else {
-          const int32_t* spos = spos_all + (buf * TPI + i) * 32;
-          for (int j = 0; j < k; ++j) {
-            const int32_t r = spos[j];
-            if (r >= 0 && r < R) store_sf_opts(out_sf, sfo.flags, sfo.ld, G, r, g, sfv[i]);
-          }
-        }
-      }
-    }
-    if (tid < 32) {
-#pragma unroll
-      for (int i = 0; i < TPI; ++i) {
-        const uint32_t slot = sbase + (uint32_t)(buf * TPI + i) * stride;
+    for (int i = 0; i < TOK; ++i) {
+      const int64_t t = t0 + i;
+      if (t >= T) continue;
+      if (sfo.stage != nullptr) {
+        store_stage(sfo.stage, sfo.flags, G, t, g, sfv[i]);
+      } else {
+        const int32_t* spos = spos_all + i * 32;
         for (int j = 0; j < k; ++j) {
-          const int32_t r = __shfl_sync(0xFFFFFFFFu, pc[i], j);
-          if (tid == 0 && r >= 0) {
-            if (r >= R) {
-              bad = true;
-            } else {
-              bulk_s2g(out + (int64_t)r * HB, slot, (uint32_t)HB);
-              if (sf_bulk) bulk_s2g(out_sf + (int64_t)r * G, slot + HB, (uint32_t)(4 * G));
-            }
-          }
+          const int32_t r = spos[j];
+          if (r >= 0 && r < R) store_sf_opts(out_sf, sfo.flags, sfo.ld, G, r, g, sfv[i]);
         }
-      }
-      if (tid == 0) {
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        // buffer (it + 2) % NBUF is written two groups from now, after the
-        // next group's barrier: its copies (NBUF - 2 groups back) must have
-        // read it by then.  One barrier per group of TPI tokens.
-        asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(NBUF - 2) : "memory");
       }
     }
   }
-  // the copies read shared memory until they complete: wait before exiting
-  if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-  if (zsrc != nullptr)
+  if (tid < 32) {
+#pragma unroll
+    for (int i = 0; i < TOK; ++i) {
+      if (t0 + i >= T) continue;  // the same for the whole warp
+      const uint32_t slot = sbase + (uint32_t)i * stride;
+      for (int j = 0; j < k; ++j) {
+        const int32_t r = __shfl_sync(0xFFFFFFFFu, pv[i], j);
+        if (tid == 0 && r >= 0) {
+          if (r >= R) {
+            bad = true;
+          } else {
+            bulk_s2g(out + (int64_t)r * HB, slot, (uint32_t)HB);
+            if (sf_bulk) bulk_s2g(out_sf + (int64_t)r * G, slot + HB, (uint32_t)(4 * G));
+          }
+        }
+      }
+    }
+    if (tid == 0) {
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      // shared memory must stay valid until the copies have read it; their
+      // global writes complete on their own after the CTA exits
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    }
+  }
+  if (ZF && zsrc != nullptr)
     zero_fill_rows(zsrc, R, HB, G, out, out_sf,
                    (int64_t)(threadIdx.x >> 5) * gridDim.x + blockIdx.x,
                    ((int64_t)gridDim.x * blockDim.x) >> 5, threadIdx.x & 31, sfo);
   if (bad) flag_error(err, MOE_DEVERR_POS_RANGE);
 }
 
-template <int L, int TPI>
+template <int L, bool ZF>
 cudaError_t launch_lt(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                       const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
                       const int32_t* zsrc, SfOut sfo) {
-  constexpr int NBUF = kFp4Buffers;
+  constexpr int TOK = kFp4TokensPerCta;
   const int P = H / 16;
   const int threads = (P + 31) / 32 * 32;
   const int G = P / L;
   const size_t stride = (size_t)(H / 2 + 4 * G + 127) / 128 * 128;
-  const size_t smem = (stride + sizeof(int32_t) * 32) * NBUF * TPI;
+  const size_t smem = (stride + sizeof(int32_t) * 32) * TOK;
   if (smem > 48 * 1024) {
-    cudaError_t st = allow_max_dynamic_smem(expand_cast_fp4_kernel<L, NBUF, TPI>);
+    cudaError_t st = allow_max_dynamic_smem(expand_cast_fp4_kernel<L, TOK, ZF>);
     if (st != cudaSuccess) return st;
   }
   const int sf_bulk = (sfo.flags == 0 && sfo.stage == nullptr && G % 4 == 0 &&
                        reinterpret_cast<uintptr_t>(out_sf) % 16 == 0)
                           ? 1
                           : 0;
-  const int64_t cap = (int64_t)c.num_sms * kFp4CtasPerSm;
-  const int64_t groups = (T + TPI - 1) / TPI;
-  const int blocks = (int)(groups < cap ? (groups > 0 ? groups : 1) : cap);  // >= 1: zero-fill
-  return launch_pdl(expand_cast_fp4_kernel<L, NBUF, TPI>, blocks, threads, smem, c.stream,
+  int64_t blocks = (T + TOK - 1) / TOK;
+  if (ZF) {  // enough warps for one 32-row group of the zero-fill each
+    const int64_t zb = ((R + 31) / 32 + threads / 32 - 1) / (threads / 32);
+    blocks = blocks > zb ? blocks : zb;
+  }
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(expand_cast_fp4_kernel<L, TOK, ZF>, (unsigned)blocks, threads, smem, c.stream,
                     static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, zsrc, sfo,
                     sf_bulk, c.err);
 }
 
-// Two tokens per iteration where a token slice has at most 448 threads
-// (H <= 7168: two such CTAs per SM keep 72 registers a thread), else one.
 template <int L>
 cudaError_t launch_l(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                      const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
                      const int32_t* zsrc, SfOut sfo) {
-  if constexpr (kFp4TokensPerIter == 2) {
-    if (H <= 7168) return launch_lt<L, 2>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
-  }
-  return launch_lt<L, 1>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
+  return zsrc != nullptr ? launch_lt<L, true>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo)
+                         : launch_lt<L, false>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
 }
 
 }  // namespace

@@ -6,8 +6,8 @@
 // host framework hands out all buffers from its own arena, and runtimes that
 // fix their memory budget at start-up.  Such a caller can pass inputs and
 // outputs but has no way to provide moe_route_map's workspace.  This entry
-// point runs the same three route-map kernels with their per-chunk histogram
-// in a fixed file-scope device array instead.
+// point runs the same route-map kernels with their per-chunk histogram in a
+// fixed file-scope device array instead.
 //
 // The array is a __device__ variable, so every GPU that loads this library
 // holds it (kRouteScratchBytes) until the process exits, whether or not the
@@ -33,7 +33,6 @@ struct ScratchSlot {
   std::once_flag once;
   cudaError_t status = cudaSuccess;
   void* ptr = nullptr;
-  int num_sms = 0;
 };
 ScratchSlot g_slots[kMaxDevices];
 
@@ -53,28 +52,35 @@ extern "C" moe_status_t moe_route_map_noalloc(const int32_t* topk_idx, int64_t n
   if (num_tokens == 0) return moe_route_map(topk_idx, 0, num_experts, num_topk, counts, offsets,
                                             pos, sorted_src, nullptr, 0, stream);
   if (!topk_idx || !counts || !offsets || !pos || !sorted_src) return MOE_ERR_INVALID_ARG;
+  // the same alignment rule as moe_route_map: every array is int32
+  const auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; };
+  if (misaligned(topk_idx) || misaligned(counts) || misaligned(offsets) || misaligned(pos) ||
+      misaligned(sorted_src))
+    return MOE_ERR_INVALID_ARG;
   if (moe_route_map_workspace_bytes(num_tokens, num_experts, num_topk) > kRouteScratchBytes)
     return MOE_ERR_UNSUPPORTED;  // beyond the static scratch: use moe_route_map
 
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
-  ScratchSlot& s = g_slots[dev];
-  std::call_once(s.once, [&s, dev]() {
-    // runs with `dev` current: these are that device's addresses
-    cudaError_t e = cudaGetSymbolAddress(&s.ptr, g_route_scratch);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
-    s.status = e;
-  });
-  if (s.status != cudaSuccess || s.ptr == nullptr) return MOE_ERR_CUDA;
-
+  // the library's launch context: SM count and the device error word (itself
+  // a __device__ variable, so nothing is allocated here either)
   LaunchCtx c;
-  c.stream = static_cast<cudaStream_t>(stream);
-  c.num_sms = s.num_sms;
-  c.err = nullptr;  // out-of-range experts are skipped (pos = -1) but not flagged
+  moe_status_t st = context(stream, &c);
+  if (st != MOE_OK) return st;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  ScratchSlot& s = g_slots[dev];
+  std::call_once(s.once, [&s]() {
+    // runs with `dev` current: this is that device's address of the array
+    s.status = cudaGetSymbolAddress(&s.ptr, g_route_scratch);
+  });
+  if (s.status != cudaSuccess) return cuda_fail(s.status);
+  if (s.ptr == nullptr) return MOE_ERR_CUDA;
+
   const int64_t chunks = route_num_chunks(num_tokens);
   // every histogram entry the kernels read is written first in the same call,
   // so the scratch needs no clearing between calls
-  cudaError_t e = launch_route_map(c, topk_idx, num_tokens, num_experts, num_topk, counts, offsets,
-                                   pos, sorted_src, static_cast<int32_t*>(s.ptr), chunks);
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  e = launch_route_map(c, topk_idx, num_tokens, num_experts, num_topk, counts, offsets, pos,
+                       sorted_src, static_cast<int32_t*>(s.ptr), chunks);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
 }

@@ -1,8 +1,7 @@
 """GPU parity: every op through the C ABI against the CPU oracle.
 
-Small ragged shapes compare every element; the full workloads compare the
-whole route map and top-k, and sampled token rows of the cast and combine
-outputs (the oracle computes those rows one by one).
+Small ragged shapes compare every element here; the benchmarked sizes are
+compared element by element in test_gpu_full_size.py.
 """
 import numpy as np
 import pytest
@@ -303,56 +302,6 @@ def test_small_workloads_every_element(name):
     o32, o16, mag = oracle.combine(bits(inp["y"]), o_w, o_pos)
     check_combine_f32(np_(got["comb32"]), o32, mag)
     check_combine_bf16(bits(got["comb16"].cpu()), o16, o32, mag)
-
-
-def _sample_tokens(T, n, seed):
-    g = torch.Generator().manual_seed(seed)
-    s = torch.randperm(T, generator=g)[:n]
-    return torch.unique(torch.cat([s, torch.tensor([0, T - 1])])).sort().values
-
-
-@pytest.mark.parametrize("name", ["skewed_8k", "prefill_64k"])
-def test_large_workloads_full_route_sampled_rows(name):
-    """Full-size inputs, the launch shapes the bench times.  The whole top-k
-    and route map are compared; cast and combine on ~600 sampled tokens."""
-    w = workloads.WORKLOADS[name]
-    inp = workloads.make_inputs(w, seed=0, device=DEV, with_y=True)
-    got = _chain(w, inp)
-    assert ops.device_status() == 0
-    o_idx, o_w, o_counts, o_off, o_pos, o_src = _route_oracle(w, inp)
-    assert_equal(np_(got["idx"]), o_idx, "idx")
-    assert_weights_close(np_(got["w"]), o_w)
-    for n, r in (("counts", o_counts), ("offsets", o_off), ("pos", o_pos), ("src", o_src)):
-        assert_equal(np_(got[n]), r, n)
-    toks = _sample_tokens(w.T, 600, seed=7)
-    xs = inp["x"][toks.to(DEV)].cpu()
-    o_qs, o_sfs = oracle.per_token_cast(bits(xs))
-    rows = torch.from_numpy(o_pos[toks.numpy()]).long()           # [n, k]
-    gq = np_(got["q"][rows.flatten().to(DEV)]).reshape(len(toks), w.k, w.H)
-    gsf = np_(got["sf"][rows.flatten().to(DEV)]).reshape(len(toks), w.k, w.G)
-    for j in range(w.k):
-        assert_equal(gq[:, j], o_qs, f"q copy {j}")
-        assert_f32_bits_equal(gsf[:, j], o_sfs, f"sf copy {j}")
-    ys = inp["y"][rows.flatten().to(DEV)].cpu()                   # [n*k, H]
-    lpos = np.arange(len(toks) * w.k, dtype=np.int32).reshape(len(toks), w.k)
-    o32, o16, mag = oracle.combine(bits(ys), o_w[toks.numpy()], lpos)
-    check_combine_f32(np_(got["comb32"][toks.to(DEV)]), o32, mag)
-    check_combine_bf16(bits(got["comb16"][toks.to(DEV)].cpu()), o16, o32, mag)
-    del got, inp
-    torch.cuda.empty_cache()
-
-
-def test_swiglu_workload_sampled_rows():
-    w = workloads.WORKLOADS["swiglu_64k"]
-    inp = workloads.make_inputs(w, seed=0, device=DEV)
-    x = inp["swiglu_x"]
-    q, sf = ops.swiglu_cast_fp8(x)
-    rows = _sample_tokens(w.M, 2000, seed=9).to(DEV)
-    o_q, o_sf = oracle.swiglu_cast_fp8(bits(x[rows].cpu()))
-    frac = check_swiglu(np_(q[rows]), np_(sf[rows]), o_q, o_sf)
-    assert frac <= 1e-3
-    del inp, q, sf
-    torch.cuda.empty_cache()
 
 
 # ---------------------------------------------------------------- padded layout
