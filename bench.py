@@ -15,8 +15,16 @@ resident in HBM before timing; every input tensor but the 67 MB score matrix
 is larger than L2, and the step moves ~19 GB, so nothing is L2-resident when a
 step starts.
 
+The printed JSON line is kept short: besides the contract's keys it carries
+`configs`, one compact entry per benchmarked workload (the tiny and decode
+batches, the skewed routing, the SwiGLU rows, the large prefill) with its time
+and fraction of the measured HBM peak, and the rooflines of the step's and of
+the headline's dominant kernels.  Everything else (per-op bytes, two-stream
+and variant rows, decode tables, the copy kernel) goes to the JSON file that
+`detail` names.
+
 --impl reference times the CPU oracle (test infrastructure) on the same
-metric, on a bounded sample of the same workload.
+metric and the same workload.
 """
 from __future__ import annotations
 
@@ -39,8 +47,7 @@ UNIT = "routed tokens/s"
 WORKLOAD = "prefill_64k"
 SWIGLU_N = 2048
 FALLBACK_HBM_GBS = 6800.0
-L2_NOTE = ("inputs larger than L2: x 0.94 GB, SwiGLU input 4.3 GB, y 7.5 GB; the 67 MB score "
-           "matrix is evicted by the ~19 GB each step moves")
+DETAIL_DEFAULT = os.path.join("gpurun_out", "bench_detail.json")
 
 
 # ---------------------------------------------------------------- helpers
@@ -59,6 +66,14 @@ def algorithmic_bytes(T, E, k, H, N=SWIGLU_N, M=None):
     }
     b["route_expand_cast"] = b["topk_gate"] + b["route_map"] + b["expand_cast_fp8"]
     return b
+
+
+def config_dict(world: int) -> dict:
+    """The benchmarked workload, named the same way by both arms."""
+    return {"workload": "prefill_64k: T=65536 E=256 k=8 H=7168, route+expand+cast",
+            "T": 65536, "E": 256, "k": 8, "H": 7168, "seed": "rank",
+            "parallelism": f"replicas x{world}, no collective",
+            "l2": "inputs > L2 (x 0.94 GB)"}
 
 
 # GB300's nominal HBM3e bandwidth per GPU as NVIDIA states it (context for the
@@ -84,9 +99,10 @@ def source_sha(fname):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(op, units_scale=1.0):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+def ncu_traffic(op, units):
+    """DRAM bytes per launch of `op`'s kernel for `units` units of work (tokens
+    or rows), from the committed ncu summary, if it was taken on the current
+    kernel source: the captured bytes per unit times `units`; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if op not in KERNEL_OF_OP or not os.path.exists(path):
         return None
@@ -94,7 +110,7 @@ def ncu_traffic(op, units_scale=1.0):
         rec = json.load(f).get(KERNEL_OF_OP[op][0])
     if not rec or rec.get("source_sha") != source_sha(KERNEL_OF_OP[op][1]):
         return None
-    return rec["dram_bytes_per_launch"] * units_scale
+    return round(rec["dram_bytes_per_launch"] / rec["units"] * units)
 
 
 def load_peaks():
@@ -191,6 +207,9 @@ def job_throughput(units_per_rank: int, world: int, seconds: float) -> float:
 
 # ---------------------------------------------------------------- GPU arm
 
+
+# ---------------------------------------------------------------- GPU arm
+
 def gpu_arm(args):
     import torch
     import torch.distributed as dist
@@ -223,6 +242,7 @@ def gpu_arm(args):
     counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
     pos, src = torch.empty(T, k, **i32), torch.empty(R, **i32)
     ws = torch.empty(max(1, ops.route_map_workspace_bytes(T, E, k)), dtype=torch.uint8, device=dev)
+    ws1 = ops.route_expand_cast_workspace(T, E, k, x)   # the one-call path's (zeroed once)
     q = torch.empty(R, H, dtype=torch.uint8, device=dev)
     sf = torch.empty(R, G, dtype=torch.float32, device=dev)
     if full:
@@ -236,29 +256,47 @@ def gpu_arm(args):
         if rc != 0:
             raise ops.MoeError(rc, what)
 
-    def route_expand_cast():
-        chk(L.moe_topk_gate(scores.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
-        chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
-                            pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
-        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
-                                  sf.data_ptr(), 128, sp), "expand")
+    def route_expand_cast(p=sp):
+        """topk_gate + route_map + expand_cast_fp8 as a caller runs them: the
+        one-call entry point (AUTO: the separate launches at this size), or
+        with --headline-path calls the three individual calls."""
+        if args.headline_path == "calls":
+            chk(L.moe_topk_gate(scores.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, p),
+                "topk")
+            chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
+                                pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), p),
+                "route")
+            chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
+                                      sf.data_ptr(), 128, p), "expand")
+        else:
+            chk(L.moe_route_expand_cast_fp8(scores.data_ptr(), T, E, k, x.data_ptr(), H,
+                                            idx.data_ptr(), wt.data_ptr(), counts.data_ptr(),
+                                            offsets.data_ptr(), pos.data_ptr(), src.data_ptr(),
+                                            q.data_ptr(), sf.data_ptr(), ws1.data_ptr(),
+                                            ws1.numel(), ops.PATH_AUTO, 128, p), "route_expand_cast")
 
     def step(ev=None, split=True):
-        """One step.  ev: 6 events (split) around each op, or 2 around
-        topk + route + expand only: an event between two kernels ends the
-        programmatic-dependent-launch overlap between them, so the timed
-        steps record only the two that bracket the headline."""
+        """One step.  ev: 2 events around route + expand + cast (the timed
+        steps), or, split, 6 events around each op with the route + expand +
+        cast run as the three individual calls (the per-op breakdown, in
+        separate steps: an event between two kernels ends their
+        programmatic-dependent-launch overlap)."""
         def rec(i):
             if ev and (split or i in (0, 3)):
                 ev[i if split else (0 if i == 0 else 1)].record(stream)
         rec(0)
-        chk(L.moe_topk_gate(scores.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
-        rec(1)
-        chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
-                            pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
-        rec(2)
-        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
-                                  sf.data_ptr(), 128, sp), "expand")
+        if split:
+            chk(L.moe_topk_gate(scores.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp),
+                "topk")
+            rec(1)
+            chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
+                                pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp),
+                "route")
+            rec(2)
+            chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
+                                      sf.data_ptr(), 128, sp), "expand")
+        else:
+            route_expand_cast()
         rec(3)
         if full:
             chk(L.swiglu_cast_fp8(hx.data_ptr(), R, N, q2.data_ptr(), sf2.data_ptr(), 128, sp),
@@ -324,14 +362,14 @@ def gpu_arm(args):
     e2e = None
     if not args.no_e2e:
         e2e = e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, src,
-                      ws, q, sf, T, E, k, H, R, chk, barrier, maxr)
+                      ws1, q, sf, T, E, k, H, R, chk, barrier, maxr)
 
-    # ---- other workloads (their own lines' worth of numbers, L2 flushed)
-    extra = None
+    peak, peak_src = load_peaks()
+    # ---- the other workloads: compact per-config entries + detail (rank 0)
+    summaries, detail = {}, {}
     if rank == 0 and not args.no_extra:
-        extra = extra_workloads(L, dev, stream, sp, chk, args)
-
-    peak_copy = measure_peak_copy(L, dev, stream, sp) if rank == 0 else None
+        summaries, detail = other_configs(L, dev, stream, sp, chk, args, peak)
+        detail["peak_copy_GB_s"] = measure_peak_copy(L, dev, stream, sp)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -343,7 +381,6 @@ def gpu_arm(args):
         dist.destroy_process_group()
         return None
 
-    peak, peak_src = load_peaks()
     B = algorithmic_bytes(T, E, k, H, N, R)
     breakdown = {}
     for n in ops_names:
@@ -354,45 +391,65 @@ def gpu_arm(args):
         breakdown[n] = {"ms": round(ms, 4), "algorithmic_bytes": B[n], "GB_s": round(gbs, 1),
                         "frac_of_peak": round(gbs / peak, 4)}
     rec_gbs = B["route_expand_cast"] / (rec_ms_mean * 1e-3) / 1e9
-    breakdown["route_expand_cast"] = {
-        "ms": round(rec_ms_mean, 4), "algorithmic_bytes": B["route_expand_cast"],
-        "GB_s": round(rec_gbs, 1), "frac_of_peak": round(rec_gbs / peak, 4),
-        "frac_of_nominal": round(rec_gbs / NOMINAL_HBM_GBS, 4),
-        "tokens_per_s": round(T * world / (rec_ms_mean * 1e-3), 1)}
+    units = {"topk_gate": T, "expand_cast_fp8": T, "swiglu_cast_fp8": R, "combine": T}
+
+    def roofline(op):
+        gbs = B[op] / (op_ms[op] * 1e-3) / 1e9
+        return {"bound": "hbm", "kernel": KERNEL_OF_OP[op][0], "achieved": round(gbs, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4), "peak_source": peak_src,
+                "traffic": ncu_traffic(op, units[op]), "ms": round(op_ms[op], 4)}
+
     dom = max((n for n in ops_names if n in KERNEL_OF_OP and n in ran), key=lambda n: op_ms[n])
-    dom_gbs = B[dom] / (op_ms[dom] * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": KERNEL_OF_OP[dom][0], "achieved": round(dom_gbs, 1),
-                "peak": peak, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
-                "peak_source": peak_src, "traffic": ncu_traffic(dom),
-                "algorithmic_bytes_per_launch": B[dom]}
+    head_dom = max(("topk_gate", "expand_cast_fp8"), key=lambda n: op_ms[n])
     value = job_throughput(R, world, rec_ms_mean * 1e-3)
+    summaries["c4_prefill_64k"] = {"ms": round(rec_ms_mean, 4), "frac": round(rec_gbs / peak, 4)}
+    if full:
+        summaries["c4_prefill_64k"]["combine_frac"] = breakdown["combine"]["frac_of_peak"]
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3",
-        "data": "synthetic (seeded torch.Generator, no dataset)",
-        "config": {"workload": f"{w.name}: T={T} E={E} k={k} H={H} (+SwiGLU 2x{N} per routed "
-                               "row, combine y [T*k,H]); value = route+expand+cast",
-                   "T": T, "E": E, "k": k, "H": H, "swiglu_N": N, "seed": "rank",
-                   "parallelism": f"replicas x{world} (token-sharded, no collective)",
-                   "l2": L2_NOTE},
-        "value_scope": "T*k routed tokens / (topk_gate + route_map + expand_cast_fp8 time)",
-        "step_ops": args.ops,
-        "route_expand_cast_GB_s": round(rec_gbs, 1),
-        "route_expand_cast_frac_of_peak": round(rec_gbs / peak, 4),
-        "step_routed_tokens_per_s": round(R * world / (step_ms * 1e-3), 1),
+        "data": "synthetic (seeded, no dataset)",
+        "config": config_dict(world),
+        "roofline": roofline(dom),
+        "roofline_headline": roofline(head_dom),
+        "configs": summaries,
+        "configs_note": "c0-c3 ms/us: one batch after a 512 MB L2 flush, median; sus: back to "
+                        "back, inputs not in L2, mean; c4: the timed steps; frac of measured peak",
+        "cpu_baseline": None if cpu is None else {
+            "value": cpu["value"], "unit": UNIT, "cores": cpu["cores"], "kind": "oracle",
+            "sample": cpu["sample_short"]},
+        "e2e": None if e2e is None else {
+            "value": e2e["value"], "unit": UNIT, "ms_per_step": e2e["ms_per_step"],
+            "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+            "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+            "link_bound_ms": e2e["link"]["copy_bound_ms_per_step"]},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "detail": None,
+    }
+    detail.update({
+        "line": {k2: v for k2, v in line.items() if k2 != "detail"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
         "breakdown": breakdown,
         "breakdown_timing": "per-op CUDA events in separate steps after the timed region (an "
                             "event between two kernels ends their launch overlap, so the "
                             "timed steps bracket only topk+route+expand and the whole step)",
-        "roofline": roofline,
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": int(launches),
-        "clocks": clk,
-        "peak_copy_GB_s": peak_copy,
-        "other_workloads": extra,
-    }
+        "route_expand_cast": {"ms": round(rec_ms_mean, 4), "GB_s": round(rec_gbs, 1),
+                              "frac_of_peak": round(rec_gbs / peak, 4),
+                              "frac_of_nominal": round(rec_gbs / NOMINAL_HBM_GBS, 4),
+                              "algorithmic_bytes": B["route_expand_cast"]},
+        "step_routed_tokens_per_s": round(R * world / (step_ms * 1e-3), 1),
+    })
+    if args.detail_out:
+        try:
+            os.makedirs(os.path.dirname(os.path.abspath(args.detail_out)), exist_ok=True)
+            with open(args.detail_out, "w") as f:
+                json.dump(detail, f, indent=1)
+            line["detail"] = args.detail_out
+        except OSError:
+            line["detail"] = None
     return line
 
 
@@ -441,7 +498,9 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
     h_x.copy_(x)
     names = ["scores", "x", "idx", "wt", "counts", "offsets", "pos", "src", "ws", "q", "sf"]
     slot0 = dict(zip(names, [scores, x, idx, wt, counts, offsets, pos, src, ws, q, sf]))
-    slots = [slot0, {n: torch.empty_like(t) for n, t in slot0.items()}]
+    # ws: the one-call path's workspace, whose control words start at zero
+    slots = [slot0, {n: (torch.zeros_like if n == "ws" else torch.empty_like)(t)
+                     for n, t in slot0.items()}]
     out_names = ["idx", "wt", "counts", "offsets", "pos", "src", "q", "sf"]
     h_outs = [[torch.empty_like(sl[n], device="cpu").pin_memory() for n in out_names]
               for sl in slots]
@@ -459,13 +518,11 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
         with torch.cuda.stream(st):
             sl["scores"].copy_(h_scores, non_blocking=True)
             sl["x"].copy_(h_x, non_blocking=True)
-            chk(L.moe_topk_gate(sl["scores"].data_ptr(), T, E, k, sl["idx"].data_ptr(),
-                                sl["wt"].data_ptr(), 1, p), "topk")
-            chk(L.moe_route_map(sl["idx"].data_ptr(), T, E, k, sl["counts"].data_ptr(),
-                                sl["offsets"].data_ptr(), sl["pos"].data_ptr(), sl["src"].data_ptr(),
-                                sl["ws"].data_ptr(), sl["ws"].numel(), p), "route")
-            chk(L.moe_expand_cast_fp8(sl["x"].data_ptr(), T, H, k, sl["pos"].data_ptr(), R,
-                                      sl["q"].data_ptr(), sl["sf"].data_ptr(), 128, p), "expand")
+            chk(L.moe_route_expand_cast_fp8(
+                sl["scores"].data_ptr(), T, E, k, sl["x"].data_ptr(), H, sl["idx"].data_ptr(),
+                sl["wt"].data_ptr(), sl["counts"].data_ptr(), sl["offsets"].data_ptr(),
+                sl["pos"].data_ptr(), sl["src"].data_ptr(), sl["q"].data_ptr(), sl["sf"].data_ptr(),
+                sl["ws"].data_ptr(), sl["ws"].numel(), 0, 128, p), "route_expand_cast")
             for h, n in zip(h_outs[i % 2], out_names):
                 h.copy_(sl[n], non_blocking=True)
 
@@ -517,7 +574,7 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
                      "copy_bound_ms_per_step": round(bound_ms, 3),
                      "note": "one direction at a time, best of 3; the step's copies cannot "
                              "finish sooner than the slower direction allows"},
-            "path": "pinned host -> device, C ABI topk_gate/route_map/expand_cast_fp8, "
+            "path": "pinned host -> device, C ABI moe_route_expand_cast_fp8 (AUTO), "
                     "all outputs -> pinned host; steps alternate between two streams"}
 
 
@@ -542,20 +599,23 @@ def measure_peak_copy(L, dev, stream, sp):
     return round(best, 1)
 
 
-def extra_workloads(L, dev, stream, sp, chk, args):
-    """The skewed-routing and SwiGLU workloads, each iteration after an L2
-    flush (a 512 MB device write outside the timed events)."""
+def other_configs(L, dev, stream, sp, chk, args, peak):
+    """The other benchmarked workloads, on rank 0: the tiny and decode
+    batches, the skewed routing and the SwiGLU rows, each with a compact
+    summary for the printed line; and the variant rows (two streams, the
+    padded layout, the scale options, FP4, more decode sizes) for the detail
+    file.  Each single-batch time is taken after an L2 flush (a 512 MB
+    device write outside the timed events), median of the iterations."""
     import torch
 
     from moe_routing_precision_gb300 import ops, workloads
-    peak, _ = load_peaks()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     iters = args.extra_iters
-    res = {}
+    summ, det = {}, {}
 
-    def timed(fn):
+    def timed(fn, n=iters):
         ts = []
-        for i in range(iters + 3):
+        for i in range(n + 3):
             flush.fill_(i & 0xFF)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -567,33 +627,66 @@ def extra_workloads(L, dev, stream, sp, chk, args):
                 ts.append(e0.elapsed_time(e1))
         return statistics.median(ts)
 
+    def back_to_back(fn, reps):
+        """Mean time per call of `reps` calls back to back (one before, untimed)."""
+        fn(0)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            fn(i)
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def frac(b, ms):
+        return round(b / (ms * 1e-3) / 1e9 / peak, 4)
+
+    def route_bufs(T, E, k, H):
+        R, G = T * k, H // 128
+        i32 = dict(dtype=torch.int32, device=dev)
+        return dict(idx=torch.empty(T, k, **i32), wt=torch.empty(T, k, device=dev),
+                    counts=torch.empty(E, **i32), offsets=torch.empty(E + 1, **i32),
+                    pos=torch.empty(T, k, **i32), src=torch.empty(R, **i32),
+                    ws=torch.empty(max(1, ops.route_map_workspace_bytes(T, E, k)),
+                                   dtype=torch.uint8, device=dev),
+                    ws1=torch.zeros(L.moe_route_expand_cast_fp8_workspace_bytes(T, E, k),
+                                    dtype=torch.uint8, device=dev),
+                    q=torch.empty(R, H, dtype=torch.uint8, device=dev),
+                    sf=torch.empty(R, G, device=dev))
+
+    def rec_call(b, s, x, T, E, k, H, p=sp, calls=False, mode=None):
+        """topk_gate + route_map + expand_cast_fp8: the one-call entry point
+        (AUTO, or `mode`), or with calls=True the three individual C-ABI calls."""
+        if not calls:
+            chk(L.moe_route_expand_cast_fp8(s.data_ptr(), T, E, k, x.data_ptr(), H,
+                                            b["idx"].data_ptr(), b["wt"].data_ptr(),
+                                            b["counts"].data_ptr(), b["offsets"].data_ptr(),
+                                            b["pos"].data_ptr(), b["src"].data_ptr(),
+                                            b["q"].data_ptr(), b["sf"].data_ptr(),
+                                            b["ws1"].data_ptr(), b["ws1"].numel(),
+                                            ops.PATH_AUTO if mode is None else mode, 128, p),
+                "route_expand_cast")
+            return
+        chk(L.moe_topk_gate(s.data_ptr(), T, E, k, b["idx"].data_ptr(), b["wt"].data_ptr(), 1, p),
+            "topk")
+        chk(L.moe_route_map(b["idx"].data_ptr(), T, E, k, b["counts"].data_ptr(),
+                            b["offsets"].data_ptr(), b["pos"].data_ptr(), b["src"].data_ptr(),
+                            b["ws"].data_ptr(), b["ws"].numel(), p), "route")
+        chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, b["pos"].data_ptr(), T * k,
+                                  b["q"].data_ptr(), b["sf"].data_ptr(), 128, p), "expand")
+
     def two_stream_batches(T, E, k, H, sets, reps):
         """Device time per batch of topk + route_map + expand_cast_fp8 with
         consecutive batches on two streams, each stream with its own routing
         and output buffers: every batch does all of its own work, and one
         batch's latency-bound routing overlaps the other's expand."""
-        R, G = T * k, H // 128
-        i32 = dict(dtype=torch.int32, device=dev)
-        bufs = [dict(idx=torch.empty(T, k, **i32), wt=torch.empty(T, k, device=dev),
-                     counts=torch.empty(E, **i32), offsets=torch.empty(E + 1, **i32),
-                     pos=torch.empty(T, k, **i32), src=torch.empty(R, **i32),
-                     ws=torch.empty(max(1, ops.route_map_workspace_bytes(T, E, k)),
-                                    dtype=torch.uint8, device=dev),
-                     q=torch.empty(R, H, dtype=torch.uint8, device=dev),
-                     sf=torch.empty(R, G, device=dev)) for _ in range(2)]
+        bufs = [route_bufs(T, E, k, H) for _ in range(2)]
         streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
 
         def one(i):
-            b, st = bufs[i % 2], streams[i % 2]
             si, xi = sets[i % len(sets)]
-            p = st.cuda_stream
-            chk(L.moe_topk_gate(si.data_ptr(), T, E, k, b["idx"].data_ptr(), b["wt"].data_ptr(), 1,
-                                p), "topk")
-            chk(L.moe_route_map(b["idx"].data_ptr(), T, E, k, b["counts"].data_ptr(),
-                                b["offsets"].data_ptr(), b["pos"].data_ptr(), b["src"].data_ptr(),
-                                b["ws"].data_ptr(), b["ws"].numel(), p), "route")
-            chk(L.moe_expand_cast_fp8(xi.data_ptr(), T, H, k, b["pos"].data_ptr(), R,
-                                      b["q"].data_ptr(), b["sf"].data_ptr(), 128, p), "expand")
+            rec_call(bufs[i % 2], si, xi, T, E, k, H, streams[i % 2].cuda_stream)
 
         for i in range(4):
             one(i)
@@ -616,149 +709,117 @@ def extra_workloads(L, dev, stream, sp, chk, args):
         del bufs
         return e0.elapsed_time(e1) / reps
 
+    # ---- configs[0], configs[1]: the tiny and decode batches through the
+    # one-call entry point (AUTO: the path measured fastest for the shape)
+    for key, name in (("c0_tiny", "tiny"), ("c1_decode_1k", "decode_1k")):
+        w = workloads.WORKLOADS[name]
+        d = decode_workload(L, dev, stream, sp, chk, flush, iters, peak, w=w)
+        det[name] = d
+        auto = d["auto"]
+        summ[key] = {"us": auto["us"], "frac": auto["frac_of_peak"]}
+
+    # ---- configs[2]: skewed routing (and its mild-skew variant, detail only)
     def skewed(name):
         w = workloads.WORKLOADS[name]
-        inp = workloads.make_inputs(w, seed=0, device=dev)
+        inp = workloads.make_inputs(w, seed=0, device=dev, with_y=(name == "skewed_8k"))
         s, x = inp["scores"], inp["x"]
-        T, E, k, H, R, G = w.T, w.E, w.k, w.H, w.R, w.G
-        i32 = dict(dtype=torch.int32, device=dev)
-        idx, wt = torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device=dev)
-        counts, offsets, pos, src = (torch.empty(E, **i32), torch.empty(E + 1, **i32),
-                                     torch.empty(T, k, **i32), torch.empty(R, **i32))
-        ws = torch.empty(max(1, ops.route_map_workspace_bytes(T, E, k)), dtype=torch.uint8, device=dev)
-        q = torch.empty(R, H, dtype=torch.uint8, device=dev)
-        sf = torch.empty(R, G, dtype=torch.float32, device=dev)
-
-        def rec():
-            chk(L.moe_topk_gate(s.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
-            chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
-                                pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
-            chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
-                                      sf.data_ptr(), 128, sp), "expand")
-
-        def exp_only():
-            chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
-                                      sf.data_ptr(), 128, sp), "expand")
-
-        ms = timed(rec)
-        ms_e = timed(exp_only)
+        T, E, k, H, R = w.T, w.E, w.k, w.H, w.R
+        b = route_bufs(T, E, k, H)
         B = algorithmic_bytes(T, E, k, H)
-        gbs = B["route_expand_cast"] / (ms * 1e-3) / 1e9
-        gbs_e = B["expand_cast_fp8"] / (ms_e * 1e-3) / 1e9
-        # sustained: back-to-back batches over NSETS independent input sets (seeds
-        # 0..NSETS-1), so each batch's 125 MB of inputs was last touched NSETS-1
-        # batches (~1.8 GB of traffic) ago and is no longer in L2
+        ms = timed(lambda: rec_call(b, s, x, T, E, k, H))
+        ms_c = timed(lambda: rec_call(b, s, x, T, E, k, H, calls=True))
+        ms_ch = timed(lambda: rec_call(b, s, x, T, E, k, H, mode=ops.PATH_CHAINED))
+        ms_e = timed(lambda: chk(L.moe_expand_cast_fp8(x.data_ptr(), T, H, k, b["pos"].data_ptr(),
+                                                       R, b["q"].data_ptr(), b["sf"].data_ptr(),
+                                                       128, sp), "expand"))
+        # sustained: back-to-back batches over NSETS independent input sets
+        # (seeds 0..NSETS-1), so each batch's inputs were last touched NSETS-1
+        # batches (~1.8 GB of traffic) ago and are no longer in L2
         nsets = 4
         sets = [(s, x)] + [(d["scores"], d["x"]) for d in
                            (workloads.make_inputs(w, seed=i, device=dev) for i in range(1, nsets))]
-
-        def rec_set(i):
-            si, xi = sets[i % nsets]
-            chk(L.moe_topk_gate(si.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
-            chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
-                                pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
-            chk(L.moe_expand_cast_fp8(xi.data_ptr(), T, H, k, pos.data_ptr(), R, q.data_ptr(),
-                                      sf.data_ptr(), 128, sp), "expand")
-
         reps = max(8, 2 * iters)
-        for i in range(nsets):
-            rec_set(i)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(reps):
-            rec_set(i)
-        e1.record(stream)
-        e1.synchronize()
-        ms_s = e0.elapsed_time(e1) / reps
-        gbs_s = B["route_expand_cast"] / (ms_s * 1e-3) / 1e9
+        ms_s = back_to_back(lambda i: rec_call(b, sets[i % nsets][0], sets[i % nsets][1], T, E, k, H),
+                            reps)
         ms_2 = two_stream_batches(T, E, k, H, sets, reps)
-        gbs_2 = B["route_expand_cast"] / (ms_2 * 1e-3) / 1e9
-        res[name] = {"op": "route+expand+cast",
-                            "single_shot": {"ms": round(ms, 4),
-                                            "routed_tokens_per_s": round(R / (ms * 1e-3), 1),
-                                            "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                                            "timing": "one batch after a 512 MB L2 flush, median"},
-                            "sustained": {"ms": round(ms_s, 4),
-                                          "routed_tokens_per_s": round(R / (ms_s * 1e-3), 1),
-                                          "GB_s": round(gbs_s, 1),
-                                          "frac_of_peak": round(gbs_s / peak, 4),
-                                          "timing": f"{reps} batches back to back over {nsets} input "
-                                                    "sets (inputs not in L2), mean"},
-                            "sustained_two_streams": {
-                                "ms": round(ms_2, 4), "routed_tokens_per_s": round(R / (ms_2 * 1e-3), 1),
-                                "GB_s": round(gbs_2, 1), "frac_of_peak": round(gbs_2 / peak, 4),
-                                "timing": f"{reps} batches, consecutive ones on two streams with their "
-                                          "own buffers (one batch's routing overlaps the other's "
-                                          "expand), mean per batch"},
-                            "expand_only_ms": round(ms_e, 4), "expand_only_GB_s": round(gbs_e, 1),
-                            "skew": workloads.skew_stats(counts.cpu())}
+        r = {"single_ms": round(ms, 4), "single_frac": frac(B["route_expand_cast"], ms),
+             "single_calls_ms": round(ms_c, 4),
+             "single_calls_frac": frac(B["route_expand_cast"], ms_c),
+             "single_chained_ms": round(ms_ch, 4),
+             "single_chained_frac": frac(B["route_expand_cast"], ms_ch),
+             "sustained_ms": round(ms_s, 4), "sustained_frac": frac(B["route_expand_cast"], ms_s),
+             "two_streams_ms": round(ms_2, 4),
+             "two_streams_frac": frac(B["route_expand_cast"], ms_2),
+             "expand_only_ms": round(ms_e, 4), "expand_only_frac": frac(B["expand_cast_fp8"], ms_e),
+             "skew": workloads.skew_stats(b["counts"].cpu()),
+             "timing": "single: one batch after a 512 MB L2 flush, median (the one-call entry "
+                       "point, AUTO; single_calls: the three individual calls); sustained: batches "
+                       f"back to back over {nsets} input sets (inputs not in L2), mean; two "
+                       "streams: consecutive batches on two streams with their own buffers, mean"}
+        if "y" in inp:
+            out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+            ms_cb = timed(lambda: chk(L.moe_combine(inp["y"].data_ptr(), b["wt"].data_ptr(),
+                                                   b["pos"].data_ptr(), T, H, k, R, out.data_ptr(),
+                                                   0, sp), "combine"))
+            r["combine_ms"] = round(ms_cb, 4)
+            r["combine_frac"] = frac(B["combine"], ms_cb)
+        del inp, sets, b
+        torch.cuda.empty_cache()
+        return r
 
-    skewed("skewed_8k")
-    torch.cuda.empty_cache()
-    skewed("skewed_8k_mild")
-    torch.cuda.empty_cache()
-    # the headline workload with consecutive steps on two streams (each step
-    # still does all of its own work; one step's routing overlaps the other's
-    # expand), beside the one-stream headline
-    wp = workloads.WORKLOADS[WORKLOAD]
-    pin = workloads.make_inputs(wp, seed=0, device=dev)
-    reps_p = max(8, iters)
-    ms_p = two_stream_batches(wp.T, wp.E, wp.k, wp.H, [(pin["scores"], pin["x"])], reps_p)
-    Bp = algorithmic_bytes(wp.T, wp.E, wp.k, wp.H)["route_expand_cast"]
-    gbs_p = Bp / (ms_p * 1e-3) / 1e9
-    res[f"{WORKLOAD}_two_streams"] = {
-        "op": "topk + route_map + expand_cast_fp8, consecutive steps on two streams",
-        "ms": round(ms_p, 4), "routed_tokens_per_s": round(wp.R / (ms_p * 1e-3), 1),
-        "GB_s": round(gbs_p, 1), "frac_of_peak": round(gbs_p / peak, 4),
-        "timing": f"{reps_p} steps, each with its own routing and output buffers per stream, "
-                  "mean per step (inputs larger than L2)"}
-    del pin
-    torch.cuda.empty_cache()
+    det["skewed_8k"] = sk = skewed("skewed_8k")
+    summ["c2_skewed_8k"] = {
+        "ms": sk["single_ms"], "frac": sk["single_frac"], "sus_ms": sk["sustained_ms"],
+        "sus_frac": sk["sustained_frac"], "combine_frac": sk.get("combine_frac"),
+        "experts_half": sk["skew"]["experts_taking_half"], "empty": sk["skew"]["empty_experts"]}
+    det["skewed_8k_mild"] = skewed("skewed_8k_mild")
+
+    # ---- configs[3]: SwiGLU rows
     w = workloads.WORKLOADS["swiglu_64k"]
     hx = workloads.make_inputs(w, seed=0, device=dev)["swiglu_x"]
     M, N = w.M, w.N
     q2 = torch.empty(M, N, dtype=torch.uint8, device=dev)
     sf2 = torch.empty(M, N // 128, dtype=torch.float32, device=dev)
-    def sw():
+
+    def sw(i=0):
         chk(L.swiglu_cast_fp8(hx.data_ptr(), M, N, q2.data_ptr(), sf2.data_ptr(), 128, sp), "swiglu")
 
     ms = timed(sw)
     bsw = M * 2 * N * 2 + M * N + M * (N // 128) * 4
-    gbs = bsw / (ms * 1e-3) / 1e9
     # sustained: back to back; the 537 MB input exceeds L2, so each pass
     # starts on lines the previous pass evicted
-    reps = max(8, 2 * iters)
-    sw()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        sw()
-    e1.record(stream)
-    e1.synchronize()
-    ms_s = e0.elapsed_time(e1) / reps
-    gbs_s = bsw / (ms_s * 1e-3) / 1e9
-    res["swiglu_64k"] = {"op": "swiglu_cast_fp8",
-                         "single_shot": {"ms": round(ms, 4), "rows_per_s": round(M / (ms * 1e-3), 1),
-                                         "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                                         "timing": "after a 512 MB L2 flush, median"},
-                         "sustained": {"ms": round(ms_s, 4),
-                                       "rows_per_s": round(M / (ms_s * 1e-3), 1),
-                                       "GB_s": round(gbs_s, 1), "frac_of_peak": round(gbs_s / peak, 4),
-                                       "timing": f"{reps} passes back to back, mean"}}
+    ms_s = back_to_back(sw, max(8, 2 * iters))
+    det["swiglu_64k"] = {"single_ms": round(ms, 4), "single_frac": frac(bsw, ms),
+                         "sustained_ms": round(ms_s, 4), "sustained_frac": frac(bsw, ms_s),
+                         "rows_per_s": round(M / (ms * 1e-3), 1), "algorithmic_bytes": bsw}
+    summ["c3_swiglu_64k"] = {"ms": round(ms, 4), "frac": frac(bsw, ms), "sus_ms": round(ms_s, 4),
+                             "sus_frac": frac(bsw, ms_s)}
     del hx, q2, sf2
     torch.cuda.empty_cache()
-    res["prefill_64k_padded"] = padded_workload(L, dev, stream, sp, chk, flush, iters, peak)
+
+    # ---- detail only: the large prefill on two streams, the padded layout,
+    # the scale options and FP4, more decode sizes
+    wp = workloads.WORKLOADS[WORKLOAD]
+    pin = workloads.make_inputs(wp, seed=0, device=dev)
+    reps_p = max(8, iters)
+    ms_p = two_stream_batches(wp.T, wp.E, wp.k, wp.H, [(pin["scores"], pin["x"])], reps_p)
+    Bp = algorithmic_bytes(wp.T, wp.E, wp.k, wp.H)["route_expand_cast"]
+    det[f"{WORKLOAD}_two_streams"] = {"ms": round(ms_p, 4), "frac": frac(Bp, ms_p),
+                                      "timing": f"{reps_p} steps on two streams, mean per step"}
+    del pin
     torch.cuda.empty_cache()
-    res.update(cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak))
+    det["prefill_64k_padded"] = padded_workload(L, dev, stream, sp, chk, flush, iters, peak)
     torch.cuda.empty_cache()
-    res["decode_1k"] = decode_workload(L, dev, stream, sp, chk, flush, iters, peak)
+    det.update(cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak))
+    torch.cuda.empty_cache()
+    base = workloads.WORKLOADS["decode_1k"]
     for t in (64, 256):
-        res[f"decode_{t}"] = decode_workload(L, dev, stream, sp, chk, flush, iters, peak, T=t)
+        det[f"decode_{t}"] = decode_workload(
+            L, dev, stream, sp, chk, flush, iters, peak,
+            w=workloads.Workload(f"decode_{t}", T=t, E=base.E, k=base.k, H=base.H))
     del flush
     torch.cuda.empty_cache()
-    return res
+    return summ, det
 
 
 def padded_workload(L, dev, stream, sp, chk, flush, iters, peak, align=128):
@@ -940,21 +1001,17 @@ def cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak):
     return res
 
 
-def decode_workload(L, dev, stream, sp, chk, flush, iters, peak, T=1024):
-    """route + expand + cast of a decode batch of T tokens (E=256, k=8,
-    H=4096, the decode_1k recipe) through moe_route_expand_cast_fp8: the
-    separate launches (chained by programmatic dependent launch; three up to
-    T = 1024, where the route map is one launch, else four), the same
-    captured in a CUDA graph, the fused single cooperative launch, and the
-    replicated-routing path (one launch for T <= 32, else the top-k launch and
-    one more) where the shape allows each.  Each timed
-    after a 512 MB L2 flush that also keeps the GPU busy while the host
-    enqueues (device time only)."""
+def decode_workload(L, dev, stream, sp, chk, flush, iters, peak, w):
+    """route + expand + cast of a small batch `w` through the one-call entry
+    point moe_route_expand_cast_fp8: AUTO (what a caller gets), the separate
+    launches (chained by programmatic dependent launch), the same captured in
+    a CUDA graph, the fused single cooperative launch and the
+    replicated-routing path, where the shape allows each.  Each timed after a
+    512 MB L2 flush that also keeps the GPU busy while the host enqueues
+    (device time only)."""
     import torch
 
     from moe_routing_precision_gb300 import ops, workloads
-    base = workloads.WORKLOADS["decode_1k"]
-    w = workloads.Workload(f"decode_{T}", T=T, E=base.E, k=base.k, H=base.H)
     inp = workloads.make_inputs(w, seed=0, device=dev)
     s, x = inp["scores"], inp["x"]
     T, E, k, H, R, G = w.T, w.E, w.k, w.H, w.R, w.G
@@ -966,12 +1023,14 @@ def decode_workload(L, dev, stream, sp, chk, flush, iters, peak, T=1024):
     sf = torch.empty(R, G, dtype=torch.float32, device=dev)
     ws = ops.route_expand_cast_workspace(T, E, k, x)
 
+    def raw(mode, st=sp):
+        return L.moe_route_expand_cast_fp8(s.data_ptr(), T, E, k, x.data_ptr(), H, idx.data_ptr(),
+                                           wt.data_ptr(), counts.data_ptr(), offsets.data_ptr(),
+                                           pos.data_ptr(), src.data_ptr(), q.data_ptr(),
+                                           sf.data_ptr(), ws.data_ptr(), ws.numel(), mode, 128, st)
+
     def call(mode, st=sp):
-        chk(L.moe_route_expand_cast_fp8(s.data_ptr(), T, E, k, x.data_ptr(), H, idx.data_ptr(),
-                                        wt.data_ptr(), counts.data_ptr(), offsets.data_ptr(),
-                                        pos.data_ptr(), src.data_ptr(), q.data_ptr(),
-                                        sf.data_ptr(), ws.data_ptr(), ws.numel(), mode, 128, st),
-            "route_expand_cast")
+        chk(raw(mode, st), "route_expand_cast")
 
     def timed(fn):
         ts = []
@@ -989,22 +1048,26 @@ def decode_workload(L, dev, stream, sp, chk, flush, iters, peak, T=1024):
 
     res = {"op": f"topk + route_map + expand_cast_fp8 (T={T}, E={E}, k={k}, H={H})"}
     B = algorithmic_bytes(T, E, k, H)["route_expand_cast"]
-    sep = timed(lambda: call(ops.PATH_SEPARATE))
-    fused = timed(lambda: call(ops.PATH_FUSED))
-    rep = timed(lambda: call(ops.PATH_REPLICATED)) if T <= 2048 else None
+    times = {"auto": timed(lambda: call(ops.PATH_AUTO)),
+             "separate_launches": timed(lambda: call(ops.PATH_SEPARATE))}
+    for name, mode in (("fused_single_launch", ops.PATH_FUSED),
+                       ("replicated_routing", ops.PATH_REPLICATED),
+                       ("chained", ops.PATH_CHAINED)):
+        rc = raw(mode)
+        if rc == ops.MOE_ERR_UNSUPPORTED:
+            continue
+        chk(rc, name)
+        times[name] = timed(lambda m=mode: call(m))
     call(ops.PATH_SEPARATE)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     cs = torch.cuda.Stream(device=dev)
     with torch.cuda.graph(g, stream=cs):
         call(ops.PATH_SEPARATE, cs.cuda_stream)
-    graph = timed(lambda: g.replay())
+    times["separate_in_cuda_graph"] = timed(lambda: g.replay())
     if L.moe_get_device_status(sp, None) != 0:
         raise RuntimeError("device error in the decode workload")
-    for name, us in (("separate_launches", sep), ("separate_in_cuda_graph", graph),
-                     ("fused_single_launch", fused), ("replicated_routing", rep)):
-        if us is None:
-            continue
+    for name, us in times.items():
         gbs = B / (us * 1e-6) / 1e9
         res[name] = {"us": round(us, 2), "routed_tokens_per_s": round(R / (us * 1e-6), 1),
                      "GB_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
@@ -1081,6 +1144,7 @@ def cpu_baseline_leg(scores, x, k, E, total=65536, single_tokens=16384):
             "sample": f"all {T} of {total} tokens of the benchmarked workload (topk_gate + "
                       f"route_map + expand_cast_fp8), {n} threads over token shards (route map "
                       f"serial), best of 2 passes, {dt:.2f} s",
+            "sample_short": f"all {T} tokens, {n} threads, best of 2 passes ({dt:.2f} s)",
             "single_thread": {"value": round(ts * k / dt1, 1), "unit": UNIT, "cores": 1,
                               "sample": f"first {ts} tokens, one thread, {dt1:.1f} s"}}
 
@@ -1109,12 +1173,13 @@ def cpu_model() -> str:
 
 # ---------------------------------------------------------------- reference arm
 
+
+# ---------------------------------------------------------------- reference arm
+
 def reference_arm(args):
     """The oracle timed on the host cores (all host threads, token shards),
-    same metric and workload, each step a bounded sample (--ref-tokens tokens)
-    of the large-prefill workload."""
-    import torch
-
+    same metric and workload: every step is one pass over all tokens of the
+    large-prefill batch (rank 0's: seed 0), drawn on the host."""
     import oracle
     from moe_routing_precision_gb300 import workloads
     rank, world, _ = dist_env()
@@ -1122,11 +1187,13 @@ def reference_arm(args):
         return None
     oracle.build()
     w = workloads.WORKLOADS[WORKLOAD]
-    tokens = args.ref_tokens
-    sub = workloads.Workload(w.name, T=tokens, E=w.E, k=w.k, H=w.H, bias=w.bias, x_std=w.x_std)
-    inp = workloads.make_inputs(sub, seed=0, device="cpu")
+    tokens = w.T if args.ref_tokens <= 0 else min(w.T, args.ref_tokens)
+    sub = w if tokens == w.T else workloads.Workload(w.name, T=tokens, E=w.E, k=w.k, H=w.H,
+                                                     bias=w.bias, x_std=w.x_std)
+    inp = workloads.make_inputs(sub, seed=shard_seed(rank), device="cpu")
     s = inp["scores"].numpy()
     xb = oracle.bf16_bits(inp["x"])
+    del inp
 
     n = host_threads()
     chain = OracleChain(s, xb, w.k, w.E, threads=n)
@@ -1135,20 +1202,18 @@ def reference_arm(args):
     dt = sum(chain.run() for _ in range(args.steps)) / args.steps
     chain.close()
     value = tokens * w.k / dt
-    del torch
+    sample = (f"all {tokens} tokens per step" if tokens == w.T else
+              f"{tokens} of {w.T} tokens per step") + \
+        f" (topk_gate + route_map + expand_cast_fp8), the C oracle on {n} threads over token " \
+        "shards (route map serial)"
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32 (CPU oracle)", "data": "synthetic",
-        "config": {"workload": f"large prefill T=65536 E=256 k=8 H=7168, bounded sample of "
-                               f"{tokens} tokens per step", "T": tokens, "E": w.E, "k": w.k,
-                   "H": w.H},
+        "config": config_dict(world),
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": n, "kind": "oracle",
-                         "cpu": cpu_model(), "host_cores": os.cpu_count(),
-                         "sample": f"{tokens} tokens per step (topk_gate + route_map + "
-                                   f"expand_cast_fp8), the C oracle on {n} threads over token "
-                                   f"shards (route map serial)"},
+                         "cpu": cpu_model(), "host_cores": os.cpu_count(), "sample": sample},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -1163,12 +1228,18 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--extra-iters", type=int, default=30)
-    ap.add_argument("--ref-tokens", type=int, default=8192)
+    ap.add_argument("--ref-tokens", type=int, default=0,
+                    help="reference arm: tokens per step (0: the whole workload)")
     ap.add_argument("--workload", choices=["prefill_64k", "skewed_8k", "decode_1k", "tiny"],
                     default=WORKLOAD)
     ap.add_argument("--ops", choices=["all", "route_expand_cast"], default="all",
                     help="all: the whole step (route+expand+cast, SwiGLU, combine); "
                          "route_expand_cast: the headline ops only")
+    ap.add_argument("--headline-path", choices=["one_call", "calls"], default="one_call",
+                    help="route+expand+cast as the one-call entry point (AUTO) or as the three "
+                         "individual calls")
+    ap.add_argument("--detail-out", default=DETAIL_DEFAULT,
+                    help="where the long-form results go ('' to skip)")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1177,7 +1248,7 @@ def main():
         ap.error("--warmup must be >= 3")
     line = reference_arm(args) if args.impl == "reference" else gpu_arm(args)
     if line is not None:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, separators=(",", ":")), flush=True)
 
 
 if __name__ == "__main__":

@@ -109,6 +109,7 @@ typedef enum moe_out_dtype {
 #define MOE_PATH_FUSED 1      /* one cooperative launch (decode shapes only)              */
 #define MOE_PATH_SEPARATE 2   /* moe_topk_gate + moe_route_map + moe_expand_cast_fp8     */
 #define MOE_PATH_REPLICATED 3 /* one ordinary launch, routing repeated per block (small T) */
+#define MOE_PATH_CHAINED 4    /* three launches: top-k + chunk ranks, a scan, the expand   */
 #define MOE_AUTO_REPLICATED_MAX_TOKENS 1024 /* AUTO's switch from REPLICATED to SEPARATE  */
 
 /*
@@ -435,7 +436,14 @@ moe_status_t moe_combine(const void *y, const float *topk_weights,
  * kernel runs first and a second launch does the rest.  It applies to
  * T <= 2048, T*k <= 16384, 32 < E <= 256, k <= 32, H <= 8192.  The SEPARATE
  * path is the launches of the individual calls (three or four: the route map
- * is one launch for T <= 1024).
+ * is one launch for T <= 1024).  The CHAINED path is three launches: the
+ * top-k kernel, one CTA per chunk of 16 to 64 consecutive tokens, also counts
+ * each chunk's copies per expert and ranks every copy among its expert's
+ * copies in the chunk; a scan turns the counts into per-chunk bases; the
+ * expand kernel places every copy itself (expert offset + chunk base + rank),
+ * writing pos, sorted_src and offsets, then stores the rows.  It applies to
+ * 32 < E <= 256, k <= 32, H <= 16384 with H/128 % 4 == 0 and 16-byte aligned
+ * out and out_sf.
  *   scores [T,E] f32; x [T,H] bf16; topk_idx [T,k] i32; topk_weights [T,k]
  *   f32; counts [E], offsets [E+1], pos [T,k], sorted_src [T*k] i32;
  *   out [T*k,H] u8; out_sf [T*k,H/128] f32.
@@ -444,8 +452,9 @@ moe_status_t moe_combine(const void *y, const float *topk_weights,
  *   control words: ZERO them once before the first call (each call leaves
  *   them zero; after a MOE_DEVERR_TIMEOUT, zero them again).  One workspace
  *   must not be used by two calls in flight at once.
- *   mode: MOE_PATH_AUTO, MOE_PATH_FUSED or MOE_PATH_REPLICATED
- *   (MOE_ERR_UNSUPPORTED where they do not apply) or MOE_PATH_SEPARATE.  AUTO
+ *   mode: MOE_PATH_AUTO, MOE_PATH_FUSED, MOE_PATH_REPLICATED or
+ *   MOE_PATH_CHAINED (MOE_ERR_UNSUPPORTED where they do not apply) or
+ *   MOE_PATH_SEPARATE.  AUTO
  *   takes the path measured fastest on GB300 for the shape: REPLICATED for
  *   T <= MOE_AUTO_REPLICATED_MAX_TOKENS where it applies (E = 256, k = 8,
  *   H = 4096, one call: 8.8 against 14.0 us at T = 16, 12.9 against 14.0 at
@@ -455,7 +464,9 @@ moe_status_t moe_combine(const void *y, const float *topk_weights,
  *   (the separate launches, chained by programmatic dependent launch, were
  *   as fast as the FUSED launch for T <= 64 and faster above: its single
  *   routing block and the cooperative launch cost more than the gaps they
- *   remove).
+ *   remove; and 1-2 % faster than CHAINED at T = 1024 to 65536: the chained
+ *   top-k kernel, the scan and the expand's placement step take longer than
+ *   the route map's two launches they replace).
  * Requirements as the individual calls; group == 128.
  */
 moe_status_t moe_route_expand_cast_fp8(const float *scores, int64_t num_tokens,

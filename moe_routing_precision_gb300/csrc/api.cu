@@ -28,6 +28,11 @@ thread_local char g_last_cuda_error[256] = "no CUDA error";
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Control words of moe_route_expand_cast_fp8's workspace (its first 256
+// bytes): words 0 and 1 belong to the fused decode launch, this one to the
+// chained path's scan.
+constexpr int kChainArrivalWord = 16;
+
 bool experts_ok(int32_t E, int32_t k) {
   return E >= 1 && E <= MOE_MAX_EXPERTS && k >= 1 && k <= MOE_MAX_TOPK && k <= E;
 }
@@ -445,7 +450,9 @@ moe_status_t moe_combine(const void* y, const float* topk_weights, const int32_t
 
 size_t moe_route_expand_cast_fp8_workspace_bytes(int64_t num_tokens, int32_t num_experts,
                                                  int32_t num_topk) {
-  return 256 + moe_route_map_workspace_bytes(num_tokens, num_experts, num_topk);
+  const size_t route = moe_route_map_workspace_bytes(num_tokens, num_experts, num_topk);
+  const size_t chain = route_chain_workspace_bytes(num_tokens, num_experts);
+  return 256 + (route > chain ? route : chain);
 }
 
 moe_status_t moe_route_expand_cast_fp8(const float* scores, int64_t num_tokens,
@@ -457,7 +464,7 @@ moe_status_t moe_route_expand_cast_fp8(const float* scores, int64_t num_tokens,
                                        int32_t group, void* stream) {
   if (group != MOE_CAST_GROUP) return MOE_ERR_UNSUPPORTED;
   if (mode != MOE_PATH_AUTO && mode != MOE_PATH_FUSED && mode != MOE_PATH_SEPARATE &&
-      mode != MOE_PATH_REPLICATED)
+      mode != MOE_PATH_REPLICATED && mode != MOE_PATH_CHAINED)
     return MOE_ERR_INVALID_ARG;
   if (num_tokens < 0 || !experts_ok(num_experts, num_topk)) return MOE_ERR_INVALID_ARG;
   if (hidden < MOE_CAST_GROUP || hidden % MOE_CAST_GROUP != 0) return MOE_ERR_INVALID_ARG;
@@ -484,10 +491,22 @@ moe_status_t moe_route_expand_cast_fp8(const float* scores, int64_t num_tokens,
       decode_fused_smem(num_tokens, num_experts, num_topk, hidden, c.num_sms, nullptr, nullptr) > 0;
   const bool replicated_ok =
       num_tokens > 0 && decode_replicated_ok(num_tokens, num_experts, num_topk, hidden);
+  const bool chained_ok =
+      num_tokens > 0 && route_chain_ok(num_tokens, num_experts, num_topk, hidden, out, out_sf);
   if (mode == MOE_PATH_FUSED && !fused_ok && num_tokens > 0) return MOE_ERR_UNSUPPORTED;
   if (mode == MOE_PATH_REPLICATED && !replicated_ok && num_tokens > 0) return MOE_ERR_UNSUPPORTED;
+  if (mode == MOE_PATH_CHAINED && !chained_ok && num_tokens > 0) return MOE_ERR_UNSUPPORTED;
   if (mode == MOE_PATH_AUTO && replicated_ok && num_tokens <= MOE_AUTO_REPLICATED_MAX_TOKENS)
     mode = MOE_PATH_REPLICATED;
+  if (mode == MOE_PATH_CHAINED && chained_ok) {
+    cudaError_t e = launch_route_chain(c, scores, num_tokens, num_experts, num_topk, x, hidden,
+                                       topk_idx, topk_weights, counts, offsets, pos, sorted_src,
+                                       out, out_sf,
+                                       reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
+                                                                  256),
+                                       static_cast<unsigned*>(workspace) + kChainArrivalWord);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+  }
   if (mode == MOE_PATH_REPLICATED && replicated_ok) {
     cudaError_t e = launch_decode_replicated(c, scores, num_tokens, num_experts, num_topk, x,
                                              hidden, topk_idx, topk_weights, counts, offsets, pos,

@@ -389,6 +389,38 @@ cudaError_t launch_expand_cast_fp4(const LaunchCtx& c, const void* x, int64_t T,
 cudaError_t launch_sf_gather(const LaunchCtx& c, const int32_t* src, int64_t R, int64_t T, int k,
                              int G, SfOut sfo, void* out_sf);
 
+// The chained route + expand (route_chain.cu): the top-k kernel leaves, in
+// pos, each copy's rank among its expert's copies within its chunk of
+// consecutive tokens and writes one histogram row per chunk; a column scan
+// turns the histogram into base[chunk][e], the copies of expert e in earlier
+// chunks, and writes counts and offsets; the expand kernel then places every
+// copy itself:
+//   pos = offsets[e] + base[chunk][e] + rank in chunk,
+// and writes pos and sorted_src before it stores the rows.
+struct RouteChain {
+  const int32_t* idx = nullptr;      // [T, k] experts of each token
+  const int32_t* base = nullptr;     // [chunks, E]
+  const int32_t* offsets = nullptr;  // [E + 1]
+  int32_t* sorted_src = nullptr;     // [T * k], written
+  int E = 0;
+  int chunk_shift = 0;               // chunk = 1 << chunk_shift tokens
+};
+// The expand kernel's chained form (expand_cast.cu): plain E4M3 with f32
+// row-major scales; needs H <= 16384, H / 128 % 4 == 0, 16-byte aligned out
+// and out_sf, E <= 256.
+cudaError_t launch_expand_cast_chain(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
+                                     int32_t* pos, uint8_t* out, float* out_sf,
+                                     const RouteChain& rc);
+// The whole chain (route_chain.cu); hist: (T >> chunk_shift rounded up) * E
+// int32 of workspace (route_chain_workspace_bytes).
+bool route_chain_ok(int64_t T, int E, int k, int H, const void* out, const void* out_sf);
+size_t route_chain_workspace_bytes(int64_t T, int E);
+// arrivals: a 32-bit counter that is zero before the call (left at zero).
+cudaError_t launch_route_chain(const LaunchCtx& c, const float* scores, int64_t T, int E, int k,
+                               const void* x, int H, int32_t* idx, float* w, int32_t* counts,
+                               int32_t* offsets, int32_t* pos, int32_t* src, uint8_t* out,
+                               float* out_sf, int32_t* hist, unsigned* arrivals);
+
 cudaError_t launch_expand_cast(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                                const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
                                const int32_t* zero_rows = nullptr, SfOut sfo = SfOut());

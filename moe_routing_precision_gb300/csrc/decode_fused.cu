@@ -233,9 +233,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(DecodeArgs
 
   // top-k + weights, one warp per token; token t on block t % grid (warp
   // t / grid), so every block selects about T / grid tokens
+  uint32_t sel_e;
   for (int t = (int)blockIdx.x + wib * nblk; t < a.T; t += nblk * kDecWarps)
     topk_token<V, VEC, KMAX>(a.scores + (int64_t)t * a.E, a.E, k, lane, s_list[wib], s_cand[wib],
-                             a.idx + (int64_t)t * k, a.w != nullptr ? a.w + (int64_t)t * k : nullptr);
+                             a.idx + (int64_t)t * k, a.w != nullptr ? a.w + (int64_t)t * k : nullptr,
+                             sel_e);
 
   for (int s0 = 0; s0 < S; s0 += kDecThreads * kSlices) {
     if (s0 > 0) load_batch(s0);

@@ -131,10 +131,11 @@ __global__ void __launch_bounds__(kRepThreads, 1) decode_replicated_kernel(RepAr
   for (int i = tid; i < W * E; i += kRepThreads) bm[i] = 0u;
 
   // ---- 1: the experts of every token (block 0: also the weights)
+  uint32_t sel_e;
   for (int tt = wib; tt < T; tt += kRepWarps)
     topk_token<V, VEC, KMAX>(a.scores + (int64_t)tt * E, E, k, lane, s_list[wib], s_cand[wib],
                              s_idx + tt * k,
-                             (b0 && a.w != nullptr) ? a.w + (int64_t)tt * k : nullptr);
+                             (b0 && a.w != nullptr) ? a.w + (int64_t)tt * k : nullptr, sel_e);
   __syncthreads();
 
   // ---- 2: the route map.  Bit (t % 32) of bm[t / 32][e] <=> token t chose e;

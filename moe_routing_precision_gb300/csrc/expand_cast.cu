@@ -256,11 +256,52 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
 // the padding rows (zsrc non-null) is.  The plain form (row-major f32 scales,
 // copied in bulk with the codes; no padding) keeps fewer registers, so more
 // CTAs are resident.
-template <int TOK, bool OPTS, bool ZF>
+// The chained form's prologue (warp 0, CHAIN): each of the CTA's copies is
+// placed at offsets[e] + base[chunk][e] (the copies of expert e in earlier
+// chunks) + its rank among its expert's copies in the chunk (held in pos on
+// entry); pos and sorted_src are written and lane j of pv[i] gets the row of
+// token t0 + i's copy j.
+template <int TOK>
+__device__ __forceinline__ void chain_place(const RouteChain& rc, int64_t t0, int64_t T, int k,
+                                            int64_t R, int32_t* __restrict__ pos, int lane,
+                                            int32_t (&pv)[TOK], bool& bad) {
+  const int E = rc.E;
+  int32_t e[TOK], lr[TOK];
+#pragma unroll
+  for (int i = 0; i < TOK; ++i) {  // the ids and ranks first: the other loads need the ids
+    const int64_t t = t0 + i;
+    const bool on = t < T && lane < k;
+    e[i] = on ? __ldg(rc.idx + t * k + lane) : -1;
+    lr[i] = on ? pos[t * k + lane] : 0;
+  }
+#pragma unroll
+  for (int i = 0; i < TOK; ++i) {
+    pv[i] = -1;
+    const int64_t t = t0 + i;
+    if (t >= T || lane >= k) continue;
+    if ((unsigned)e[i] >= (unsigned)E) {  // never from the top-k kernel: flag, skip
+      pos[t * k + lane] = -1;
+      bad = true;
+      continue;
+    }
+    const int32_t p = __ldg(rc.offsets + e[i]) +
+                      __ldg(rc.base + (t >> rc.chunk_shift) * E + e[i]) + lr[i];
+    if (p < 0 || (int64_t)p >= R) {
+      pos[t * k + lane] = -1;
+      bad = true;
+      continue;
+    }
+    pos[t * k + lane] = p;
+    rc.sorted_src[p] = (int32_t)(t * k + lane);
+    pv[i] = p;
+  }
+}
+
+template <int TOK, bool OPTS, bool ZF, bool CHAIN>
 __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
     int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf,
-    const int32_t* __restrict__ zsrc, SfOut sfo, unsigned* err) {
+    const int32_t* __restrict__ zsrc, SfOut sfo, RouteChain rc, unsigned* err) {
   extern __shared__ __align__(128) uint8_t s_buf[];
   pdl_enter();
   const int P = H >> 4;  // threads per token
@@ -299,9 +340,11 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
           b[i] = ld_stream_v4(src + 8);
         }
       }
-      if (tid < 32 && lane < k) pv[i] = __ldg(pos + t * k + lane);
+      if (!CHAIN && tid < 32 && lane < k) pv[i] = __ldg(pos + t * k + lane);
     }
   }
+  if (CHAIN && tid < 32)  // the x loads above are in flight meanwhile
+    chain_place<TOK>(rc, t0, T, k, R, const_cast<int32_t*>(pos), lane, pv, bad);
   float sfv[TOK];
 #pragma unroll
   for (int i = 0; i < TOK; ++i) {
@@ -376,20 +419,25 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
 // 0.80 ms and 104 us for a persistent grid of 3 CTAs per SM that strode over
 // the tokens with the next token's loads in flight.  The persistent grid kept
 // the accesses in flight at any moment spread over the whole of x and q; here
-// the CTAs in flight at once cover a compact run of consecutive tokens.
-constexpr int kBulkTokensPerCta = 2;
+// the CTAs in flight at once cover a compact run of consecutive tokens.  One
+// token per CTA suits the plain form (1-2 % faster at T = 8192, equal at
+// 65536); two suit the forms with scale options or the zero-fill (0.74 against
+// 0.83 ms for the padded layout at T = 65536, 0.75 against 0.87 ms for packed
+// UE8M0 column-major scales).
+constexpr int kBulkTokensPlain = 1;
+constexpr int kBulkTokensOpts = 2;
 
-template <int TOK, bool OPTS, bool ZF>
+template <int TOK, bool OPTS, bool ZF, bool CHAIN = false>
 cudaError_t launch_bulk_t(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                         const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
-                        const int32_t* zsrc, SfOut sfo) {
+                        const int32_t* zsrc, SfOut sfo, const RouteChain& rc = RouteChain()) {
   const int P = H / 16;
   const int threads = (P + 31) / 32 * 32;
   const int G = H / kGroup;
   const size_t stride = (size_t)(H + 4 * G + 127) / 128 * 128;
-  const size_t smem = (stride + sizeof(int32_t) * 32) * TOK;  // + per-token destinations
+  const size_t smem = (stride + 128) * TOK;  // per token: its slot and its 32 destinations
   if (smem > 48 * 1024) {
-    cudaError_t st = allow_max_dynamic_smem(expand_cast_bulk_kernel<TOK, OPTS, ZF>);
+    cudaError_t st = allow_max_dynamic_smem(expand_cast_bulk_kernel<TOK, OPTS, ZF, CHAIN>);
     if (st != cudaSuccess) return st;
   }
   int64_t blocks = (T + TOK - 1) / TOK;
@@ -398,23 +446,34 @@ cudaError_t launch_bulk_t(const LaunchCtx& c, const void* x, int64_t T, int H, i
     blocks = blocks > zb ? blocks : zb;
   }
   if (blocks < 1) blocks = 1;
-  return launch_pdl(expand_cast_bulk_kernel<TOK, OPTS, ZF>, (unsigned)blocks, threads, smem, c.stream,
-                    static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, zsrc, sfo,
-                    c.err);
+  return launch_pdl(expand_cast_bulk_kernel<TOK, OPTS, ZF, CHAIN>, (unsigned)blocks, threads, smem,
+                    c.stream, static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, zsrc,
+                    sfo, rc, c.err);
 }
 
 cudaError_t launch_bulk(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                         const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
                         const int32_t* zsrc, SfOut sfo) {
-  constexpr int TOK = kBulkTokensPerCta;
+  constexpr int TP = kBulkTokensPlain, TO = kBulkTokensOpts;
   if (sfo.flags != 0)
     return zsrc != nullptr
-               ? launch_bulk_t<TOK, true, true>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo)
-               : launch_bulk_t<TOK, true, false>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
+               ? launch_bulk_t<TO, true, true>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo)
+               : launch_bulk_t<TO, true, false>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
   return zsrc != nullptr
-             ? launch_bulk_t<TOK, false, true>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo)
-             : launch_bulk_t<TOK, false, false>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
+             ? launch_bulk_t<TO, false, true>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo)
+             : launch_bulk_t<TP, false, false>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
 }
+
+}  // namespace
+
+cudaError_t launch_expand_cast_chain(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
+                                     int32_t* pos, uint8_t* out, float* out_sf,
+                                     const RouteChain& rc) {
+  return launch_bulk_t<kBulkTokensPlain, false, false, true>(c, x, T, H, k, pos, T * k, out,
+                                                             out_sf, nullptr, SfOut(), rc);
+}
+
+namespace {
 
 // CTAs per SM for the row form, measured on GB300 (prefill-sized expand).
 constexpr int kRowCtasPerSm = 1;

@@ -24,8 +24,12 @@ namespace {
 // tokens, retiring once its copies have read shared memory, so the CTAs in
 // flight at any moment cover a compact run of tokens (the E4M3 bulk form's
 // layout; there a persistent grid striding over the tokens ran at 0.89 of the
-// measured copy peak against 1.01).
-constexpr int kFp4TokensPerCta = 2;
+// measured copy peak against 1.01).  Each token writes fewer bytes here than
+// in E4M3, so more tokens per CTA pay: measured on GB300 (H = 7168, k = 8,
+// after an L2 flush) at T = 65536, group 32: 0.91 / 0.91 / 0.96 / 0.98 of the
+// measured copy peak for 1 / 2 / 3 / 4 tokens per CTA; group 16: 0.97 / 0.97 /
+// 1.00 / 0.99; at T = 8192 three were as fast as one and four slower.
+constexpr int kFp4TokensPerCta = 3;
 
 __device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),

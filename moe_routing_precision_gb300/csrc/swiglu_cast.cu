@@ -19,13 +19,16 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// kGridNote: the grid is not persistent.  One warp per tile of units, so the
-// CTAs in flight at any moment cover a compact run of consecutive rows.
-// Measured on GB300 (65536 rows of 2 x 2048, after an L2 flush / back to
-// back): E4M3 0.929 / 0.968 of the measured copy peak against 0.895 / 0.941
-// for a persistent grid of the resident CTAs striding over the tiles; E2M1
-// (group 32) 0.906 / 0.936 against 0.870 / 0.898.  The loops below still
-// stride, so any grid size is correct.
+// kGridNote: the plain forms' grid is not persistent.  One warp per tile of
+// units, so the CTAs in flight at any moment cover a compact run of
+// consecutive rows.  Measured on GB300 (65536 rows of 2 x 2048, after an L2
+// flush / back to back): E4M3 0.929 / 0.968 of the measured copy peak against
+// 0.895 / 0.941 for a persistent grid of the resident CTAs striding over the
+// tiles; E2M1 (group 32) 0.906 / 0.936 against 0.870 / 0.898.  The variants
+// (EXT) measured the other way round and keep the persistent grid: with
+// per-row weights 0.86 / 0.90 persistent against 0.82 / 0.85; with clamp,
+// weights, count and packed UE8M0 column-major scales 0.80 / 0.84 against
+// 0.75 / 0.78.  The loops stride, so any grid size is correct.
 
 __device__ __forceinline__ float swiglu(float g, float u) {
   // evaluated in the order written on the page, in f32, with the hardware
@@ -212,7 +215,15 @@ cudaError_t launch_t(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_
   const uint32_t units = (uint32_t)(M * G);  // < 2^31, checked by the caller
   const uint32_t tiles = (units + 3) / 4;
   const int64_t need = ((int64_t)tiles + (kThreads / 32) - 1) / (kThreads / 32);
-  const int blocks = (int)(need > 0 ? need : 1);  // one tile per warp: see kGridNote
+  int64_t cap = need;
+  if (EXT) {  // the variants keep a persistent grid: see kGridNote
+    int per_sm = 0;
+    cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, swiglu_cast_kernel<EXT>, kThreads, 0);
+    if (st != cudaSuccess) return st;
+    cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
+  }
+  const int blocks = (int)(need < cap ? (need > 0 ? need : 1) : cap);
   return launch_pdl(swiglu_cast_kernel<EXT>, blocks, kThreads, 0, c.stream,
                     static_cast<const uint16_t*>(x), units, N, out, out_sf, FastDiv((uint32_t)G),
                     ext);
@@ -226,7 +237,15 @@ cudaError_t launch_fp4_t(const LaunchCtx& c, const void* x, int64_t M, int N, ui
   const uint32_t units = (uint32_t)(M * G);  // < 2^31, checked by the caller
   const uint32_t tiles = (units + U - 1) / U;
   const int64_t need = ((int64_t)tiles + (kThreads / 32) - 1) / (kThreads / 32);
-  const int blocks = (int)(need > 0 ? need : 1);  // one tile per warp: see kGridNote
+  int64_t cap = need;
+  if (EXT) {  // the variants keep a persistent grid: see kGridNote
+    int per_sm = 0;
+    cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, swiglu_cast_fp4_kernel<L, EXT>, kThreads, 0);
+    if (st != cudaSuccess) return st;
+    cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
+  }
+  const int blocks = (int)(need < cap ? (need > 0 ? need : 1) : cap);
   return launch_pdl(swiglu_cast_fp4_kernel<L, EXT>, blocks, kThreads, 0, c.stream,
                     static_cast<const uint16_t*>(x), units, N, out, out_sf, FastDiv((uint32_t)G),
                     ext);

@@ -89,9 +89,11 @@ __global__ void __launch_bounds__(kSortedWarps * 32) topk_gate_sorted_kernel(
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  uint32_t sel_e;
   for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps)
     topk_token<V, VEC, KMAX>(scores + t * E, E, k, lane, s_list[wib], s_cand[wib],
-                             topk_idx + t * k, topk_w != nullptr ? topk_w + t * k : nullptr);
+                             topk_idx + t * k, topk_w != nullptr ? topk_w + t * k : nullptr,
+                             sel_e);
 }
 
 template <int V, bool VEC>

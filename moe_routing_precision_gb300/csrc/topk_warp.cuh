@@ -1,6 +1,6 @@
 // topk_warp.cuh -- one warp selects one token's top-k experts (E <= 256) and
-// their softmax weights.  Shared by the top-k kernel and the fused decode
-// kernel.
+// their softmax weights.  Shared by the top-k kernel, the decode kernels and
+// the chained route kernel.
 //
 // TileKernels article (itsolotime.com), section 2.1 "Top-K Gating": the k
 // largest scores of a token, the lowest expert index first among equal
@@ -78,13 +78,15 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 // [32] shared-memory scratch; idx_out / w_out = the token's k outputs (w_out
 // may be null).  V slots per lane.  VEC: E % 128 == 0 and row 16-byte
 // aligned, lane l loads experts h*128 + 4l + j; otherwise expert i*32 + l in
-// slot i.  KMAX >= k bounds the unrolled rounds.
+// slot i.  KMAX >= k bounds the unrolled rounds.  Returns the output slot
+// this lane wrote (-1: none; every slot j < k is written by exactly one
+// lane) and sets sel_expert to that slot's expert.
 template <int V, bool VEC, int KMAX>
-__device__ __forceinline__ void topk_token(const float* __restrict__ row, int E, int k, int lane,
-                                           unsigned long long (*s_list)[32],
-                                           unsigned long long* s_cand,
-                                           int32_t* __restrict__ idx_out,
-                                           float* __restrict__ w_out) {
+__device__ __forceinline__ int topk_token(const float* __restrict__ row, int E, int k, int lane,
+                                          unsigned long long (*s_list)[32],
+                                          unsigned long long* s_cand,
+                                          int32_t* __restrict__ idx_out,
+                                          float* __restrict__ w_out, uint32_t& sel_expert) {
   unsigned long long p[V];
   if constexpr (VEC) {
 #pragma unroll
@@ -187,6 +189,8 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ row, int E,
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
     if (out_j >= 0) w_out[out_j] = __fdiv_rn(ex, sum);
   }
+  sel_expert = out_e;
+  return out_j;
 }
 
 }  // namespace moe

@@ -247,7 +247,7 @@ def sf_empty(rows: int, G: int, flags: int, ld: int | None, like: torch.Tensor):
     return _empty((rows, G), torch.float32, like), ld
 
 
-PATH_AUTO, PATH_FUSED, PATH_SEPARATE, PATH_REPLICATED = 0, 1, 2, 3
+PATH_AUTO, PATH_FUSED, PATH_SEPARATE, PATH_REPLICATED, PATH_CHAINED = 0, 1, 2, 3, 4
 MOE_DEVERR_TIMEOUT = 0x10
 DEBUG_WAIT_TIMEOUT_NS, DEBUG_SKIP_ROUTE_SIGNAL = 1, 2
 
@@ -262,9 +262,10 @@ def route_expand_cast_workspace(T: int, E: int, k: int, like: torch.Tensor) -> t
 def route_expand_cast_fp8(scores: torch.Tensor, x: torch.Tensor, k: int, *, mode: int = PATH_AUTO,
                           workspace=None, out=None, stream=None):
     """topk_gate + route_map + expand_cast_fp8 in one call; mode PATH_AUTO,
-    PATH_SEPARATE, PATH_FUSED (one cooperative launch) or PATH_REPLICATED (one
-    launch, routing repeated per block).  -> (topk_idx, topk_w, counts,
-    offsets, pos, sorted_src, q, sf)."""
+    PATH_SEPARATE, PATH_FUSED (one cooperative launch), PATH_REPLICATED (one
+    launch, routing repeated per block) or PATH_CHAINED (top-k with chunk
+    ranks, a scan, the expand placing its own copies).  -> (topk_idx, topk_w,
+    counts, offsets, pos, sorted_src, q, sf)."""
     _dev(scores, "scores", torch.float32)
     _dev(x, "x", torch.bfloat16)
     T, E = scores.shape

@@ -94,3 +94,35 @@ def combine_gathered(y_rows_bits: np.ndarray, w: np.ndarray, threads: int | None
 
     _map(one, shard_bounds(n, 4 * threads), threads)
     return o32, o16, mag
+
+
+def per_token_cast_fp4(x_bits: np.ndarray, group: int, threads: int | None = None):
+    """The FP4 E2M1 cast of every token (oracle.expand_cast_fp4 with one copy
+    per token, on token shards) -> (q [T, H/2] packed, sf [T, H/group])."""
+    threads = threads or host_threads()
+    T, H = x_bits.shape
+    q = np.empty((T, H // 2), dtype=np.uint8)
+    sf = np.empty((T, H // group), dtype=np.float32)
+
+    def one(ab):
+        a, b = ab
+        ident = np.arange(b - a, dtype=np.int32)[:, None]
+        q[a:b], sf[a:b] = oracle.expand_cast_fp4(x_bits[a:b], ident, group=group)
+
+    _map(one, shard_bounds(T, 4 * threads), threads)
+    return q, sf
+
+
+def swiglu_cast_fp4(x_bits: np.ndarray, group: int, threads: int | None = None):
+    """oracle.swiglu_cast_fp4 over row shards -> (q [M, N/2], sf [M, N/group])."""
+    threads = threads or host_threads()
+    M, N2 = x_bits.shape
+    q = np.empty((M, N2 // 4), dtype=np.uint8)
+    sf = np.empty((M, N2 // 2 // group), dtype=np.float32)
+
+    def one(ab):
+        a, b = ab
+        q[a:b], sf[a:b], _ = oracle.swiglu_cast_fp4(x_bits[a:b], group=group)
+
+    _map(one, shard_bounds(M, 4 * threads), threads)
+    return q, sf

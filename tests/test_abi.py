@@ -198,11 +198,15 @@ def test_route_expand_cast_rejects_bad_arguments(L):
     f = L.moe_route_expand_cast_fp8
     T, E, k, H = 8, 256, 8, 512
     need = L.moe_route_expand_cast_fp8_workspace_bytes(T, E, k)
-    assert need == 256 + L.moe_route_map_workspace_bytes(T, E, k)
+    assert need >= 256 + L.moe_route_map_workspace_bytes(T, E, k)
+    # the chained path's histogram: one row of E counters per chunk of 16 to 64 tokens
+    for TT, chunk in ((8, 16), (16385, 32), (65536, 64)):
+        rows = -(-TT // chunk)
+        assert L.moe_route_expand_cast_fp8_workspace_bytes(TT, E, k) >= 256 + rows * E * 4
     def args(mode=0, H=H, x=FAKE, ws=FAKE, wsb=need, group=128):
         return (FAKE, T, E, k, x, H, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, wsb,
                 mode, group, None)
-    assert f(*args(mode=4)) == INVALID
+    assert f(*args(mode=5)) == INVALID
     assert f(*args(mode=-1)) == INVALID
     assert f(*args(mode=3, wsb=need - 1)) == INVALID   # REPLICATED checks the same arguments
     assert f(*args(group=64)) == UNSUPPORTED

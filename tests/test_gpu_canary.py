@@ -52,6 +52,7 @@ class Guarded:
 
 def _pos_with_last_row(T, k, R, seed):
     """pos [T, k]: distinct rows of [0, R) that include R - 1."""
+    assert R >= T * k
     g = torch.Generator().manual_seed(seed)
     rows = torch.randperm(R, generator=g)[:T * k]
     if (rows == R - 1).sum() == 0:
@@ -59,7 +60,7 @@ def _pos_with_last_row(T, k, R, seed):
     return rows.to(torch.int32).view(T, k).to(DEV)
 
 
-EXPAND_SHAPES = [(1, 512, 1, 3), (3, 7168, 8, 5), (33, 1024, 2, 70), (5, 384, 3, 16),
+EXPAND_SHAPES = [(1, 512, 1, 3), (3, 7168, 8, 29), (33, 1024, 2, 70), (5, 384, 3, 16),
                  (7, 896, 4, 29), (4, 20480, 2, 9)]   # bulk, bulk, bulk, rows (G=3), rows (G=7), tile
 
 

@@ -102,7 +102,8 @@ def test_path_launch_counts_and_auto_choice():
                               (32, ops.PATH_REPLICATED, 1), (33, ops.PATH_REPLICATED, 2),
                               (4096, ops.PATH_AUTO, 4), (32, ops.PATH_AUTO, 1),
                               (512, ops.PATH_AUTO, 2), (1024, ops.PATH_AUTO, 2),
-                              (1025, ops.PATH_AUTO, 4), (1024, ops.PATH_SEPARATE, 3)]:
+                              (1025, ops.PATH_AUTO, 4), (1024, ops.PATH_SEPARATE, 3),
+                              (1025, ops.PATH_SEPARATE, 4), (512, ops.PATH_CHAINED, 3)]:
         scores, x = _inputs(T, E, k, H, seed=T)
         s, xd = scores.to(DEV), x.to(DEV)
         ws = ops.route_expand_cast_workspace(T, E, k, xd)
@@ -150,7 +151,7 @@ def test_wait_that_runs_out_reports_timeout_and_leaves_a_usable_context():
 
 
 @pytest.mark.parametrize("mode", [ops.PATH_AUTO, ops.PATH_FUSED, ops.PATH_SEPARATE,
-                                  ops.PATH_REPLICATED])
+                                  ops.PATH_REPLICATED, ops.PATH_CHAINED])
 def test_no_tokens(mode):
     E, k, H = 64, 4, 256
     s = torch.empty(0, E, device=DEV)

@@ -126,45 +126,27 @@ def test_expand_fp4_flags_pos_out_of_range():
     assert int(q[7].sum()) == 0
 
 
-def test_expand_fp4_full_size_sampled_rows():
-    """prefill_64k inputs, group 32 (the bench's FP4 launch): sampled tokens'
-    rows against the oracle."""
-    w = workloads.WORKLOADS["prefill_64k"]
+@pytest.mark.parametrize("name", ["skewed_8k", "prefill_64k"])
+def test_expand_fp4_full_size_every_row(name):
+    """The skewed and prefill inputs, group 32 (the bench's FP4 launch): every
+    copy of every token against the oracle's cast of that token (on token
+    shards over the host's threads), compared on the device."""
+    from tests import oracle_pool
+    w = workloads.WORKLOADS[name]
     inp = workloads.make_inputs(w, seed=0, device=DEV)
     idx, _ = ops.topk_gate(inp["scores"], w.k)
     _, _, pos, _ = ops.route_map(idx, w.E)
     q, sf = ops.expand_cast_fp4(inp["x"], pos, group=32)
     assert ops.device_status() == 0
-    rng = np.random.default_rng(0)
-    toks = np.sort(rng.choice(w.T, 300, replace=False))
-    xs = inp["x"][torch.from_numpy(toks).to(DEV)].cpu()
-    pos_np = np_(pos)[toks]
-    o_q, o_sf = oracle.expand_cast_fp4(oracle.bf16_bits(xs), np.arange(300, dtype=np.int32)[:, None],
-                                       group=32)
-    for i in range(300):
-        for j in range(w.k):
-            r = pos_np[i, j]
-            assert np.array_equal(np_(q[r]), o_q[i]) and np.array_equal(np_(sf[r]), o_sf[i])
-
-
-def test_expand_fp4_skewed_size_sampled_rows():
-    """skewed_8k inputs (T=8192, H=7168, k=8; inputs above L2 size), group 32:
-    sampled tokens' rows against the oracle."""
-    w = workloads.WORKLOADS["skewed_8k"]
-    inp = workloads.make_inputs(w, seed=0, device=DEV)
-    idx, _ = ops.topk_gate(inp["scores"], w.k)
-    _, _, pos, _ = ops.route_map(idx, w.E)
-    q, sf = ops.expand_cast_fp4(inp["x"], pos, group=32)
-    assert ops.device_status() == 0
-    toks = np.sort(np.random.default_rng(1).choice(w.T, 200, replace=False))
-    xs = inp["x"][torch.from_numpy(toks).to(DEV)].cpu()
-    pos_np = np_(pos)[toks]
-    o_q, o_sf = oracle.expand_cast_fp4(oracle.bf16_bits(xs), np.arange(200, dtype=np.int32)[:, None],
-                                       group=32)
-    for i in range(200):
-        for j in range(w.k):
-            r = pos_np[i, j]
-            assert np.array_equal(np_(q[r]), o_q[i]) and np.array_equal(np_(sf[r]), o_sf[i])
+    o_q, o_sf = oracle_pool.per_token_cast_fp4(oracle.bf16_bits(inp["x"]), 32)
+    o_q, o_sf = torch.from_numpy(o_q).to(DEV), torch.from_numpy(o_sf.view(np.int32)).to(DEV)
+    sf_bits = sf.view(torch.int32)
+    for j in range(w.k):
+        rows = pos[:, j].long()
+        assert torch.equal(q[rows], o_q), f"codes of copy {j}"
+        assert torch.equal(sf_bits[rows], o_sf), f"scales of copy {j}"
+    del inp, q, sf, o_q, o_sf
+    torch.cuda.empty_cache()
 
 
 # ---------------------------------------------------------------- SwiGLU -> FP4
@@ -196,16 +178,17 @@ def test_swiglu_fp4_parity(group, flags, variant, M, N):
     assert ops.device_status() == 0
 
 
-def test_swiglu_fp4_full_size_sampled_rows():
-    """swiglu_64k (65536 rows x 2x2048), group 32: 2000 sampled rows."""
+def test_swiglu_fp4_full_size_every_row():
+    """swiglu_64k (65536 rows x 2x2048), group 32: every row."""
+    from tests import oracle_pool
     w = workloads.WORKLOADS["swiglu_64k"]
     hx = workloads.make_inputs(w, seed=0, device=DEV)["swiglu_x"]
     q, sf = ops.swiglu_cast_fp4(hx, group=32)
     assert ops.device_status() == 0
-    rows = np.sort(np.random.default_rng(2).choice(w.M, 2000, replace=False))
-    xs = hx[torch.from_numpy(rows).to(DEV)].cpu()
-    o_q, o_sf, _ = oracle.swiglu_cast_fp4(oracle.bf16_bits(xs), group=32)
-    check_swiglu_opts(np_(q)[rows], np_(sf)[rows], o_q, o_sf, o_sf, 0, 2000, ordinal=fp4_ordinal)
+    o_q, o_sf = oracle_pool.swiglu_cast_fp4(oracle.bf16_bits(hx), 32)
+    check_swiglu_opts(np_(q), np_(sf), o_q, o_sf, o_sf, 0, w.M, ordinal=fp4_ordinal)
+    del hx, q, sf
+    torch.cuda.empty_cache()
 
 
 def test_fp4_empty_inputs_and_zero_fill_only():

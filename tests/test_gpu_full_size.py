@@ -1,8 +1,9 @@
 """GPU parity at the benchmarked sizes: every element of every output.
 
 The skewed-routing workload (T=8192), the large prefill (T=65536) and the
-SwiGLU workload (65536 rows of 2x2048) run through the C ABI in the launch
-configuration the bench times, and every output element is compared with
+SwiGLU workload (65536 rows of 2x2048) run through the C ABI, both as the
+individual calls (the launches the bench times) and as the chained one-call
+form, and every output element is compared with
 the oracle: the whole top-k and route map, the E4M3 codes and scale bits of
 all k copies of every token (bit-exact), combine for every token in both
 output dtypes, and every SwiGLU row.  The oracle runs on token shards over
@@ -53,14 +54,24 @@ def _assert_rows_equal_on_device(got, ref_dev, what):
                          f"gpu={got[i].item()!r} oracle={ref_dev[i].item()!r}")
 
 
+@pytest.mark.parametrize("path", ["calls", "chained"])
 @pytest.mark.parametrize("name", ["skewed_8k", "prefill_64k"])
-def test_full_size_every_element(name):
+def test_full_size_every_element(name, path):
+    """path "calls": moe_topk_gate, moe_route_map, moe_expand_cast_fp8 (the
+    launches the bench times: its one-call AUTO path takes them at these
+    sizes); "chained": moe_route_expand_cast_fp8 with MOE_PATH_CHAINED."""
     w = workloads.WORKLOADS[name]
     T, E, k, H, R, G = w.T, w.E, w.k, w.H, w.R, w.G
     inp = workloads.make_inputs(w, seed=0, device=DEV, with_y=True)
-    idx, wt = ops.topk_gate(inp["scores"], k)
-    counts, offsets, pos, src = ops.route_map(idx, E)
-    q, sf = ops.expand_cast_fp8(inp["x"], pos)
+    if path == "calls":
+        idx, wt = ops.topk_gate(inp["scores"], k)
+        counts, offsets, pos, src = ops.route_map(idx, E)
+        q, sf = ops.expand_cast_fp8(inp["x"], pos)
+    else:
+        n0 = ops.launch_count()
+        idx, wt, counts, offsets, pos, src, q, sf = ops.route_expand_cast_fp8(
+            inp["scores"], inp["x"], k, mode=ops.PATH_CHAINED)
+        assert ops.launch_count() - n0 == 3          # the chained launches
     comb16 = ops.combine(inp["y"], wt, pos, torch.bfloat16)
     comb32 = ops.combine(inp["y"], wt, pos, torch.float32)
     assert ops.device_status() == 0
