@@ -439,19 +439,21 @@ moe_status_t moe_combine(const void *y, const float *topk_weights,
  * is one launch for T <= 1024).  The CHAINED path is three launches: the
  * top-k kernel, one CTA per chunk of 16 to 64 consecutive tokens, also counts
  * each chunk's copies per expert and ranks every copy among its expert's
- * copies in the chunk; a scan turns the counts into per-chunk bases; the
- * expand kernel places every copy itself (expert offset + chunk base + rank),
- * writing pos, sorted_src and offsets, then stores the rows.  It applies to
+ * copies in the chunk; a scan turns the counts into per-chunk bases, the
+ * counts and the offsets; the expand kernel places every copy itself (expert
+ * offset + chunk base + rank), writing pos and sorted_src, then stores the
+ * rows.  It applies to
  * 32 < E <= 256, k <= 32, H <= 16384 with H/128 % 4 == 0 and 16-byte aligned
  * out and out_sf.
  *   scores [T,E] f32; x [T,H] bf16; topk_idx [T,k] i32; topk_weights [T,k]
  *   f32; counts [E], offsets [E+1], pos [T,k], sorted_src [T*k] i32;
  *   out [T*k,H] u8; out_sf [T*k,H/128] f32.
  *   workspace: at least moe_route_expand_cast_fp8_workspace_bytes(T,E,k)
- *   bytes, 16-byte aligned.  Its first 256 bytes hold the fused path's
- *   control words: ZERO them once before the first call (each call leaves
- *   them zero; after a MOE_DEVERR_TIMEOUT, zero them again).  One workspace
- *   must not be used by two calls in flight at once.
+ *   bytes, 16-byte aligned.  Its first 256 bytes hold the FUSED and CHAINED
+ *   paths' control words (the fused launch's arrival counters; the chained
+ *   scan's count of finished CTAs): ZERO them once before the first call
+ *   (each call leaves them zero; after a MOE_DEVERR_TIMEOUT, zero them
+ *   again).  One workspace must not be used by two calls in flight at once.
  *   mode: MOE_PATH_AUTO, MOE_PATH_FUSED, MOE_PATH_REPLICATED or
  *   MOE_PATH_CHAINED (MOE_ERR_UNSUPPORTED where they do not apply) or
  *   MOE_PATH_SEPARATE.  AUTO
