@@ -8,14 +8,15 @@
 // copy of a token casts identically, so here each token is read and cast once
 // and its codes are written k times.
 //
-// Work unit: one (token, 128-channel group) per aligned 8-lane subgroup; lane
-// l of the subgroup holds channels 16l..16l+15 (two 16-byte loads), the group
-// amax is a 3-step xor-shuffle, and each lane writes one 16-byte code vector
-// per destination row.  A warp handles 4 consecutive units, so a warp's loads
-// cover 1 KiB and its stores 512 contiguous bytes per destination row.
-// The grid is persistent (a multiple of the SM count) and strides over tiles
-// of 4 units; HBM traffic is ~80% writes (k copies of 1 byte per channel plus
-// scales, against 2 bytes per channel read once).
+// Three forms, all with one 128-channel group per aligned 8-lane subgroup
+// (lane l holds channels 16l..16l+15, two 16-byte loads; the group amax is a
+// 3-step xor shuffle):
+//   bulk (H <= 16384, H/128 % 4 == 0, 16-byte aligned out and out_sf): one
+//     CTA per one or two tokens, the rows leave by TMA bulk copies;
+//   row (other H <= 16384): whole tokens per CTA, 16-byte stores;
+//   tile (H > 16384): one warp per 4 consecutive (token, group) units.
+// HBM traffic is ~80% writes (k copies of 1 byte per channel plus scales,
+// against 2 bytes per channel read once).
 #include "common.cuh"
 
 namespace moe {
@@ -475,18 +476,21 @@ cudaError_t launch_expand_cast_chain(const LaunchCtx& c, const void* x, int64_t 
 
 namespace {
 
-// CTAs per SM for the row form, measured on GB300 (prefill-sized expand).
-constexpr int kRowCtasPerSm = 1;
-
+// The fallback forms' grids cover all their work (one CTA per token group, one
+// warp per tile) instead of a persistent grid of the resident CTAs striding
+// over it, as the bulk form's: measured on GB300 (k = 8, after an L2 flush)
+// the row form at H = 7296 (G = 57) ran at 0.84 of the measured copy peak
+// against 0.73, at H = 640 at 0.63 against 0.42, and the tile form at
+// H = 20480 at 0.96 against 0.82.  The loops still stride, so any grid size
+// is correct.
 template <bool G4>
 cudaError_t launch_rows(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                         const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
-                        int ctas_per_sm, const int32_t* zsrc, SfOut sfo) {
+                        const int32_t* zsrc, SfOut sfo) {
   const int P = H / 16;
   const int tpc = P >= 256 ? 1 : 256 / P;
   const int64_t groups = (T + tpc - 1) / tpc;
-  const int64_t cap = (int64_t)c.num_sms * ctas_per_sm;
-  const int blocks = (int)(groups < cap ? (groups > 0 ? groups : 1) : cap);  // >= 1: zero-fill
+  const int blocks = (int)(groups > 0 ? groups : 1);  // >= 1: zero-fill
   const int threads = (P * tpc + 31) / 32 * 32;  // whole warps: the shuffles use full masks
   return launch_pdl(expand_cast_rows_kernel<G4>, blocks, threads, 0, c.stream,
                     static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, tpc, zsrc, sfo,
@@ -501,12 +505,7 @@ cudaError_t launch_g(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
   const uint32_t units = (uint32_t)(T * G);  // < 2^31, checked by the caller
   const uint32_t tiles = (units + 3) / 4;
   const int64_t need = ((int64_t)tiles + (kThreads / 32) - 1) / (kThreads / 32);
-  int per_sm = 0;
-  cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, expand_cast_kernel<G4>,
-                                                                 kThreads, 0);
-  if (st != cudaSuccess) return st;
-  const int64_t cap = (int64_t)c.num_sms * (per_sm > 0 ? per_sm : 1);
-  const int blocks = (int)(need < cap ? (need > 0 ? need : 1) : cap);  // >= 1: zero-fill with T = 0
+  const int blocks = (int)(need > 0 ? need : 1);  // >= 1: zero-fill with T = 0
   return launch_pdl(expand_cast_kernel<G4>, blocks, kThreads, 0, c.stream,
                     static_cast<const uint16_t*>(x), units, H, k, pos, R, out, out_sf,
                     FastDiv((uint32_t)G), zsrc, sfo, c.err);
@@ -574,9 +573,8 @@ cudaError_t launch_expand_cast_kernel(const LaunchCtx& c, const void* x, int64_t
   if (H <= 16384 && bulk_ok && (H / kGroup) % 4 == 0 && aligned16)
     return launch_bulk(c, x, T, H, k, pos, R, out, out_sf, zero_rows, sfo);
   if (H <= 16384)
-    return g4 ? launch_rows<true>(c, x, T, H, k, pos, R, out, out_sf, kRowCtasPerSm, zero_rows, sfo)
-              : launch_rows<false>(c, x, T, H, k, pos, R, out, out_sf, kRowCtasPerSm, zero_rows,
-                                   sfo);
+    return g4 ? launch_rows<true>(c, x, T, H, k, pos, R, out, out_sf, zero_rows, sfo)
+              : launch_rows<false>(c, x, T, H, k, pos, R, out, out_sf, zero_rows, sfo);
   return g4 ? launch_g<true>(c, x, T, H, k, pos, R, out, out_sf, zero_rows, sfo)
             : launch_g<false>(c, x, T, H, k, pos, R, out, out_sf, zero_rows, sfo);
 }

@@ -2,7 +2,7 @@
 against the oracle: shapes the fixed parity cases do not name (odd T, E not a
 power of two, every k, H across the kernel forms, all scale layouts, every
 FP4 group size, padded alignments, decode shapes on the fused and replicated
-paths).  Each case is small enough for the oracle to finish at once."""
+paths, and the chained form).  Each case is small enough for the oracle to finish at once."""
 import numpy as np
 import pytest
 import torch
@@ -139,7 +139,7 @@ def test_fp4_and_swiglu(case):
 
 
 @pytest.mark.parametrize("case", range(CASES // 2))
-@pytest.mark.parametrize("mode", ["fused", "replicated"])
+@pytest.mark.parametrize("mode", ["fused", "replicated", "chained"])
 def test_decode_paths(case, mode):
     rng = np.random.default_rng(3000 + case)
     E = int(rng.choice([40, 64, 96, 128, 200, 256]))
@@ -150,7 +150,12 @@ def test_decode_paths(case, mode):
         T = int(rng.integers(1, 33))          # the one-launch form
     inp = workloads.random_small(T, E, k, H, seed=case, ties=bool(rng.integers(0, 2)))
     s, x = inp["scores"], inp["x"]
-    path = ops.PATH_FUSED if mode == "fused" else ops.PATH_REPLICATED
+    if mode == "chained":
+        H = 512 * int(rng.integers(1, 9))     # the chained form's H / 128 % 4 == 0
+        if case % 2 == 0:
+            T = int(rng.integers(2049, 40000))   # past the decode sizes, across chunk sizes
+    path = {"fused": ops.PATH_FUSED, "replicated": ops.PATH_REPLICATED,
+            "chained": ops.PATH_CHAINED}[mode]
     try:
         res = ops.route_expand_cast_fp8(s.to(DEV), x.to(DEV), k, mode=path)
     except ops.MoeError as e:               # a shape outside the form's limits

@@ -2,7 +2,7 @@
 it): one capture of moe_route_expand_cast_fp8 with the library's own choice
 of path, replayed on fresh inputs copied into the captured buffers, must give
 the oracle's results every time.  Covers the one-launch replicated form, the
-top-k + route/expand form, and the separate launches."""
+top-k + route/expand form, the separate launches, and the chained form."""
 import ctypes
 
 import numpy as np
@@ -33,8 +33,12 @@ def np_(t):
     return t.detach().cpu().numpy()
 
 
-@pytest.mark.parametrize("T", [16, 200, 1500])   # one launch / top-k + one / separate
-def test_captured_call_replays_on_new_inputs(T):
+@pytest.mark.parametrize("T,mode", [(16, ops.PATH_AUTO), (200, ops.PATH_AUTO),
+                                    (1500, ops.PATH_AUTO), (1500, ops.PATH_CHAINED)])
+def test_captured_call_replays_on_new_inputs(T, mode):
+    """AUTO: one launch / top-k + one / the separate launches; CHAINED: its
+    three launches, including the scan's count of finished CTAs, which each
+    replay must leave at zero for the next."""
     L = ops.lib()
     i32 = dict(dtype=torch.int32, device=DEV)
     scores = torch.empty(T, E, device=DEV)
@@ -49,7 +53,7 @@ def test_captured_call_replays_on_new_inputs(T):
     def call():
         rc = L.moe_route_expand_cast_fp8(scores.data_ptr(), T, E, K, x.data_ptr(), H,
                                          *[o.data_ptr() for o in outs], ws.data_ptr(), ws.numel(),
-                                         ops.PATH_AUTO, 128, ctypes.c_void_p(stream.cuda_stream))
+                                         mode, 128, ctypes.c_void_p(stream.cuda_stream))
         assert rc == 0
 
     first = workloads.random_small(T, E, K, H, seed=T)
@@ -61,7 +65,7 @@ def test_captured_call_replays_on_new_inputs(T):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         call()
-    for seed in (T + 1, T + 2):
+    for seed in (T + 1, T + 2, T + 3):
         inp = workloads.random_small(T, E, K, H, seed=seed, ties=seed % 2 == 0)
         scores.copy_(inp["scores"])
         x.copy_(inp["x"])
