@@ -134,8 +134,11 @@ __device__ __forceinline__ int topk_token(const float* __restrict__ row, int E, 
   }
   unsigned cmask = 0;  // this lane's candidates (absent slots are 0)
 #pragma unroll
-  for (int i = 0; i < V; ++i)
-    if (p[i] != 0ull && (uint32_t)(p[i] >> 32) >= theta) cmask |= 1u << i;
+  for (int i = 0; i < V; ++i) {
+    // VEC: E = 32 V, so no slot is absent
+    const bool present = VEC || p[i] != 0ull;
+    if (present && (uint32_t)(p[i] >> 32) >= theta) cmask |= 1u << i;
+  }
   const int nc = __popc(cmask);
   const int C = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)nc);
   __syncwarp();  // the previous token is done with shared memory
