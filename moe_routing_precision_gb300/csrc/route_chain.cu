@@ -44,7 +44,8 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_topk_kernel(
     float* __restrict__ topk_w, int32_t* __restrict__ rank, int32_t* __restrict__ hist) {
   __shared__ unsigned long long s_list[kChainWarps][V][32];
   __shared__ unsigned long long s_cand[kChainWarps][32];
-  __shared__ uint32_t s_bits[TPW > 2 ? 2 : 1][256];  // [tokens / 32][E], E <= 256
+  constexpr int W = (kChainWarps * TPW + 31) / 32;  // 32-token bitmap words per chunk
+  __shared__ uint32_t s_bits[W][256];                // [word][E], E <= 256
   __shared__ int32_t s_sel[TPW][kChainWarps][32];    // slot << 16 | expert, or -1
   pdl_enter();
   const int tid = threadIdx.x;
@@ -52,8 +53,8 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_topk_kernel(
   const int warp = tid >> 5;
   const int64_t c0 = (int64_t)blockIdx.x * (kChainWarps * TPW);
   for (int e = tid; e < E; e += kChainWarps * 32) {
-    s_bits[0][e] = 0u;
-    if (TPW > 2) s_bits[TPW > 2 ? 1 : 0][e] = 0u;
+#pragma unroll
+    for (int w = 0; w < W; ++w) s_bits[w][e] = 0u;
   }
   __syncthreads();
   // token c0 + i for i = warp, warp + 16, ... (TPW per warp); each lane's
@@ -81,13 +82,18 @@ __global__ void __launch_bounds__(kChainWarps * 32) chain_topk_kernel(
     if (sel >= 0) {
       const int ex = sel & 0xFFFF;
       int r = __popc(s_bits[i >> 5][ex] & ((1u << (i & 31)) - 1u));
-      if (TPW > 2 && i >= 32) r += __popc(s_bits[0][ex]);
+#pragma unroll
+      for (int w = 0; w < W; ++w) r += w < (i >> 5) ? __popc(s_bits[w][ex]) : 0;
       rank[(c0 + i) * k + (sel >> 16)] = r;
     }
   }
   int32_t* row = hist + (int64_t)blockIdx.x * E;
-  for (int e = tid; e < E; e += kChainWarps * 32)
-    row[e] = __popc(s_bits[0][e]) + (TPW > 2 ? __popc(s_bits[TPW > 2 ? 1 : 0][e]) : 0);
+  for (int e = tid; e < E; e += kChainWarps * 32) {
+    int n = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) n += __popc(s_bits[w][e]);
+    row[e] = n;
+  }
 }
 
 // The column scan.  CTA b owns experts 32 b .. 32 b + 31 (lane = expert), and
