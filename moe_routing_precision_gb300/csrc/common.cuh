@@ -128,6 +128,33 @@ __device__ __forceinline__ void store_stage(uint8_t* stage, int flags, int G, in
     reinterpret_cast<float*>(stage)[t * G + g] = sf;
 }
 
+// Row-major UE8M0 scales with wide stores: the width (8 or 4 bytes) that
+// out_sf's address and the row length G both allow, else 0 (byte stores).
+__host__ __device__ __forceinline__ int ue8m0_store_width(const void* out_sf, int G) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(out_sf) | (uintptr_t)G;
+  return (a & 7u) == 0 ? 8 : ((a & 3u) == 0 ? 4 : 0);
+}
+
+// One warp writes a token's G row-major UE8M0 scale bytes, held at `src` in
+// shared memory (n-byte aligned), to each of its destination rows spos[j],
+// j < k (skipped where negative or >= R), n = ue8m0_store_width bytes per
+// store: G / n stores per row, spread over the lanes.
+__device__ __forceinline__ void store_ue8m0_rows(uint8_t* out_sf, const uint8_t* src,
+                                                 const int32_t* spos, int k, int G, int64_t R,
+                                                 int n, int lane) {
+  const int per = G / n;
+  for (int u = lane; u < k * per; u += 32) {
+    const int j = u / per, c = u - j * per;
+    const int32_t r = spos[j];
+    if (r < 0 || r >= R) continue;
+    uint8_t* dst = out_sf + (int64_t)r * G + c * n;
+    if (n == 8)
+      *reinterpret_cast<uint64_t*>(dst) = *reinterpret_cast<const uint64_t*>(src + c * n);
+    else
+      *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src + c * n);
+  }
+}
+
 // Quantise 16 f32 values with multiplier `inv`, pack the 16 codes.
 __device__ __forceinline__ uint4 quant16(const float (&v)[16], float inv) {
   uint4 q;

@@ -298,8 +298,16 @@ __device__ __forceinline__ void chain_place(const RouteChain& rc, int64_t t0, in
   }
 }
 
+// Held to 32 registers (the form with options and the zero-fill spills 4 bytes), so
+// that 4 CTAs of 448 threads (H = 7168) fit an SM; with more registers only 3
+// or 2 do, and the bandwidth follows the tokens in flight.  Measured on GB300
+// at T = 65536 (H = 7168, k = 8, after an L2 flush) with packed UE8M0
+// column-major scales (staged, with the zero-fill): 0.765 ms at 56 registers
+// and two tokens per CTA (2 CTAs per SM), 0.714 ms at 40 (3 CTAs per SM),
+// 0.704 ms at 32 with one token per CTA; the padded layout 0.763 -> 0.738 ms
+// between the last two.
 template <int TOK, bool OPTS, bool ZF, bool CHAIN>
-__global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
+__global__ void __maxnreg__(32) expand_cast_bulk_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
     int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf,
     const int32_t* __restrict__ zsrc, SfOut sfo, RouteChain rc, unsigned* err) {
@@ -317,6 +325,16 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
   int32_t* spos_all = reinterpret_cast<int32_t*>(s_buf + (size_t)TOK * stride);  // [TOK][32]
   bool bad = false;
   const int flags = OPTS ? sfo.flags : 0;
+  // Scale layouts: row-major f32 (power-of-two rounded or not) leaves with the
+  // codes by bulk copy; row-major UE8M0 bytes are assembled in shared memory
+  // and written with wide stores by one warp (sf_wide: 8 or 4 bytes per
+  // store, whichever the row length and out_sf's alignment allow); the rest
+  // (column-major, direct or staged) is stored per group by one lane.
+  const bool sf_bulk =
+      !OPTS || ((flags & (MOE_SF_COLMAJOR | MOE_SF_UE8M0)) == 0 && sfo.stage == nullptr);
+  const int sf_wide = (OPTS && (flags & MOE_SF_UE8M0) && !(flags & MOE_SF_COLMAJOR))
+                          ? ue8m0_store_width(out_sf, G)
+                          : 0;
   // only the column-major and byte scale layouts store partial lines
   const bool hint = OPTS && (flags & (MOE_SF_COLMAJOR | MOE_SF_UE8M0)) != 0 && sfo.stage == nullptr;
   const uint64_t policy = l2_evict_first_policy();
@@ -356,13 +374,24 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
     uint8_t* sq = s_buf + (size_t)i * stride;
     if (act && t0 + i < T) {
       *reinterpret_cast<uint4*>(sq + tid * 16) = q;
-      if (l8 == 0 && flags == 0) *reinterpret_cast<float*>(sq + H + 4 * g) = sfv[i];
+      if (l8 == 0 && sf_bulk) *reinterpret_cast<float*>(sq + H + 4 * g) = sfv[i];
+      if (l8 == 0 && sf_wide) sq[H + g] = (uint8_t)((__float_as_uint(sfv[i]) >> 23) & 0xFFu);
     }
-    if (flags != 0 && tid < 32) spos_all[i * 32 + tid] = pv[i];  // for every warp
+    if (!sf_bulk && tid < 32) spos_all[i * 32 + tid] = pv[i];  // for every warp
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the copies
   __syncthreads();
-  if (flags != 0 && act && l8 == 0) {  // scale options: per-group scale stores
+  if (sf_wide) {
+    // row-major UE8M0 by one warp (warp 1 where there is one, so that warp 0
+    // issues its copies meanwhile)
+    if ((tid >> 5) == (blockDim.x >= 64 ? 1 : 0)) {
+#pragma unroll
+      for (int i = 0; i < TOK; ++i)
+        if (t0 + i < T)
+          store_ue8m0_rows(reinterpret_cast<uint8_t*>(out_sf), s_buf + (size_t)i * stride + H,
+                           spos_all + i * 32, k, G, R, sf_wide, lane);
+    }
+  } else if (!sf_bulk && act && l8 == 0) {  // scale options: per-group scale stores
 #pragma unroll
     for (int i = 0; i < TOK; ++i) {
       const int64_t t = t0 + i;
@@ -392,7 +421,7 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
               bulk_s2g_hint(out + (int64_t)r * H, slot, (uint32_t)H, policy);
             else
               bulk_s2g(out + (int64_t)r * H, slot, (uint32_t)H);
-            if (flags == 0) bulk_s2g(out_sf + (int64_t)r * G, slot + H, (uint32_t)(4 * G));
+            if (sf_bulk) bulk_s2g(out_sf + (int64_t)r * G, slot + H, (uint32_t)(4 * G));
           }
         }
       }
@@ -421,12 +450,9 @@ __global__ void __launch_bounds__(1024) expand_cast_bulk_kernel(
 // the tokens with the next token's loads in flight.  The persistent grid kept
 // the accesses in flight at any moment spread over the whole of x and q; here
 // the CTAs in flight at once cover a compact run of consecutive tokens.  One
-// token per CTA suits the plain form (1-2 % faster at T = 8192, equal at
-// 65536); two suit the forms with scale options or the zero-fill (0.74 against
-// 0.83 ms for the padded layout at T = 65536, 0.75 against 0.87 ms for packed
-// UE8M0 column-major scales).
-constexpr int kBulkTokensPlain = 1;
-constexpr int kBulkTokensOpts = 2;
+// token per CTA, at 32 registers, suits every form (with two, the option and
+// zero-fill forms need more registers: see the kernel).
+constexpr int kBulkTokensPerCta = 1;
 
 template <int TOK, bool OPTS, bool ZF, bool CHAIN = false>
 cudaError_t launch_bulk_t(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
@@ -437,8 +463,9 @@ cudaError_t launch_bulk_t(const LaunchCtx& c, const void* x, int64_t T, int H, i
   const int G = H / kGroup;
   const size_t stride = (size_t)(H + 4 * G + 127) / 128 * 128;
   const size_t smem = (stride + 128) * TOK;  // per token: its slot and its 32 destinations
+  const auto kern = expand_cast_bulk_kernel<TOK, OPTS, ZF, CHAIN>;
   if (smem > 48 * 1024) {
-    cudaError_t st = allow_max_dynamic_smem(expand_cast_bulk_kernel<TOK, OPTS, ZF, CHAIN>);
+    cudaError_t st = allow_max_dynamic_smem(kern);
     if (st != cudaSuccess) return st;
   }
   int64_t blocks = (T + TOK - 1) / TOK;
@@ -447,22 +474,22 @@ cudaError_t launch_bulk_t(const LaunchCtx& c, const void* x, int64_t T, int H, i
     blocks = blocks > zb ? blocks : zb;
   }
   if (blocks < 1) blocks = 1;
-  return launch_pdl(expand_cast_bulk_kernel<TOK, OPTS, ZF, CHAIN>, (unsigned)blocks, threads, smem,
-                    c.stream, static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, zsrc,
-                    sfo, rc, c.err);
+  return launch_pdl(kern, (unsigned)blocks, threads, smem, c.stream,
+                    static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, zsrc, sfo, rc,
+                    c.err);
 }
 
 cudaError_t launch_bulk(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                         const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
                         const int32_t* zsrc, SfOut sfo) {
-  constexpr int TP = kBulkTokensPlain, TO = kBulkTokensOpts;
+  constexpr int TK = kBulkTokensPerCta;
   if (sfo.flags != 0)
     return zsrc != nullptr
-               ? launch_bulk_t<TO, true, true>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo)
-               : launch_bulk_t<TO, true, false>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
+               ? launch_bulk_t<TK, true, true>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo)
+               : launch_bulk_t<TK, true, false>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
   return zsrc != nullptr
-             ? launch_bulk_t<TO, false, true>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo)
-             : launch_bulk_t<TP, false, false>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
+             ? launch_bulk_t<TK, false, true>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo)
+             : launch_bulk_t<TK, false, false>(c, x, T, H, k, pos, R, out, out_sf, zsrc, sfo);
 }
 
 }  // namespace
@@ -470,8 +497,8 @@ cudaError_t launch_bulk(const LaunchCtx& c, const void* x, int64_t T, int H, int
 cudaError_t launch_expand_cast_chain(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                                      int32_t* pos, uint8_t* out, float* out_sf,
                                      const RouteChain& rc) {
-  return launch_bulk_t<kBulkTokensPlain, false, false, true>(c, x, T, H, k, pos, T * k, out,
-                                                             out_sf, nullptr, SfOut(), rc);
+  return launch_bulk_t<kBulkTokensPerCta, false, false, true>(c, x, T, H, k, pos, T * k, out,
+                                                              out_sf, nullptr, SfOut(), rc);
 }
 
 namespace {
@@ -569,7 +596,8 @@ cudaError_t launch_expand_cast_kernel(const LaunchCtx& c, const void* x, int64_t
   // the 16-byte scale store needs G % 4 == 0 and a 16-byte aligned out_sf
   const bool g4 = (H / kGroup) % 4 == 0 && (reinterpret_cast<uintptr_t>(out_sf) % 16) == 0;
   const bool aligned16 = (reinterpret_cast<uintptr_t>(out) % 16) == 0;
-  const bool bulk_ok = sfo.flags != 0 || g4;  // scale options don't use the bulk scale copy
+  // row-major f32 scales (flags 0 or power-of-two alone) leave by bulk copy
+  const bool bulk_ok = (sfo.flags & (MOE_SF_COLMAJOR | MOE_SF_UE8M0)) != 0 || g4;
   if (H <= 16384 && bulk_ok && (H / kGroup) % 4 == 0 && aligned16)
     return launch_bulk(c, x, T, H, k, pos, R, out, out_sf, zero_rows, sfo);
   if (H <= 16384)

@@ -25,11 +25,16 @@ namespace {
 // flight at any moment cover a compact run of tokens (the E4M3 bulk form's
 // layout; there a persistent grid striding over the tokens ran at 0.89 of the
 // measured copy peak against 1.01).  Each token writes fewer bytes here than
-// in E4M3, so more tokens per CTA pay: measured on GB300 (H = 7168, k = 8,
-// after an L2 flush) at T = 65536, group 32: 0.91 / 0.91 / 0.96 / 0.98 of the
-// measured copy peak for 1 / 2 / 3 / 4 tokens per CTA; group 16: 0.97 / 0.97 /
-// 1.00 / 0.99; at T = 8192 three were as fast as one and four slower.
-constexpr int kFp4TokensPerCta = 3;
+// in E4M3, and with the kernel's natural 55-59 registers (2 CTAs of 448
+// threads per SM at H = 7168) more tokens per CTA paid: measured on GB300
+// (H = 7168, k = 8, after an L2 flush) at T = 65536, group 32: 0.91 / 0.91 /
+// 0.96 / 0.98 of the measured copy peak for 1 / 2 / 3 / 4 tokens per CTA.
+// Held to 32 registers (no spills), 4 CTAs fit an SM and one token per CTA
+// is best: group 32 at 1.01 (0.482 against 0.505 ms for 3 tokens per CTA
+// unconstrained), group 16 at 1.00 (0.552 against 0.557 ms); at T = 8192
+// 66 against 74 us (group 32).  40 registers with 1 or 2 tokens per CTA, and
+// 48 with 2, were slower.
+constexpr int kFp4TokensPerCta = 1;
 
 __device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
@@ -37,14 +42,17 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t byt
                : "memory");
 }
 
-// L = lanes per group (group = 16 L channels).  sf_bulk: plain row-major f32
-// scales whose rows (4G bytes) are 16-byte multiples go out with the codes.
-// ZF: the zero-fill of the padding rows (zsrc non-null) is compiled in.
+// L = lanes per group (group = 16 L channels).  sf_bulk: row-major f32
+// scales (power-of-two rounded or not) whose rows (4G bytes) are 16-byte
+// multiples go out with the codes.  sf_wide: row-major UE8M0 bytes are
+// assembled in shared memory and one warp writes them sf_wide (8 or 4) bytes
+// per store.  Otherwise one lane per group stores its scale.  ZF: the
+// zero-fill of the padding rows (zsrc non-null) is compiled in.
 template <int L, int TOK, bool ZF>
-__global__ void __launch_bounds__(1024) expand_cast_fp4_kernel(
+__global__ void __maxnreg__(32) expand_cast_fp4_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
     int64_t R, uint8_t* __restrict__ out, float* __restrict__ out_sf,
-    const int32_t* __restrict__ zsrc, SfOut sfo, int sf_bulk, unsigned* err) {
+    const int32_t* __restrict__ zsrc, SfOut sfo, int sf_bulk, int sf_wide, unsigned* err) {
   extern __shared__ __align__(128) uint8_t s_buf[];
   pdl_enter();
   const int P = H >> 4;   // threads per token
@@ -90,12 +98,23 @@ __global__ void __launch_bounds__(1024) expand_cast_fp4_kernel(
     if (act && valid) {
       *reinterpret_cast<uint2*>(sq + tid * 8) = q;
       if (lead && sf_bulk) *reinterpret_cast<float*>(sq + HB + 4 * g) = sfv[i];
+      if (lead && sf_wide) sq[HB + g] = (uint8_t)((__float_as_uint(sfv[i]) >> 23) & 0xFFu);
     }
     if (!sf_bulk && tid < 32) spos_all[i * 32 + tid] = valid ? pv[i] : -1;
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the copies
   __syncthreads();
-  if (!sf_bulk && act && lead) {  // one lane per group stores its scale
+  if (sf_wide) {
+    // by one warp (warp 1 where there is one, so that warp 0 issues its
+    // copies meanwhile)
+    if ((tid >> 5) == (blockDim.x >= 64 ? 1 : 0)) {
+#pragma unroll
+      for (int i = 0; i < TOK; ++i)
+        if (t0 + i < T)
+          store_ue8m0_rows(reinterpret_cast<uint8_t*>(out_sf), s_buf + (size_t)i * stride + HB,
+                           spos_all + i * 32, k, G, R, sf_wide, lane);
+    }
+  } else if (!sf_bulk && act && lead) {  // one lane per group stores its scale
 #pragma unroll
     for (int i = 0; i < TOK; ++i) {
       const int64_t t = t0 + i;
@@ -156,10 +175,12 @@ cudaError_t launch_lt(const LaunchCtx& c, const void* x, int64_t T, int H, int k
     cudaError_t st = allow_max_dynamic_smem(expand_cast_fp4_kernel<L, TOK, ZF>);
     if (st != cudaSuccess) return st;
   }
-  const int sf_bulk = (sfo.flags == 0 && sfo.stage == nullptr && G % 4 == 0 &&
+  const bool rowmajor = !(sfo.flags & MOE_SF_COLMAJOR) && sfo.stage == nullptr;
+  const int sf_bulk = (rowmajor && !(sfo.flags & MOE_SF_UE8M0) && G % 4 == 0 &&
                        reinterpret_cast<uintptr_t>(out_sf) % 16 == 0)
                           ? 1
                           : 0;
+  const int sf_wide = rowmajor && (sfo.flags & MOE_SF_UE8M0) ? ue8m0_store_width(out_sf, G) : 0;
   int64_t blocks = (T + TOK - 1) / TOK;
   if (ZF) {  // enough warps for one 32-row group of the zero-fill each
     const int64_t zb = ((R + 31) / 32 + threads / 32 - 1) / (threads / 32);
@@ -168,7 +189,7 @@ cudaError_t launch_lt(const LaunchCtx& c, const void* x, int64_t T, int H, int k
   if (blocks < 1) blocks = 1;
   return launch_pdl(expand_cast_fp4_kernel<L, TOK, ZF>, (unsigned)blocks, threads, smem, c.stream,
                     static_cast<const uint16_t*>(x), T, H, k, pos, R, out, out_sf, zsrc, sfo,
-                    sf_bulk, c.err);
+                    sf_bulk, sf_wide, c.err);
 }
 
 template <int L>

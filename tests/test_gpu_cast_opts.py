@@ -66,6 +66,38 @@ def test_expand_ex_parity(flags, T, H, k):
     _raw_equal(sf, o_sf, f"expand_ex sf flags={flags}")
 
 
+@pytest.mark.parametrize("flags,off", [(6, 0), (6, 1), (6, 4), (6, 8), (2, 0), (2, 4), (2, 16)])
+@pytest.mark.parametrize("T,H,k", [(7, 512, 3), (11, 1024, 32), (9, 1536, 5), (21, 7168, 8),
+                                   (6, 7168, 20), (3, 16384, 2)])
+def test_expand_ex_rowmajor_scales_at_offsets(flags, off, T, H, k):
+    """Row-major scales (f32 power-of-two, packed UE8M0 bytes) written into a
+    buffer that starts `off` bytes into an allocation: 8-, 4- and 1-byte
+    alignments for the bytes, 4 and 16 for the f32 rows, row lengths G of 4,
+    8, 12, 56 and 128 entries and k up to 32 copies.  The bytes around the
+    scale buffer must keep their fill."""
+    x = workloads.random_small(T, 16, k, H, seed=T * H + off, zero_groups=True)["x"]
+    R = T * k + 3
+    g = torch.Generator().manual_seed(off + H + k)
+    pos = torch.randperm(R, generator=g)[:T * k].to(torch.int32).view(T, k)
+    pos[1::3, k - 1] = -1
+    G = H // 128
+    ref, _ = oracle.sf_buffer(R, G, flags)
+    raw = np.ascontiguousarray(ref).view(np.uint8).reshape(-1)
+    buf = torch.full((raw.size + off + 32,), 0x5C, dtype=torch.uint8, device=DEV)
+    buf[off:off + raw.size] = torch.from_numpy(raw.copy()).to(DEV)
+    q = torch.full((R, H), 0xAB, dtype=torch.uint8, device=DEV)
+    ops.expand_cast_fp8_ex(x.to(DEV), pos.to(DEV), R, sf_flags=flags, out=q,
+                           out_sf=buf[off:off + raw.size])
+    assert ops.device_status() == 0
+    o_q, o_sf = oracle.expand_cast_fp8_ex(oracle.bf16_bits(x), pos.numpy(), num_rows=R,
+                                          flags=flags)
+    assert_equal(np_(q), o_q, "rowmajor q")
+    got = np_(buf)
+    assert_equal(got[off:off + raw.size], np.ascontiguousarray(o_sf).view(np.uint8).reshape(-1),
+                 "rowmajor sf")
+    assert (got[:off] == 0x5C).all() and (got[off + raw.size:] == 0x5C).all()
+
+
 @pytest.mark.parametrize("flags", FLAGS)
 @pytest.mark.parametrize("T,E,k,H,align", [(60, 16, 4, 512, 32), (37, 16, 2, 384, 16),
                                            (30, 8, 8, 7168, 128)])

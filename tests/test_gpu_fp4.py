@@ -63,6 +63,36 @@ def test_expand_fp4_parity(group, flags, T, H, k):
     _raw_equal(sf, o_sf, f"fp4 sf group={group} flags={flags}")
 
 
+@pytest.mark.parametrize("flags,off", [(6, 1), (6, 4), (6, 8), (2, 4), (2, 16)])
+@pytest.mark.parametrize("group,T,H,k", [(32, 21, 7168, 8), (16, 6, 7168, 20), (32, 9, 384, 5),
+                                         (128, 11, 512, 32), (64, 3, 16384, 2)])
+def test_expand_fp4_rowmajor_scales_at_offsets(flags, off, group, T, H, k):
+    """Row-major scales (power-of-two f32, packed UE8M0 bytes) written into a
+    buffer `off` bytes into an allocation: the byte rows go out 8, 4 or 1
+    bytes per store, the f32 rows by bulk copy or per group; rows of 4 to 448
+    entries, k up to 32.  The bytes around the buffer keep their fill."""
+    x = workloads.random_small(T, 16, k, H, seed=T * H + off + group, zero_groups=True)["x"]
+    R = T * k + 3
+    g = torch.Generator().manual_seed(off + H + k + group)
+    pos = torch.randperm(R, generator=g)[:T * k].to(torch.int32).view(T, k)
+    pos[1::3, k - 1] = -1
+    ref, _ = oracle.sf_buffer(R, H // group, flags)
+    raw = np.ascontiguousarray(ref).view(np.uint8).reshape(-1)
+    buf = torch.full((raw.size + off + 32,), 0x5C, dtype=torch.uint8, device=DEV)
+    buf[off:off + raw.size] = torch.from_numpy(raw.copy()).to(DEV)
+    q = torch.full((R, H // 2), 0xAB, dtype=torch.uint8, device=DEV)
+    ops.expand_cast_fp4(x.to(DEV), pos.to(DEV), R, group=group, sf_flags=flags, out=q,
+                        out_sf=buf[off:off + raw.size])
+    assert ops.device_status() == 0
+    o_q, o_sf = oracle.expand_cast_fp4(oracle.bf16_bits(x), pos.numpy(), num_rows=R, group=group,
+                                       flags=flags)
+    assert_equal(np_(q), o_q, "fp4 rowmajor q")
+    got = np_(buf)
+    assert_equal(got[off:off + raw.size], np.ascontiguousarray(o_sf).view(np.uint8).reshape(-1),
+                 "fp4 rowmajor sf")
+    assert (got[:off] == 0x5C).all() and (got[off + raw.size:] == 0x5C).all()
+
+
 @pytest.mark.parametrize("group", [16, 32, 128])
 @pytest.mark.parametrize("flags,staged", [(1, False), (1, True), (3, True), (7, False), (7, True)])
 def test_expand_fp4_colmajor_and_padded(group, flags, staged):
