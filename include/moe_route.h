@@ -103,6 +103,8 @@ typedef enum moe_out_dtype {
 #define MOE_DEVERR_DUPLICATE_EXPERT 0x4u /* route_map: a token names an expert twice */
 #define MOE_DEVERR_ROWS_SHORT 0x8u   /* route_map_aligned: num_rows < padded total */
 #define MOE_DEVERR_TIMEOUT 0x10u     /* fused decode path: a bounded wait ran out */
+#define MOE_DEVERR_BOUNDS 0x20u      /* debug-bounds library only: an internal index
+                                        or alignment check failed, access skipped */
 
 /* Paths of moe_route_expand_cast_fp8. */
 #define MOE_PATH_AUTO 0       /* the library's choice (see moe_route_expand_cast_fp8)     */
@@ -531,6 +533,27 @@ int32_t moe_abi_version(void);
 
 /* Number of kernels this library has launched in this process so far. */
 uint64_t moe_kernel_launch_count(void);
+
+/*
+ * Debug-bounds build.  The same sources compiled with MOE_DEBUG_BOUNDS
+ * defined give libmoe_route_debug.so (the Python binding loads it when the
+ * environment variable MOE_DEBUG_BOUNDS is 1).  Its kernels check, before the
+ * access each guards, invariants that the normal build takes from the kernels'
+ * construction: the alignment, size and shared-memory source of every TMA bulk
+ * copy, the alignment of wide scale stores, the shared-memory extent of the
+ * staging slots, and the sorted_src row of every copy the decode kernels
+ * place.  A failed check skips that access and sets MOE_DEVERR_BOUNDS; no
+ * kernel traps.  Results are otherwise identical to the normal build's.
+ *
+ * moe_debug_bounds_enabled: 1 in the debug-bounds library, 0 otherwise.
+ * moe_debug_bounds_selftest: in the debug-bounds library, launches one
+ *   kernel whose single check is false by construction (it guards no memory
+ *   access), so that the next moe_get_device_status reports
+ *   MOE_DEVERR_BOUNDS; returns MOE_OK, or MOE_ERR_CUDA if the launch failed.
+ *   In the normal library: MOE_ERR_UNSUPPORTED, nothing launched.
+ */
+int32_t moe_debug_bounds_enabled(void);
+moe_status_t moe_debug_bounds_selftest(void *stream);
 
 #ifdef __cplusplus
 }

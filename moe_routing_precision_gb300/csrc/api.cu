@@ -98,6 +98,17 @@ cudaError_t allow_max_dynamic_smem(const void* kernel) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, cap);
 }
 
+#ifdef MOE_DEBUG_BOUNDS
+namespace {
+// The debug-bounds self-test: one check that is false by construction (a
+// one-thread launch has no thread 1), guarding no memory access.
+__global__ void debug_bounds_selftest_kernel(unsigned* err) {
+  pdl_enter();
+  (void)MOE_DBG_OK(threadIdx.x == 1, err);
+}
+}  // namespace
+#endif
+
 }  // namespace moe
 
 using namespace moe;
@@ -107,6 +118,22 @@ extern "C" {
 int32_t moe_abi_version(void) { return MOE_ROUTE_ABI_VERSION; }
 
 uint64_t moe_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+#ifdef MOE_DEBUG_BOUNDS
+int32_t moe_debug_bounds_enabled(void) { return 1; }
+
+moe_status_t moe_debug_bounds_selftest(void* stream) {
+  LaunchCtx c;
+  moe_status_t s = context(stream, &c);
+  if (s != MOE_OK) return s;
+  cudaError_t e = launch_pdl(debug_bounds_selftest_kernel, 1, 1, 0, c.stream, c.err);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e);
+}
+#else
+int32_t moe_debug_bounds_enabled(void) { return 0; }
+
+moe_status_t moe_debug_bounds_selftest(void*) { return MOE_ERR_UNSUPPORTED; }
+#endif
 
 const char* moe_last_cuda_error_string(void) { return g_last_cuda_error; }
 

@@ -19,6 +19,44 @@ constexpr float kE4M3Max = 448.0f;
 constexpr float kScaleFloor = 1e-4f;
 constexpr int kGroup = 128;
 
+// ------------------------------------------------------------ error flags
+
+// Sets `bit` in the library's device error word (moe_get_device_status).
+__device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// Debug-bounds build (compiled with MOE_DEBUG_BOUNDS defined): MOE_DBG_OK
+// checks an index, size or alignment invariant that the kernel's
+// construction guarantees, before the access it guards.  A false check sets
+// MOE_DEVERR_BOUNDS and the caller skips the access; nothing traps.  In the
+// normal build it is the constant true and the condition is not compiled.
+#ifdef MOE_DEBUG_BOUNDS
+__device__ __forceinline__ bool dbg_check(bool ok, unsigned* err) {
+  if (!ok) flag_error(err, MOE_DEVERR_BOUNDS);
+  return ok;
+}
+#define MOE_DBG_OK(cond, err) ::moe::dbg_check((cond), (err))
+#else
+#define MOE_DBG_OK(cond, err) true
+#endif
+
+// This launch's dynamic shared memory, in bytes.
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t n;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(n));
+  return n;
+}
+
+// The preconditions of a bulk shared -> global copy: the global and shared
+// addresses and the size multiples of 16 bytes, the source inside this CTA's
+// dynamic shared memory (which starts at the shared address sbase).
+__device__ __forceinline__ bool bulk_copy_ok(const void* gdst, uint32_t ssrc, uint32_t bytes,
+                                             uint32_t sbase) {
+  return ((reinterpret_cast<uintptr_t>(gdst) | ssrc | bytes) & 15u) == 0 && ssrc >= sbase &&
+         ssrc - sbase + bytes <= dynamic_smem_bytes();
+}
+
 // ---------------------------------------------------------------- memory ops
 
 // 16-byte streaming load of data read exactly once: non-coherent path, no L1
@@ -141,13 +179,17 @@ __host__ __device__ __forceinline__ int ue8m0_store_width(const void* out_sf, in
 // store: G / n stores per row, spread over the lanes.
 __device__ __forceinline__ void store_ue8m0_rows(uint8_t* out_sf, const uint8_t* src,
                                                  const int32_t* spos, int k, int G, int64_t R,
-                                                 int n, int lane) {
+                                                 int n, int lane, unsigned* err) {
   const int per = G / n;
   for (int u = lane; u < k * per; u += 32) {
     const int j = u / per, c = u - j * per;
     const int32_t r = spos[j];
     if (r < 0 || r >= R) continue;
     uint8_t* dst = out_sf + (int64_t)r * G + c * n;
+    if (!MOE_DBG_OK(((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src)) &
+                     (uintptr_t)(n - 1)) == 0,
+                    err))
+      continue;
     if (n == 8)
       *reinterpret_cast<uint64_t*>(dst) = *reinterpret_cast<const uint64_t*>(src + c * n);
     else
@@ -300,10 +342,6 @@ struct FastDiv {
 // entry instead let waiting CTAs of the next kernel take SMs early and
 // unbalanced the one-CTA-per-SM expand grid on GB300.)
 __device__ __forceinline__ void pdl_enter() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-__device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) {
-  if (err) atomicOr(err, bit);
-}
 
 }  // namespace moe
 

@@ -185,7 +185,7 @@ __device__ void route_block(const DecodeArgs& a, uint32_t* bm, uint16_t* pre, in
     const int wd = (t >> 5) * E + e;
     const int r = s_off[e] + pre[wd] + __popc(bm[wd] & ((1u << (t & 31)) - 1u));
     a.pos[p] = r;
-    s_src[r] = p;
+    if (MOE_DBG_OK(r >= 0 && r < P, a.err)) s_src[r] = p;
   }
   __syncthreads();
   // sorted_src leaves in row order (coalesced): scattered 4-byte global stores

@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kRepThreads, 1) decode_replicated_kernel(RepAr
     if (b0) {
       a.idx[p] = e;
       a.pos[p] = r;
-      if (r >= 0) a.src[r] = p;
+      if (r >= 0 && MOE_DBG_OK(r < P, a.err)) a.src[r] = p;
     }
   }
   __syncthreads();
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kRepThreads, 1) route_expand_replicated_kernel
     if ((unsigned)e < (unsigned)E) {
       const int wd = (tt >> 5) * E + e;
       r = s_off[e] + pre[wd] + __popc(bm[wd] & ((1u << (tt & 31)) - 1u));
-      a.src[r] = p;
+      if (MOE_DBG_OK(r >= 0 && r < P, a.err)) a.src[r] = p;
     } else {
       bad = true;  // top-k never selects one
     }

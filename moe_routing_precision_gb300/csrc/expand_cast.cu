@@ -323,6 +323,10 @@ __global__ void __maxnreg__(32) expand_cast_bulk_kernel(
   const uint32_t stride = (uint32_t)((H + 4 * G + 127) / 128 * 128);  // bytes per token slot
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(s_buf);
   int32_t* spos_all = reinterpret_cast<int32_t*>(s_buf + (size_t)TOK * stride);  // [TOK][32]
+  // the slots and the destination lists fit the launch's shared memory
+  if (!MOE_DBG_OK((size_t)TOK * (stride + 128) <= dynamic_smem_bytes() && 16 * P <= (int)stride,
+                  err))
+    return;  // the same for every thread of the CTA
   bool bad = false;
   const int flags = OPTS ? sfo.flags : 0;
   // Scale layouts: row-major f32 (power-of-two rounded or not) leaves with the
@@ -389,7 +393,7 @@ __global__ void __maxnreg__(32) expand_cast_bulk_kernel(
       for (int i = 0; i < TOK; ++i)
         if (t0 + i < T)
           store_ue8m0_rows(reinterpret_cast<uint8_t*>(out_sf), s_buf + (size_t)i * stride + H,
-                           spos_all + i * 32, k, G, R, sf_wide, lane);
+                           spos_all + i * 32, k, G, R, sf_wide, lane, err);
     }
   } else if (!sf_bulk && act && l8 == 0) {  // scale options: per-group scale stores
 #pragma unroll
@@ -416,7 +420,10 @@ __global__ void __maxnreg__(32) expand_cast_bulk_kernel(
         if (tid == 0 && r >= 0) {
           if (r >= R) {
             bad = true;
-          } else {
+          } else if (MOE_DBG_OK(bulk_copy_ok(out + (int64_t)r * H, slot, (uint32_t)H, sbase) &&
+                                    (!sf_bulk || bulk_copy_ok(out_sf + (int64_t)r * G, slot + H,
+                                                              (uint32_t)(4 * G), sbase)),
+                                err)) {
             if (hint)
               bulk_s2g_hint(out + (int64_t)r * H, slot, (uint32_t)H, policy);
             else

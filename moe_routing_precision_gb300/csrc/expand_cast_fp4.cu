@@ -66,6 +66,10 @@ __global__ void __maxnreg__(32) expand_cast_fp4_kernel(
   const uint32_t stride = (uint32_t)((HB + 4 * G + 127) / 128 * 128);  // bytes per token slot
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(s_buf);
   int32_t* spos_all = reinterpret_cast<int32_t*>(s_buf + (size_t)TOK * stride);  // [TOK][32]
+  // the slots and the destination lists fit the launch's shared memory
+  if (!MOE_DBG_OK((size_t)TOK * (stride + 128) <= dynamic_smem_bytes() && 8 * P <= (int)stride,
+                  err))
+    return;  // the same for every thread of the CTA
   bool bad = false;
   const int64_t t0 = (int64_t)blockIdx.x * TOK;
   // every load of the CTA's tokens is issued before any of them is used
@@ -112,7 +116,7 @@ __global__ void __maxnreg__(32) expand_cast_fp4_kernel(
       for (int i = 0; i < TOK; ++i)
         if (t0 + i < T)
           store_ue8m0_rows(reinterpret_cast<uint8_t*>(out_sf), s_buf + (size_t)i * stride + HB,
-                           spos_all + i * 32, k, G, R, sf_wide, lane);
+                           spos_all + i * 32, k, G, R, sf_wide, lane, err);
     }
   } else if (!sf_bulk && act && lead) {  // one lane per group stores its scale
 #pragma unroll
@@ -140,7 +144,10 @@ __global__ void __maxnreg__(32) expand_cast_fp4_kernel(
         if (tid == 0 && r >= 0) {
           if (r >= R) {
             bad = true;
-          } else {
+          } else if (MOE_DBG_OK(bulk_copy_ok(out + (int64_t)r * HB, slot, (uint32_t)HB, sbase) &&
+                                    (!sf_bulk || bulk_copy_ok(out_sf + (int64_t)r * G, slot + HB,
+                                                              (uint32_t)(4 * G), sbase)),
+                                err)) {
             bulk_s2g(out + (int64_t)r * HB, slot, (uint32_t)HB);
             if (sf_bulk) bulk_s2g(out_sf + (int64_t)r * G, slot + HB, (uint32_t)(4 * G));
           }

@@ -15,13 +15,13 @@ import threading
 
 import torch
 
-from ._build import LIB_PATH
+from ._build import lib_path
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(5)
 MOE_WEIGHTS_NONE, MOE_WEIGHTS_SOFTMAX_TOPK = 0, 1
 MOE_OUT_BF16, MOE_OUT_F32 = 0, 1
 MOE_DEVERR_EXPERT_RANGE, MOE_DEVERR_POS_RANGE, MOE_DEVERR_DUPLICATE_EXPERT = 0x1, 0x2, 0x4
-MOE_DEVERR_ROWS_SHORT = 0x8
+MOE_DEVERR_ROWS_SHORT, MOE_DEVERR_TIMEOUT, MOE_DEVERR_BOUNDS = 0x8, 0x10, 0x20
 GROUP = 128
 SF_COLMAJOR, SF_POW2, SF_UE8M0 = 0x1, 0x2, 0x4
 
@@ -64,28 +64,39 @@ SIGNATURES = {
     "moe_last_cuda_error_string": (ctypes.c_char_p, []),
     "moe_abi_version": (ctypes.c_int32, []),
     "moe_kernel_launch_count": (ctypes.c_uint64, []),
+    "moe_debug_bounds_enabled": (ctypes.c_int32, []),
+    "moe_debug_bounds_selftest": (ctypes.c_int, [_P]),
 }
 
 _lock = threading.Lock()
 _lib = None
 
 
+def load_library(path: str) -> ctypes.CDLL:
+    """Load a build of the library at `path` and set every signature."""
+    L = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib() -> ctypes.CDLL:
-    """The loaded ``libmoe_route.so`` (raises if it has not been built)."""
+    """The loaded ``libmoe_route.so``, or ``libmoe_route_debug.so`` when the
+    environment variable MOE_DEBUG_BOUNDS is 1 at the first call (raises if
+    it has not been built)."""
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
+            path = lib_path()
+            if not os.path.exists(path):
                 raise RuntimeError(
-                    f"{LIB_PATH} is missing: build it with moe_routing_precision_gb300.build() "
+                    f"{path} is missing: build it with moe_routing_precision_gb300.build() "
                     "(nvcc, sm_103a); there is no CPU fallback")
-            L = ctypes.CDLL(LIB_PATH)
-            for name, (res, args) in SIGNATURES.items():
-                fn = getattr(L, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = L
+            _lib = load_library(path)
     return _lib
+
 
 
 class MoeError(RuntimeError):
@@ -248,7 +259,6 @@ def sf_empty(rows: int, G: int, flags: int, ld: int | None, like: torch.Tensor):
 
 
 PATH_AUTO, PATH_FUSED, PATH_SEPARATE, PATH_REPLICATED, PATH_CHAINED = 0, 1, 2, 3, 4
-MOE_DEVERR_TIMEOUT = 0x10
 DEBUG_WAIT_TIMEOUT_NS, DEBUG_SKIP_ROUTE_SIGNAL = 1, 2
 
 

@@ -264,3 +264,39 @@ def test_debug_cvt_rejects_bad_arguments(L):
     assert f(1, FAKE + 4, FAKE, 16, None) == INVALID      # alignment
     assert f(0, None, None, 0, None) == 0
     assert L.moe_kernel_launch_count() == 0
+
+
+def test_debug_bounds_entry_points_of_the_normal_library(L):
+    """The normal library reports no debug checks and refuses the self-test
+    without launching anything."""
+    from moe_routing_precision_gb300 import ops
+    n = L.moe_kernel_launch_count()
+    assert L.moe_debug_bounds_enabled() == 0
+    assert L.moe_debug_bounds_selftest(None) == ops.MOE_ERR_UNSUPPORTED
+    assert L.moe_kernel_launch_count() == n
+
+
+def test_debug_bounds_library_builds_and_exports_every_symbol():
+    """libmoe_route_debug.so (the sources with MOE_DEBUG_BOUNDS defined)
+    builds, exports the header's symbols, says it is the debug build, and
+    rejects bad arguments on the host exactly as the normal library does."""
+    from moe_routing_precision_gb300 import ops
+    path = _build.build(debug_bounds=True)
+    assert path == _build.DEBUG_LIB_PATH and path != _build.LIB_PATH
+    D = ops.load_library(path)
+    for n in _declared_functions():
+        assert hasattr(D, n), n
+    assert D.moe_debug_bounds_enabled() == 1
+    assert D.moe_abi_version() == 1
+    assert D.moe_topk_gate(FAKE, 4, 16, 17, FAKE, FAKE, 1, None) == INVALID
+    assert D.moe_peak_copy(FAKE + 1, FAKE, 32, None) == INVALID
+    assert D.moe_kernel_launch_count() == 0
+
+
+def test_library_choice_follows_the_environment(monkeypatch):
+    monkeypatch.setenv("MOE_DEBUG_BOUNDS", "1")
+    assert _build.lib_path() == _build.DEBUG_LIB_PATH
+    monkeypatch.setenv("MOE_DEBUG_BOUNDS", "0")
+    assert _build.lib_path() == _build.LIB_PATH
+    monkeypatch.delenv("MOE_DEBUG_BOUNDS")
+    assert _build.lib_path() == _build.LIB_PATH
