@@ -298,14 +298,13 @@ __device__ __forceinline__ void chain_place(const RouteChain& rc, int64_t t0, in
   }
 }
 
-// Held to 32 registers (the form with options and the zero-fill spills 4 bytes), so
-// that 4 CTAs of 448 threads (H = 7168) fit an SM; with more registers only 3
-// or 2 do, and the bandwidth follows the tokens in flight.  Measured on GB300
-// at T = 65536 (H = 7168, k = 8, after an L2 flush) with packed UE8M0
-// column-major scales (staged, with the zero-fill): 0.765 ms at 56 registers
-// and two tokens per CTA (2 CTAs per SM), 0.714 ms at 40 (3 CTAs per SM),
-// 0.704 ms at 32 with one token per CTA; the padded layout 0.763 -> 0.738 ms
-// between the last two.
+// Held to 32 registers (no spills), so that 4 CTAs of 448 threads
+// (H = 7168) fit an SM; with more registers only 3 or 2 do, and the bandwidth
+// follows the tokens in flight.  Measured on GB300 at T = 65536 (H = 7168,
+// k = 8, after an L2 flush) with packed UE8M0 column-major scales (staged,
+// with the zero-fill): 0.765 ms at 56 registers and two tokens per CTA (2 CTAs
+// per SM), 0.714 ms at 40 (3 CTAs per SM), 0.704 ms at 32 with one token per
+// CTA; the padded layout 0.763 -> 0.738 ms between the last two.
 template <int TOK, bool OPTS, bool ZF, bool CHAIN>
 __global__ void __maxnreg__(32) expand_cast_bulk_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
