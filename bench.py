@@ -1261,7 +1261,8 @@ def reference_arm(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=int(os.environ.get("MOE_BENCH_ITERS", "300")),
+                    help="timed steps (default: $MOE_BENCH_ITERS, else 300)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--e2e-steps", type=int, default=30,
