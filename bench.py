@@ -444,7 +444,9 @@ def gpu_arm(args):
         "route_expand_cast": {"ms": round(rec_ms_mean, 4), "GB_s": round(rec_gbs, 1),
                               "frac_of_peak": round(rec_gbs / peak, 4),
                               "frac_of_nominal": round(rec_gbs / NOMINAL_HBM_GBS, 4),
-                              "algorithmic_bytes": B["route_expand_cast"]},
+                              "algorithmic_bytes": B["route_expand_cast"],
+                              "tokens_per_s": round(T * world / (rec_ms_mean * 1e-3), 1),
+                              "routed_rows_per_s": round(R * world / (rec_ms_mean * 1e-3), 1)},
         "step_routed_tokens_per_s": round(R * world / (step_ms * 1e-3), 1),
     })
     if args.detail_out:
