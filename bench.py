@@ -47,7 +47,7 @@ UNIT = "routed tokens/s"
 WORKLOAD = "prefill_64k"
 SWIGLU_N = 2048
 FALLBACK_HBM_GBS = 6800.0
-DETAIL_DEFAULT = os.path.join("gpurun_out", "bench_detail.json")
+DETAIL_DEFAULT = os.path.join("bench_out", "bench_detail.json")
 
 
 # ---------------------------------------------------------------- helpers
