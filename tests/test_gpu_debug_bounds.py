@@ -6,7 +6,7 @@ alignment checks compiled in).
    guards no access: the device error word must then read MOE_DEVERR_BOUNDS,
    and nothing else.
 2. The parity suites of the bulk-store expand kernels, the chained and decode
-   paths and the canaries run again in a child process with
+   paths, the canaries and the shape fuzz run again in a child process with
    MOE_DEBUG_BOUNDS=1, so every kernel they launch carries its checks: every
    result must still match the oracle and no check may fail (each module
    asserts a clean device error word at its end, and every test that expects
@@ -55,7 +55,8 @@ def test_parity_suites_pass_with_the_checks_compiled_in(D):
         cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert probe.returncode == 0 and probe.stdout.strip() == "1", probe.stderr
     suites = ["tests/test_gpu_parity.py", "tests/test_gpu_cast_opts.py", "tests/test_gpu_fp4.py",
-              "tests/test_gpu_chain.py", "tests/test_gpu_decode.py", "tests/test_gpu_canary.py"]
+              "tests/test_gpu_chain.py", "tests/test_gpu_decode.py", "tests/test_gpu_canary.py",
+              "tests/test_gpu_fuzz.py"]
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-m", "gpu",
                         "-p", "no:cacheprovider", *suites],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=1500)
