@@ -18,17 +18,23 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr bool kExtPersistent = true;  // the variants' grid (see kGridNote)
 
 // kGridNote: the plain forms' grid is not persistent.  One warp per tile of
 // units, so the CTAs in flight at any moment cover a compact run of
 // consecutive rows.  Measured on GB300 (65536 rows of 2 x 2048, after an L2
 // flush / back to back): E4M3 0.929 / 0.968 of the measured copy peak against
 // 0.895 / 0.941 for a persistent grid of the resident CTAs striding over the
-// tiles; E2M1 (group 32) 0.906 / 0.936 against 0.870 / 0.898.  The variants
-// (EXT) measured the other way round and keep the persistent grid: with
-// per-row weights 0.86 / 0.90 persistent against 0.82 / 0.85; with clamp,
-// weights, count and packed UE8M0 column-major scales 0.80 / 0.84 against
-// 0.75 / 0.78.  The loops stride, so any grid size is correct.
+// tiles; E2M1 (group 32) 0.906 / 0.936 against 0.870 / 0.898.  Writing the
+// loop so that the compiler sees at most one tile per warp (its bound
+// min(tiles, first + 1) instead of a stride) then gave, in one A/B: E4M3
+// 0.929 -> 0.947 and 0.965 -> 0.992, E2M1 0.888 -> 0.906 and 0.937 -> 0.957
+// (at 524288 rows E4M3 0.984 -> 1.006 single), output unchanged.  The variants (EXT) measured the other way round and keep the
+// persistent grid (kExtPersistent): with per-row weights 0.86 / 0.90
+// persistent against 0.82 / 0.85; with clamp, weights, count and packed UE8M0
+// column-major scales 0.80 / 0.84 against 0.79 / 0.82 (E2M1 with clamp,
+// weights and count 0.78 / 0.82 against 0.74 / 0.77).  The loops stride when
+// persistent, so any grid size is correct for the variants.
 
 __device__ __forceinline__ float swiglu(float g, float u) {
   // evaluated in the order written on the page, in f32, with the hardware
@@ -118,7 +124,13 @@ __global__ void __launch_bounds__(kThreads, EXT ? 5 : 6)
   const uint32_t tiles = (units + 3) >> 2;
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   unsigned clamped = 0;
-  for (uint32_t tile = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; tile < tiles; tile += warps) {
+  // the grid covers every tile (each warp its own), or, persistent, strides
+  // over them (see kGridNote)
+  const uint32_t gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const bool strided = EXT && kExtPersistent;
+  const uint32_t t_step = strided ? warps : 1u;
+  const uint32_t t_end = strided ? tiles : min(tiles, gw + 1);
+  for (uint32_t tile = gw; tile < t_end; tile += t_step) {
     const uint32_t u = tile * 4 + sub;
     const bool active = u < units;
     const uint32_t r = active ? fdG.div(u) : 0;
@@ -173,7 +185,11 @@ __global__ void __launch_bounds__(kThreads, EXT ? 5 : 6)
   const uint32_t tiles = (units + U - 1) / U;
   const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   unsigned clamped = 0;
-  for (uint32_t tile = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; tile < tiles; tile += warps) {
+  const uint32_t gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const bool strided = EXT && kExtPersistent;
+  const uint32_t t_step = strided ? warps : 1u;
+  const uint32_t t_end = strided ? tiles : min(tiles, gw + 1);
+  for (uint32_t tile = gw; tile < t_end; tile += t_step) {
     const uint32_t u = tile * U + sub;
     const bool active = u < units;
     const uint32_t r = active ? fdG.div(u) : 0;
@@ -216,7 +232,7 @@ cudaError_t launch_t(const LaunchCtx& c, const void* x, int64_t M, int N, uint8_
   const uint32_t tiles = (units + 3) / 4;
   const int64_t need = ((int64_t)tiles + (kThreads / 32) - 1) / (kThreads / 32);
   int64_t cap = need;
-  if (EXT) {  // the variants keep a persistent grid: see kGridNote
+  if (EXT && kExtPersistent) {  // see kGridNote
     int per_sm = 0;
     cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &per_sm, swiglu_cast_kernel<EXT>, kThreads, 0);
@@ -238,7 +254,7 @@ cudaError_t launch_fp4_t(const LaunchCtx& c, const void* x, int64_t M, int N, ui
   const uint32_t tiles = (units + U - 1) / U;
   const int64_t need = ((int64_t)tiles + (kThreads / 32) - 1) / (kThreads / 32);
   int64_t cap = need;
-  if (EXT) {  // the variants keep a persistent grid: see kGridNote
+  if (EXT && kExtPersistent) {  // see kGridNote
     int per_sm = 0;
     cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &per_sm, swiglu_cast_fp4_kernel<L, EXT>, kThreads, 0);
