@@ -68,20 +68,17 @@ __global__ void __launch_bounds__(kThreads) expand_cast_kernel(
   const int l8 = lane & 7;    // 16-channel slice within the group
   const int G = H >> 7;
   const uint32_t tiles = (units + 3) >> 2;
-  const uint32_t warps = (gridDim.x * blockDim.x) >> 5;
   bool bad = false;
-  uint32_t tile = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  TileIn cur;
-  if (tile < tiles) load_tile(x, pos, tile, sub, l8, units, fdG, G, H, k, cur);
-  for (; tile < tiles; tile += warps) {
+  // one tile per warp: the grid covers every tile (launch_g)
+  const uint32_t tile = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (tile < tiles) {
+    TileIn cur;
+    load_tile(x, pos, tile, sub, l8, units, fdG, G, H, k, cur);
     const uint4 a = cur.a, b = cur.b;
     const uint32_t t = cur.t;
     const int g = cur.g;
     const bool active = cur.active;
     int32_t mine = cur.pos0;
-    // start the next tile's loads; they stay in flight while this tile's k
-    // rows are written
-    if (tile + warps < tiles) load_tile(x, pos, tile + warps, sub, l8, units, fdG, G, H, k, cur);
     const float amax = max8(absmax16_bf16(a, b));
     const float sf = group_scale_opts(amax, sfo.flags);
     const float inv = __fdiv_rn(1.0f, sf);
@@ -131,8 +128,7 @@ __global__ void __launch_bounds__(kThreads) expand_cast_kernel(
 // token, thread c of a token owning channels 16c..16c+15.  All k destination
 // rows of a token are therefore written by one CTA at the same moment, which
 // keeps fewer rows open across HBM at once than the tile form: on GB300 a
-// scattered-row copy ran ~7% faster this way.  The next token's slice is
-// loaded before the current one is stored.
+// scattered-row copy ran ~7% faster this way.
 template <bool G4>
 __global__ void __launch_bounds__(1024) expand_cast_rows_kernel(
     const uint16_t* __restrict__ x, int64_t T, int H, int k, const int32_t* __restrict__ pos,
@@ -150,29 +146,18 @@ __global__ void __launch_bounds__(1024) expand_cast_rows_kernel(
   const bool slot_ok = tl < tpc;
   const int64_t groups = (T + tpc - 1) / tpc;
   bool bad = false;
-  int64_t grp = blockIdx.x;
-  uint4 a = make_uint4(0, 0, 0, 0), b = a;
-  int32_t pos0 = -1;
-  {
-    const int64_t t = grp * tpc + tl;
-    if (slot_ok && grp < groups && t < T) {
-      const uint16_t* src = x + t * H + c * 16;
-      a = ld_stream_v4(src);
-      b = ld_stream_v4(src + 8);
-      pos0 = (l8 < k) ? __ldg(pos + t * k + l8) : -1;
-    }
-  }
-  for (; grp < groups; grp += gridDim.x) {
+  // one token group per CTA: the grid covers every group (launch_rows)
+  const int64_t grp = blockIdx.x;
+  if (grp < groups) {
     const int64_t t = grp * tpc + tl;
     const bool active = slot_ok && t < T;
-    const uint4 ca = a, cb = b;
-    int32_t mine = pos0;
-    const int64_t tn = (grp + gridDim.x) * tpc + tl;
-    if (slot_ok && grp + gridDim.x < groups && tn < T) {
-      const uint16_t* src = x + tn * H + c * 16;
-      a = ld_stream_v4(src);
-      b = ld_stream_v4(src + 8);
-      pos0 = (l8 < k) ? __ldg(pos + tn * k + l8) : -1;
+    uint4 ca = make_uint4(0, 0, 0, 0), cb = ca;
+    int32_t mine = -1;
+    if (active) {
+      const uint16_t* src = x + t * H + c * 16;
+      ca = ld_stream_v4(src);
+      cb = ld_stream_v4(src + 8);
+      mine = (l8 < k) ? __ldg(pos + t * k + l8) : -1;
     }
     const float amax = max8(absmax16_bf16(ca, cb));
     const float sf = group_scale_opts(amax, sfo.flags);
@@ -514,8 +499,12 @@ namespace {
 // over it, as the bulk form's: measured on GB300 (k = 8, after an L2 flush)
 // the row form at H = 7296 (G = 57) ran at 0.84 of the measured copy peak
 // against 0.73, at H = 640 at 0.63 against 0.42, and the tile form at
-// H = 20480 at 0.96 against 0.82.  The loops still stride, so any grid size
-// is correct.
+// H = 20480 at 0.96 against 0.82.  Each CTA or warp takes exactly its own
+// group or tile (no loop, no prefetch of a next one), so the grid must cover
+// them all; against the same grid with striding loops that prefetched the
+// next item: row form 221.9 -> 215.7 us at T = 16384, H = 7296 and 86.7 ->
+// 84.6 us at T = 65536, H = 640; tile form 269.0 -> 264.9 us at T = 8192,
+// H = 20480 (output unchanged).
 template <bool G4>
 cudaError_t launch_rows(const LaunchCtx& c, const void* x, int64_t T, int H, int k,
                         const int32_t* pos, int64_t R, uint8_t* out, float* out_sf,
