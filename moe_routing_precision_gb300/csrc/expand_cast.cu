@@ -11,8 +11,8 @@
 // Three forms, all with one 128-channel group per aligned 8-lane subgroup
 // (lane l holds channels 16l..16l+15, two 16-byte loads; the group amax is a
 // 3-step xor shuffle):
-//   bulk (H <= 16384, H/128 % 4 == 0, 16-byte aligned out and out_sf): one
-//     CTA per one or two tokens, the rows leave by TMA bulk copies;
+//   bulk (H <= 16384, H/128 % 4 == 0, 16-byte aligned out): one CTA per
+//     token, the rows leave by TMA bulk copies;
 //   row (other H <= 16384): whole tokens per CTA, 16-byte stores;
 //   tile (H > 16384): one warp per 4 consecutive (token, group) units.
 // HBM traffic is ~80% writes (k copies of 1 byte per channel plus scales,
@@ -211,8 +211,10 @@ __global__ void __launch_bounds__(1024) expand_cast_rows_kernel(
 // shared -> global) issued by one thread, so no warp waits on k store
 // instructions per slice.  The CTA retires once the copies have read shared
 // memory (cp.async.bulk.wait_group.read).
-// Needs G % 4 == 0 and 16-byte aligned out / out_sf (bulk copies move
-// multiples of 16 bytes between 16-byte aligned addresses).
+// Needs G % 4 == 0 and a 16-byte aligned out, and for the bulk copy of
+// row-major f32 scales a 16-byte aligned out_sf (bulk copies move multiples
+// of 16 bytes between 16-byte aligned addresses); packed UE8M0 row-major
+// scales take 8-, 4- or 1-byte stores by the alignment they find.
 __device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
                "r"(bytes)
@@ -240,8 +242,7 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
 
 // OPTS: scale options (sfo.flags != 0) are compiled in; ZF: the zero-fill of
 // the padding rows (zsrc non-null) is.  The plain form (row-major f32 scales,
-// copied in bulk with the codes; no padding) keeps fewer registers, so more
-// CTAs are resident.
+// copied in bulk with the codes; no padding) compiles neither.
 // The chained form's prologue (warp 0, CHAIN): each of the CTA's copies is
 // placed at offsets[e] + base[chunk][e] (the copies of expert e in earlier
 // chunks) + its rank among its expert's copies in the chunk (held in pos on
