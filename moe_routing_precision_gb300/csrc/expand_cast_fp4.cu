@@ -9,12 +9,13 @@
 // scales to the rows pos names.  Two codes per byte, element 2i in the low
 // nibble.  Group sizes 16, 32, 64 and 128 (1, 2, 4 or 8 lanes of 16 channels).
 //
-// Same structure as the E4M3 bulk-store kernel: one CTA per two consecutive
-// tokens, thread c owning channels 16c..16c+15; each token's packed codes
-// (H/2 bytes) and, for plain row-major f32 scales with G % 4 == 0, its scales
+// Same structure as the E4M3 bulk-store kernel: one CTA per token (see
+// kFp4TokensPerCta), thread c owning channels 16c..16c+15; each token's packed
+// codes (H/2 bytes) and, for row-major f32 scales with G % 4 == 0, its scales
 // are staged in shared memory and leave with TMA bulk copies (cp.async.bulk)
-// issued by one thread; other scale layouts are stored per group by one lane,
-// or staged per token for the column-major gather.
+// issued by one thread; row-major UE8M0 scales leave by one warp's wide
+// stores; column-major scales are stored per group by one lane, or staged per
+// token for the column-major gather.
 #include "common.cuh"
 
 namespace moe {
