@@ -78,14 +78,17 @@ __global__ void __launch_bounds__(256) topk_gate_kernel(const float* __restrict_
 
 constexpr int kSortedWarps = 8;
 
-// V slots per lane (see topk_token).
-template <int V, bool VEC, int KMAX>
+// V slots per lane (see topk_token).  KFIX > 0: k is that constant (the
+// common k = 8 gets its own instance); VEC implies E = 32 V.
+template <int V, bool VEC, int KMAX, int KFIX = 0>
 __global__ void __launch_bounds__(kSortedWarps * 32) topk_gate_sorted_kernel(
-    const float* __restrict__ scores, int64_t T, int E, int k, int32_t* __restrict__ topk_idx,
+    const float* __restrict__ scores, int64_t T, int E_, int k_, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w) {
   __shared__ unsigned long long s_list[kSortedWarps][V][32];
   __shared__ unsigned long long s_cand[kSortedWarps][32];
   pdl_enter();
+  const int E = VEC ? 32 * V : E_;
+  const int k = KFIX > 0 ? KFIX : k_;
   const int lane = threadIdx.x & 31;
   const int wib = threadIdx.x >> 5;
   const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -102,6 +105,9 @@ cudaError_t launch_sorted(const LaunchCtx& c, const float* scores, int64_t T, in
   const int64_t need = (T + kSortedWarps - 1) / kSortedWarps;
   const int64_t cap = (int64_t)c.num_sms * 8;
   const int blocks = (int)(need < cap ? need : cap);
+  if (k == 8)
+    return launch_pdl(topk_gate_sorted_kernel<V, VEC, 8, 8>, blocks, kSortedWarps * 32, 0,
+                      c.stream, scores, T, E, k, idx, w);
   if (k <= 8)
     return launch_pdl(topk_gate_sorted_kernel<V, VEC, 8>, blocks, kSortedWarps * 32, 0, c.stream,
                       scores, T, E, k, idx, w);
