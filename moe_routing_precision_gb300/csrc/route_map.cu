@@ -69,11 +69,16 @@ __device__ __forceinline__ int32_t warp_incl_scan(int32_t v, int lane) {
   return v;
 }
 
+// KFIX > 0: k is that constant; ALIGN1: align == 1 (the plain layout).  The
+// common k = 8 and the plain layout get instances of their own.
+template <int KFIX, bool ALIGN1>
 __global__ void __launch_bounds__(kRankThreads) route_rank_kernel(
-    const int32_t* __restrict__ idx, int64_t T, int E, int k, int chunk_tokens, int num_chunks,
-    int align, int64_t num_rows, const int32_t* __restrict__ hist, int32_t* __restrict__ counts,
+    const int32_t* __restrict__ idx, int64_t T, int E, int k_, int chunk_tokens, int num_chunks,
+    int align_, int64_t num_rows, const int32_t* __restrict__ hist, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ pos, int32_t* __restrict__ sorted_src,
     unsigned* err) {
+  const int k = KFIX > 0 ? KFIX : k_;
+  const int align = ALIGN1 ? 1 : align_;
   extern __shared__ int32_t smem[];
   int32_t* s_off = smem;                                     // [E] totals, then offsets
   int32_t* s_base = smem + E;                                // [E] copies in earlier chunks
@@ -263,13 +268,15 @@ cudaError_t launch_route_map_aligned(const LaunchCtx& c, const int32_t* idx, int
                               c.stream, idx, R, E, chunk_tokens * k, ws, c.err);
   if (st != cudaSuccess) return st;
   const size_t rank_smem = sizeof(int32_t) * (size_t)E * (2 + 2 * kRankWarps);
+  auto kern = k == 8 ? (align == 1 ? route_rank_kernel<8, true> : route_rank_kernel<8, false>)
+                     : (align == 1 ? route_rank_kernel<0, true> : route_rank_kernel<0, false>);
   if (rank_smem > 48 * 1024) {
-    st = allow_max_dynamic_smem(route_rank_kernel);
+    st = allow_max_dynamic_smem(kern);
     if (st != cudaSuccess) return st;
   }
-  return launch_pdl(route_rank_kernel, (unsigned)num_chunks, kRankThreads, rank_smem, c.stream,
-                    idx, T, E, k, chunk_tokens, (int)num_chunks, align, num_rows, ws, counts,
-                    offsets, pos, sorted_src, c.err);
+  return launch_pdl(kern, (unsigned)num_chunks, kRankThreads, rank_smem, c.stream, idx, T, E, k,
+                    chunk_tokens, (int)num_chunks, align, num_rows, ws, counts, offsets, pos,
+                    sorted_src, c.err);
 }
 
 cudaError_t launch_route_map(const LaunchCtx& c, const int32_t* idx, int64_t T, int E, int k,
