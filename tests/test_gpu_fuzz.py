@@ -3,6 +3,8 @@ against the oracle: shapes the fixed parity cases do not name (odd T, E not a
 power of two, every k, H across the kernel forms, all scale layouts, every
 FP4 group size, padded alignments, decode shapes on the fused and replicated
 paths, and the chained form).  Each case is small enough for the oracle to finish at once."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -14,7 +16,8 @@ from tests.parity_util import (assert_equal, assert_f32_bits_equal, assert_weigh
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-CASES = 24
+# MOE_FUZZ_CASES widens the sweep (each case has its own seed); 24 by default
+CASES = int(os.environ.get("MOE_FUZZ_CASES", "24"))
 
 
 @pytest.fixture(scope="module", autouse=True)
