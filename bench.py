@@ -990,7 +990,27 @@ def cast_options_workloads(L, dev, stream, sp, chk, flush, iters, peak):
         "ms": round(ms4, 4), "routed_tokens_per_s": round(R / (ms4 * 1e-3), 1),
         "algorithmic_bytes": b4, "GB_s": round(gbs4, 1), "frac_of_peak": round(gbs4 / peak, 4),
         "timing": "one batch after a 512 MB L2 flush, median"}
-    del q4, sf4
+    # the same with packed UE8M0 scales, row-major (the MX FP4 layout: one
+    # power-of-two exponent byte per 32 channels)
+    sf4b = torch.empty(R, H // 32, dtype=torch.uint8, device=dev)
+
+    def rec4b():
+        chk(L.moe_topk_gate(s.data_ptr(), T, E, k, idx.data_ptr(), wt.data_ptr(), 1, sp), "topk")
+        chk(L.moe_route_map(idx.data_ptr(), T, E, k, counts.data_ptr(), offsets.data_ptr(),
+                            pos.data_ptr(), src.data_ptr(), ws.data_ptr(), ws.numel(), sp), "route")
+        chk(L.moe_expand_cast_fp4(x.data_ptr(), T, H, k, pos.data_ptr(), None, R, q4.data_ptr(),
+                                  sf4b.data_ptr(), 6, 0, None, 0, 32, sp), "expand_fp4_ue8m0")
+
+    ms4b = timed(rec4b, max(3, iters // 2))
+    b4b = b4 - R * (H // 32) * 4 + R * (H // 32)
+    gbs4b = b4b / (ms4b * 1e-3) / 1e9
+    res["prefill_64k_fp4_group32_ue8m0"] = {
+        "op": "topk + route_map + expand_cast_fp4 (E2M1, 32-channel groups, packed UE8M0 "
+              "row-major scales)",
+        "ms": round(ms4b, 4), "routed_tokens_per_s": round(R / (ms4b * 1e-3), 1),
+        "algorithmic_bytes": b4b, "GB_s": round(gbs4b, 1), "frac_of_peak": round(gbs4b / peak, 4),
+        "timing": "one batch after a 512 MB L2 flush, median"}
+    del q4, sf4, sf4b
     res["prefill_64k_ue8m0_colmajor"] = {
         "op": "topk + route_map + expand_cast_fp8_ex (packed UE8M0, column-major)",
         "ms": round(ms, 4), "routed_tokens_per_s": round(R / (ms * 1e-3), 1),
