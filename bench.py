@@ -538,6 +538,8 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
     one(0)
     one(1)
     barrier()
+    clk = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clk.start()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
@@ -551,6 +553,7 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
         stream.wait_event(ev)
     b.record(stream)
     barrier()
+    e2e_clocks = clk.stop()
     ms = maxr(a.elapsed_time(b) / steps)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     # the host link on its own, for context: the largest output alone back to
@@ -606,7 +609,7 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
         os.sched_setaffinity(0, old_aff)
     return {"value": round(R * world / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
             "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "host_numa_node": node,
+            "host_numa_node": node, "clocks": e2e_clocks,
             "link": {"d2h_GB_s": round(d2h_gbs, 1), "h2d_GB_s": round(h2d_gbs, 1),
                      "copy_bound_ms_per_step": round(bound_ms, 3),
                      "both_directions_ms_per_step": round(both, 3),
