@@ -545,8 +545,12 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
     a.record(stream)
     for st in streams:
         st.wait_event(a)
+    step_ends = []
     for i in range(steps):
         one(i)
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(streams[i % 2])
+        step_ends.append(ev)
     for st in streams:
         ev = torch.cuda.Event()
         ev.record(st)
@@ -554,6 +558,7 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
     b.record(stream)
     barrier()
     e2e_clocks = clk.stop()
+    ends = [a.elapsed_time(ev) for ev in step_ends]
     ms = maxr(a.elapsed_time(b) / steps)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     # the host link on its own, for context: the largest output alone back to
@@ -610,6 +615,9 @@ def e2e_leg(args, L, dev, stream, sp, scores, x, idx, wt, counts, offsets, pos, 
     return {"value": round(R * world / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 3),
             "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "host_numa_node": node, "clocks": e2e_clocks,
+            "step_end_ms": [round(v, 2) for v in ends],
+            "step_ms_median": round(statistics.median(
+                [ends[0]] + [ends[i] - ends[i - 1] for i in range(1, len(ends))]), 3),
             "link": {"d2h_GB_s": round(d2h_gbs, 1), "h2d_GB_s": round(h2d_gbs, 1),
                      "copy_bound_ms_per_step": round(bound_ms, 3),
                      "both_directions_ms_per_step": round(both, 3),
