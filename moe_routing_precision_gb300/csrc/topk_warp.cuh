@@ -40,8 +40,8 @@ __device__ __forceinline__ float key_score(uint32_t key) {
 // Fallback (more than 32 candidates, i.e. heavy ties): each lane sorts its V
 // packed candidates and the rounds merge the 32 sorted lists, the winning lane
 // advancing its head from shared memory.  Sorting networks: the optimal
-// 19-comparator network for 8 inputs (Knuth, TAOCP vol. 3, 5.3.4) and the
-// 5-comparator one for 4.
+// 19-comparator network for 8 inputs (Knuth, TAOCP vol. 3, 5.3.4), the
+// 5-comparator one for 4, and odd-even transposition for 12 and 16.
 __device__ __forceinline__ void cex(unsigned long long& a, unsigned long long& b) {
   const unsigned long long hi = a > b ? a : b;
   const unsigned long long lo = a > b ? b : a;
@@ -51,7 +51,15 @@ __device__ __forceinline__ void cex(unsigned long long& a, unsigned long long& b
 
 template <int V>
 __device__ __forceinline__ void sort_desc(unsigned long long (&p)[V]) {
-  if constexpr (V == 2) {
+  if constexpr (V != 2 && V != 4 && V != 8) {
+    // other V (12, 16): odd-even transposition sort, V passes (only the
+    // heavy-tie fallback gets here)
+#pragma unroll
+    for (int pass = 0; pass < V; ++pass) {
+#pragma unroll
+      for (int i = pass & 1; i + 1 < V; i += 2) cex(p[i], p[i + 1]);
+    }
+  } else if constexpr (V == 2) {
     cex(p[0], p[1]);
   } else if constexpr (V == 4) {
     cex(p[0], p[1]); cex(p[2], p[3]); cex(p[0], p[2]); cex(p[1], p[3]); cex(p[1], p[2]);

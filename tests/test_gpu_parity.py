@@ -38,7 +38,9 @@ def np_(t):
 # ---------------------------------------------------------------- top-k
 
 TOPK_CASES = [(1, 16, 1), (31, 16, 2), (33, 32, 8), (64, 16, 2), (100, 64, 8), (257, 256, 8),
-              (50, 384, 8), (40, 1024, 32), (10, 17, 17), (129, 100, 5), (8, 1, 1)]
+              (50, 384, 8), (40, 1024, 32), (10, 17, 17), (129, 100, 5), (8, 1, 1),
+              (77, 8, 2), (45, 12, 3), (63, 16, 16), (3, 5, 5), (61, 512, 8), (37, 300, 6),
+              (19, 384, 32), (23, 500, 20), (29, 512, 32)]
 
 
 @pytest.mark.parametrize("T,E,k", TOPK_CASES)
@@ -50,6 +52,21 @@ def test_topk_gate_parity(T, E, k, ties):
     o_idx, o_w = oracle.topk_gate(s.numpy(), k)
     assert_equal(np_(idx), o_idx, "topk_idx")
     assert_weights_close(np_(w), o_w)
+
+
+@pytest.mark.parametrize("E", [8, 16, 384, 512])
+def test_topk_gate_special_values_other_forms(E):
+    """-0 and +0 tie (lower index first), +inf and -inf are ordinary values,
+    and an all-equal row gives experts 0..k-1, in the several-tokens-per-warp
+    form (E <= 16) and the forms for 256 < E <= 512."""
+    row0 = [-0.0, 0.0, float("inf"), -float("inf"), float("inf"), -5.0] + [-7.0] * (E - 6)
+    s = torch.tensor([row0, [1.0] * E, [-float("inf")] * E, row0[::-1]], dtype=torch.float32)
+    idx, _ = ops.topk_gate(s.to(DEV), 6, weights=False)
+    o_idx, _ = oracle.topk_gate(s.numpy(), 6, weights=False)
+    assert_equal(np_(idx), o_idx, "topk_idx special")
+    assert np_(idx)[1].tolist() == [0, 1, 2, 3, 4, 5]
+    _, w = ops.topk_gate(s[1:2].to(DEV), 6)      # the finite row's weights
+    assert np.allclose(np_(w), 1.0 / 6.0, rtol=4e-6, atol=0)
 
 
 def test_topk_gate_special_values():
