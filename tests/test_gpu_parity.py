@@ -54,6 +54,28 @@ def test_topk_gate_parity(T, E, k, ties):
     assert_weights_close(np_(w), o_w)
 
 
+TOPK_SWEEP_E = list(range(1, 41)) + [48, 63, 64, 65, 96, 127, 128, 129, 200, 255, 256, 257, 300,
+                                     383, 384, 385, 448, 511, 512, 513, 700, 1024]
+
+
+@pytest.mark.parametrize("E", TOPK_SWEEP_E)
+def test_topk_gate_every_form_over_e(E):
+    """Every top-k form (several tokens per warp for E <= 16, the rescan form
+    for 16 < E <= 32 and E > 512, the candidate filter with 2 to 16 slots per
+    lane in between, float4 rows where E is a multiple of 128) on seeded
+    scores with forced ties, a random k and a token count that leaves the
+    last warp's tokens partly empty."""
+    rng = np.random.default_rng(E)
+    k = int(rng.integers(1, min(E, 32) + 1))
+    T = int(rng.integers(1, 200)) * 2 + 1
+    inp = workloads.random_small(T, E, k, 128, seed=1000 + E, ties=bool(E % 2))
+    s = inp["scores"]
+    idx, w = ops.topk_gate(s.to(DEV), k)
+    o_idx, o_w = oracle.topk_gate(s.numpy(), k)
+    assert_equal(np_(idx), o_idx, f"topk_idx E={E} k={k}")
+    assert_weights_close(np_(w), o_w, f"topk_w E={E} k={k}")
+
+
 @pytest.mark.parametrize("E", [8, 16, 384, 512])
 def test_topk_gate_special_values_other_forms(E):
     """-0 and +0 tie (lower index first), +inf and -inf are ordinary values,
