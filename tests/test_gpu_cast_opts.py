@@ -222,15 +222,19 @@ def _swiglu_x(M, N, seed, scale=2.0):
     return (torch.randn(M, 2 * N, generator=g) * scale).to(torch.bfloat16)
 
 
-VARIANTS = {"plain": (None, False), "clamp": (2.5, False), "weight": (None, True),
-            "clamp_weight": (1.0, True)}
+# (clamp, per-row weights, clamp count): with the scale flags, every option
+# set the kernels specialise on (the count with and without a clamp)
+VARIANTS = {"plain": (None, False, False), "count": (None, False, True),
+            "weight": (None, True, False), "clamp": (2.5, False, False),
+            "clamp_count": (2.5, False, True), "clamp_weight": (1.0, True, False),
+            "clamp_weight_count": (1.0, True, True)}
 
 
 @pytest.mark.parametrize("flags", FLAGS)
 @pytest.mark.parametrize("variant", list(VARIANTS))
 @pytest.mark.parametrize("M,N", [(1, 128), (7, 384), (100, 2048), (1000, 256)])
 def test_swiglu_ex_parity(flags, variant, M, N):
-    clamp, with_w = VARIANTS[variant]
+    clamp, with_w, with_cnt = VARIANTS[variant]
     x = _swiglu_x(M, N, seed=M + N + flags)
     w = torch.rand(M, generator=torch.Generator().manual_seed(M)) if with_w else None
     ld = (M + 3) // 4 * 4 + 8 if flags & ops.SF_COLMAJOR else None
@@ -239,13 +243,14 @@ def test_swiglu_ex_parity(flags, variant, M, N):
     cnt = torch.full((1,), 5, dtype=torch.int64, device=DEV)    # counts are added
     q, _ = ops.swiglu_cast_fp8_ex(x.to(DEV), clamp=clamp,
                                   weights=None if w is None else w.to(DEV),
-                                  clamp_count=cnt, sf_flags=flags, sf_ld=ld, out_sf=sf)
+                                  clamp_count=cnt if with_cnt else None, sf_flags=flags,
+                                  sf_ld=ld, out_sf=sf)
     xb = oracle.bf16_bits(x)
     wn = None if w is None else w.numpy()
     o_q, o_sf, o_cnt = oracle.swiglu_cast_fp8_ex(xb, clamp=clamp, weights=wn, flags=flags, ld=ld)
     _, o_plain, _ = oracle.swiglu_cast_fp8_ex(xb, clamp=clamp, weights=wn)
     check_swiglu_opts(np_(q), np_(sf), o_q, o_sf, o_plain, flags, M)
-    assert int(cnt.item()) == 5 + o_cnt
+    assert int(cnt.item()) == 5 + (o_cnt if with_cnt else 0)
     if clamp is not None:
         assert o_cnt > 0
     # the sentinel outside the written entries survives

@@ -181,22 +181,29 @@ def test_expand_fp4_full_size_every_row(name):
 
 # ---------------------------------------------------------------- SwiGLU -> FP4
 
+# (clamp, per-row weights, clamp count)
+FP4_VARIANTS = {"plain": (None, False, False), "weight": (None, True, False),
+                "clamp": (1.0, False, False), "clamp_count": (1.0, False, True),
+                "clamp_weight_count": (1.0, True, True)}
+
+
 @pytest.mark.parametrize("group", [16, 32, 64, 128])
 @pytest.mark.parametrize("flags", [0, 1, 2, 7])
-@pytest.mark.parametrize("variant", ["plain", "clamp_weight"])
+@pytest.mark.parametrize("variant", list(FP4_VARIANTS))
 @pytest.mark.parametrize("M,N", [(1, 128), (7, 384), (100, 2048), (1000, 256)])
 def test_swiglu_fp4_parity(group, flags, variant, M, N):
     if N % group:
         pytest.skip("N not a multiple of the group")
     g = torch.Generator().manual_seed(M + N + group + flags)
     x = (torch.randn(M, 2 * N, generator=g) * 2.0).to(torch.bfloat16)
-    clamp = 1.0 if variant == "clamp_weight" else None
-    w = torch.rand(M, generator=g) if variant == "clamp_weight" else None
+    clamp, with_w, with_cnt = FP4_VARIANTS[variant]
+    w = torch.rand(M, generator=g) if with_w else None
     ld = (M + 3) // 4 * 4 + 8 if flags & ops.SF_COLMAJOR else None
     sf, ld = _sentinel_sf(M, N // group, flags, ld)
     cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
     q, _ = ops.swiglu_cast_fp4(x.to(DEV), group=group, clamp=clamp,
-                               weights=None if w is None else w.to(DEV), clamp_count=cnt,
+                               weights=None if w is None else w.to(DEV),
+                               clamp_count=cnt if with_cnt else None,
                                sf_flags=flags, sf_ld=ld, out_sf=sf)
     xb = oracle.bf16_bits(x)
     wn = None if w is None else w.numpy()
@@ -204,7 +211,7 @@ def test_swiglu_fp4_parity(group, flags, variant, M, N):
                                               flags=flags, ld=ld)
     _, o_plain, _ = oracle.swiglu_cast_fp4(xb, group=group, clamp=clamp, weights=wn)
     check_swiglu_opts(np_(q), np_(sf), o_q, o_sf, o_plain, flags, M, ordinal=fp4_ordinal)
-    assert int(cnt.item()) == o_cnt
+    assert int(cnt.item()) == (o_cnt if with_cnt else 0)
     assert ops.device_status() == 0
 
 
