@@ -315,3 +315,45 @@ def test_swiglu_clamp_fast_path_boundaries(fmt, clamp, count):
         check_swiglu_opts(np_(q), np_(sf), o_q, o_sf, o_sf, 0, M, ordinal=fp4_ordinal)
     assert o_cnt == expect
     assert int(cnt.item()) == (expect if count else 0)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "fp4"])
+@pytest.mark.parametrize("count", [True, False])
+def test_swiglu_variants_many_tiles_per_warp(fmt, count):
+    """Enough rows (8191 x 2x2048) that the instances on a persistent grid
+    (those with the clamp count) stride over five or six tiles per warp, with
+    a ragged last stride, and the others take the grid of one tile per warp:
+    clamp 7 on N(0, 2^2) values (about 0.07 % of the (gate, up) pairs exceed
+    it, so about a third of the warp tiles clamp and count and the rest take
+    the skip test's fast path), per-row weights, packed UE8M0 column-major
+    scales.
+    Every row against the oracle, and the count exact: each tile counted once."""
+    M, N = 8191, 2048
+    x = _swiglu_x(M, N, seed=17)
+    w = torch.rand(M, generator=torch.Generator().manual_seed(18))
+    flags = 7
+    cnt = torch.full((1,), 3, dtype=torch.int64, device=DEV)
+    xb = oracle.bf16_bits(x)
+    if fmt == "fp8":
+        G = N // 128
+        sf, ld = _sentinel_sf(M, G, flags, (M + 3) // 4 * 4)
+        q, _ = ops.swiglu_cast_fp8_ex(x.to(DEV), clamp=7.0, weights=w.to(DEV),
+                                      clamp_count=cnt if count else None, sf_flags=flags,
+                                      sf_ld=ld, out_sf=sf)
+        o_q, o_sf, o_cnt = oracle.swiglu_cast_fp8_ex(xb, clamp=7.0, weights=w.numpy(),
+                                                     flags=flags, ld=ld)
+        _, o_plain, _ = oracle.swiglu_cast_fp8_ex(xb, clamp=7.0, weights=w.numpy())
+        check_swiglu_opts(np_(q), np_(sf), o_q, o_sf, o_plain, flags, M)
+    else:
+        G = N // 32
+        sf, ld = _sentinel_sf(M, G, flags, (M + 3) // 4 * 4)
+        q, _ = ops.swiglu_cast_fp4(x.to(DEV), group=32, clamp=7.0, weights=w.to(DEV),
+                                   clamp_count=cnt if count else None, sf_flags=flags,
+                                   sf_ld=ld, out_sf=sf)
+        o_q, o_sf, o_cnt = oracle.swiglu_cast_fp4(xb, group=32, clamp=7.0, weights=w.numpy(),
+                                                  flags=flags, ld=ld)
+        _, o_plain, _ = oracle.swiglu_cast_fp4(xb, group=32, clamp=7.0, weights=w.numpy())
+        check_swiglu_opts(np_(q), np_(sf), o_q, o_sf, o_plain, flags, M, ordinal=fp4_ordinal)
+    assert 1000 < o_cnt < 100000
+    assert int(cnt.item()) == 3 + (o_cnt if count else 0)
+    assert ops.device_status() == 0
