@@ -76,6 +76,31 @@ def test_topk_gate_every_form_over_e(E):
     assert_weights_close(np_(w), o_w, f"topk_w E={E} k={k}")
 
 
+# (E, k) for every top-k form; T is 2.5 times the tokens one pass of the
+# form's capped grid covers (1216 blocks: 32 tokens each for E <= 8, 16 for
+# E <= 16, 8 otherwise), so each warp takes two or three tokens and the last
+# pass is ragged
+TOPK_STRIDE_CASES = [(8, 2), (16, 4), (32, 8), (64, 6), (128, 8), (200, 5), (256, 4),
+                     (384, 8), (512, 8), (1024, 8)]
+
+
+@pytest.mark.parametrize("E,k", TOPK_STRIDE_CASES)
+@pytest.mark.parametrize("ties", [False, True])
+def test_topk_gate_grid_stride(E, k, ties):
+    """Every top-k form with more tokens than its grid covers in one pass,
+    random and heavily tied scores (the tied rows take the candidate filter's
+    sorted-merge fallback where it has one)."""
+    per_block = 32 if E <= 8 else 16 if E <= 16 else 8
+    T = 1216 * per_block * 5 // 2 + 3
+    inp = workloads.random_small(T, E, k, 128, seed=E * 31 + k, ties=ties)
+    s = inp["scores"]
+    idx, w = ops.topk_gate(s.to(DEV), k)
+    o_idx, o_w = oracle.topk_gate(s.numpy(), k)
+    assert_equal(np_(idx), o_idx, f"topk_idx E={E} k={k} T={T}")
+    assert_weights_close(np_(w), o_w, f"topk_w E={E} k={k} T={T}")
+    assert ops.device_status() == 0
+
+
 @pytest.mark.parametrize("E", [8, 16, 384, 512])
 def test_topk_gate_special_values_other_forms(E):
     """-0 and +0 tie (lower index first), +inf and -inf are ordinary values,
