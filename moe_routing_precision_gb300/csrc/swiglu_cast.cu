@@ -3,7 +3,10 @@
 // TileKernels article (itsolotime.com), section 3.3: in f32,
 // val_l / (1 + exp(-val_l)) * val_r with val_l from the left (gate) half and
 // val_r from the right (up) half of each row, then per-group absmax -> scale
-// -> cast in the same kernel (plain form: no clamp, no top-k weight).
+// -> cast in the same kernel.  The section's variants (the clamp, the top-k
+// weight, the clamp count) and the scale options are instances of the same
+// kernels, one per option set (kOptW ... kOptK); the FP4 E2M1 output shares
+// the loop (swiglu_cast_fp4_kernel).
 //
 // Work unit: one (row, 128-channel group) per aligned 8-lane subgroup; each
 // lane reads 16 gate and 16 up values (four 16-byte loads) and writes one
@@ -36,7 +39,7 @@ __host__ __device__ constexpr bool ext_persistent(int opt) {
   return ((kPersistentOpts >> opt) & 1u) != 0;
 }
 
-// kGridNote: the grid is not persistent, but for the instances that count
+// kGridNote: the grid is not persistent, except for the instances that count
 // clamped values (K).  One warp per tile of units, so the CTAs in flight at
 // any moment cover a compact run of consecutive rows.  Measured on GB300
 // (65536 rows of 2 x 2048, after an L2 flush / back to back): E4M3 0.929 /
